@@ -1,0 +1,552 @@
+#!/usr/bin/env python
+"""Benchmark of the block-paged KV-cache hot path on GB300.
+
+One step = one pass of the path over the decode-sized gather batch (fp16 pool of
+10000 pages x 16 slots x 32 heads x 128 dims, 64 sequences of U[512, 4096] tokens,
+uint32 block tables from a shuffled free list): hp_plan (device validation of the
+descriptor + ragged prefix sums) then hp_gather_planned (the page-span copy), both
+through the C ABI.  The metric is effective HBM GB/s (algorithmic bytes read and
+written per step / step time).
+
+Printed: one JSON line (rank 0) with the headline value, the roofline of the copy
+kernel, the CPU oracle timed on a bounded sample, an end-to-end figure through host
+buffers, and per-operation measurements of the other rows of the path (append,
+prefix sharing, dequantising gather, per-lane layout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+Under torchrun each rank runs its own replica of the batch on its own GPU (no
+collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (bytes read+written) of paged gather/scatter, % of roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+COPY_KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_hp_gb300", "csrc", "hp_copy.cu")
+
+
+# ----------------------------------------------------------------------------- helpers
+def peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, units_now):
+    """DRAM bytes per launch from a committed ncu summary, scaled to this launch's
+    units, or None when the summary is absent or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel_key]
+    except Exception:
+        return None
+    if rec.get("source_sha256_16") != source_hash(COPY_KERNEL_SOURCE):
+        return None
+    return rec["dram_bytes_per_unit"] * units_now
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 7:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[3:7]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def idx_tensor(a, dev):
+    import torch
+    a = np.ascontiguousarray(a)
+    v = a.view(np.int32) if a.dtype == np.uint32 else a.astype(np.uint64).view(np.int64)
+    return torch.from_numpy(v.copy()).to(dev)
+
+
+def gather_bytes(w, lens=None):
+    """Algorithmic bytes of one gather of the batch: every valid row read once and
+    written once, plus one block-table entry per page span."""
+    lens = (w.lens if lens is None else lens).astype(np.int64)
+    T = int(lens.sum())
+    spans = int((-(-lens // w.page_size)).sum())
+    ib = 4 if w.index_dtype == np.uint32 else 8
+    return 2 * T * w.row_bytes + spans * ib, spans
+
+
+def validate_bytes(w):
+    ib = 4 if w.index_dtype == np.uint32 else 8
+    return len(w.table) * ib + (2 * w.num_seqs + 1) * ib
+
+
+# ----------------------------------------------------------------------------- device arm
+class GatherStep:
+    """Resident device buffers of one gather batch and the two C-ABI calls of a step."""
+
+    def __init__(self, w, dev, hp, inputs):
+        import torch
+        self.w, self.hp = w, hp
+        self.pool = inputs.device_pool(w, dev)
+        self.table = idx_tensor(w.table, dev)
+        self.seq_ptr = idx_tensor(w.seq_ptr, dev)
+        self.lens = idx_tensor(w.lens, dev)
+        self.scales = inputs.device_scales(w, dev) if w.scales_seed is not None else None
+        self.dequant = self.scales is not None
+        self.desc = hp.PagedDesc(self.pool, self.table, self.seq_ptr, self.lens,
+                                 num_pages=w.num_pages, page_size=w.page_size,
+                                 num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype,
+                                 index_type=0 if w.index_dtype == np.uint32 else 1,
+                                 scales=self.scales, flags=hp.HAS_QUANT if self.dequant else 0)
+        self.ws = hp.workspace_for(self.desc, dev)
+        self.T = w.total_tokens
+        ob = self.T * w.num_heads * w.head_dim * (2 if self.dequant else inputs.ELEM_BYTES[w.dtype])
+        self.out = torch.empty(ob, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def plan(self, stream):
+        rc = self.hp.hp_plan(self.desc, self.T, self.ws, self.status, stream=stream)
+        assert rc == 0, self.hp.status_name(rc)
+
+    def copy(self, stream):
+        f = self.hp.hp_gather_dequant_planned if self.dequant else self.hp.hp_gather_planned
+        rc = f(self.desc, self.out, self.ws, self.status, stream=stream)
+        assert rc == 0, self.hp.status_name(rc)
+
+    def check_status(self):
+        st = int(self.status.item())
+        assert st == 0, self.hp.status_name(st)
+
+
+def time_steps(step, steps, warmup, stream, dist=None):
+    """Warm-up, then `steps` timed steps bracketed by barrier + synchronize.
+    Returns (step ms list, copy-kernel ms list, wall seconds of the timed region)."""
+    import torch
+    for _ in range(warmup):
+        step.plan(stream)
+        step.copy(stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        step.plan(stream)
+        e1.record(stream)
+        step.copy(stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    step.check_status()
+    return ([a.elapsed_time(c) for a, b, c in ev], [b.elapsed_time(c) for a, b, c in ev], wall)
+
+
+def e2e_gather(w, dev, hp, inputs, steps):
+    """The same step through host buffers: every step copies the pool and index
+    buffers from pinned host memory, gathers through the C ABI, and reads the gathered
+    tensor back to pinned host memory."""
+    import torch
+    stream = torch.cuda.current_stream()
+    pool_dev = inputs.device_pool(w, dev)
+    h_pool = torch.empty(pool_dev.shape, dtype=torch.uint8, pin_memory=True)
+    h_pool.copy_(pool_dev)
+    del pool_dev
+    host_idx = [torch.from_numpy(np.ascontiguousarray(a).view(np.int32).copy()).pin_memory()
+                for a in (w.table, w.seq_ptr, w.lens)]
+    d_pool = torch.empty(h_pool.shape, dtype=torch.uint8, device=dev)
+    d_idx = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_idx]
+    T = w.total_tokens
+    h_out = torch.empty(T * w.row_bytes, dtype=torch.uint8, pin_memory=True)
+    d_out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)
+    desc = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[2], num_pages=w.num_pages,
+                        page_size=w.page_size, num_heads=w.num_heads, head_dim=w.head_dim,
+                        dtype=w.dtype, index_type=0)
+    ws = hp.workspace_for(desc, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def one():
+        d_pool.copy_(h_pool, non_blocking=True)
+        for d, h in zip(d_idx, host_idx):
+            d.copy_(h, non_blocking=True)
+        rc = hp.hp_gather(desc, d_out, T, ws, status)
+        assert rc == 0
+        h_out.copy_(d_out, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ms = e0.elapsed_time(e1) / steps
+    h2d = h_pool.numel() + sum(h.numel() * h.element_size() for h in host_idx)
+    return ms, h2d, h_out.numel()
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def _oracle_desc_for(w, host_pool, seqs_upto, tokens_cap, oracle_mod):
+    lens = w.lens.astype(np.int64)[:seqs_upto].copy()
+    if tokens_cap is not None:
+        c = np.cumsum(lens)
+        k = int(np.searchsorted(c, tokens_cap))
+        lens = lens[:k + 1].copy()
+        prev = int(c[k - 1]) if k > 0 else 0
+        lens[-1] = max(1, min(int(lens[-1]), tokens_cap - prev))
+    n = len(lens)
+    sp = w.seq_ptr[:n + 1].astype(w.index_dtype)
+    table = w.table[:int(sp[-1])]
+    d = oracle_mod.Desc(host_pool, table, sp, lens.astype(w.index_dtype), num_pages=w.num_pages,
+                        page_size=w.page_size, num_heads=w.num_heads, head_dim=w.head_dim,
+                        dtype=w.dtype, index_type=0 if w.index_dtype == np.uint32 else 1)
+    return d, lens
+
+
+def time_oracle(w, host_pool, oracle_mod, budget_s, max_tokens=None):
+    """Oracle gather on a prefix of the batch sized to take about budget_s seconds."""
+    tokens = 256
+    while True:
+        d, lens = _oracle_desc_for(w, host_pool, w.num_seqs, tokens, oracle_mod)
+        t0 = time.perf_counter()
+        d.gather()
+        dt = time.perf_counter() - t0
+        T = int(lens.sum())
+        if dt >= budget_s * 0.5 or T >= w.total_tokens or (max_tokens and T >= max_tokens):
+            break
+        scale = max(2.0, min(16.0, budget_s / max(dt, 1e-4)))
+        tokens = int(min(w.total_tokens, tokens * scale))
+        if max_tokens:
+            tokens = min(tokens, max_tokens)
+    b, _ = gather_bytes(w, lens)
+    return b / dt / 1e9, dt, T, lens
+
+
+# ----------------------------------------------------------------------------- ops
+def ops_measurements(dev, hp, inputs, peak, reps=20):
+    """The other rows of the path at their own configurations (bytes as in
+    gather_bytes; medians over reps, inputs larger than L2 except where noted)."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+
+    def med_ms(fn, n=reps, warm=3):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def entry(bytes_, ms, **kw):
+        gbps = bytes_ / (ms * 1e-3) / 1e9
+        return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
+
+    # tiny prefix-sharing gather: latency
+    w = inputs.tiny_prefix_gather()
+    st = GatherStep(w, dev, hp, inputs)
+    ms = med_ms(lambda: (st.plan(stream), st.copy(stream)))
+    out["tiny_prefix_gather"] = {"us_per_step": round(ms * 1e3, 2)}
+    del st
+
+    # prefix sharing at scale
+    w = inputs.config("prefix_sharing")
+    st = GatherStep(w, dev, hp, inputs)
+    b, spans = gather_bytes(w)
+    ms = med_ms(lambda: st.copy(stream))
+    out["prefix_sharing_gather"] = entry(b, ms, note="logical bytes; the 128 shared pages are "
+                                         "read from L2 after their first use")
+    st.check_status()
+    del st
+
+    # int8 pool, per-slot scales -> bf16
+    w = inputs.config("quantized_pool")
+    st = GatherStep(w, dev, hp, inputs)
+    T = w.total_tokens
+    spans = int((-(-w.lens.astype(np.int64) // w.page_size)).sum())
+    b = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
+    ms = med_ms(lambda: st.copy(stream), n=10)
+    out["quantized_pool_dequant_gather"] = entry(b, ms)
+    st.check_status()
+    del st
+    torch.cuda.empty_cache()
+
+    # decode step: append one row per sequence, then gather the grown batch
+    w = inputs.config("decode_append")
+    pool = inputs.device_pool(w, dev)
+    table, sp = idx_tensor(w.table, dev), idx_tensor(w.seq_ptr, dev)
+    before, after = idx_tensor(w.lens_before, dev), idx_tensor(w.lens, dev)
+    new_ptr = idx_tensor(w.new_ptr, dev)
+    new = inputs.device_new_rows(w, dev)
+    kw = dict(num_pages=w.num_pages, page_size=w.page_size, num_heads=w.num_heads,
+              head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+    d_app = hp.PagedDesc(pool, table, sp, before, **kw)
+    ws = hp.workspace_for(d_app, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms = med_ms(lambda: hp.hp_scatter_append(d_app, new, new_ptr, w.total_new, ws, status), n=50)
+    out["decode_append_step"] = {"us_per_step": round(ms * 1e3, 2), "rows": w.total_new,
+                                 "bytes": 2 * w.total_new * w.row_bytes}
+    d_g = hp.PagedDesc(pool, table, sp, after, **kw)
+    T = w.total_tokens
+    o = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)
+    assert hp.hp_plan(d_g, T, ws, status) == 0
+    b, _ = gather_bytes(w)
+    ms = med_ms(lambda: hp.hp_gather_planned(d_g, o, ws, status), n=10)
+    out["decode_append_gather"] = entry(b, ms)
+    # bulk (prefill-style) scatter of every row of the batch into its pages
+    zeros = torch.zeros(w.num_seqs, dtype=torch.int32, device=dev)
+    d_bulk = hp.PagedDesc(pool, table, sp, zeros, **kw)
+    np_bulk = idx_tensor(np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))]).astype(np.uint32), dev)
+    assert hp.hp_append_plan(d_bulk, np_bulk, T, ws, status) == 0
+    ms = med_ms(lambda: hp.hp_scatter_append_planned(d_bulk, o, np_bulk, ws, status), n=10)
+    out["bulk_scatter_append"] = entry(b, ms)
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
+    del pool, o, new
+    torch.cuda.empty_cache()
+
+    # per-lane [N, B, H_kv, P, d] layout
+    lw = inputs.lane_synthetic()
+    g = torch.Generator(device=dev)
+    g.manual_seed(lw.seed)
+    lpool = torch.randn(lw.pool_shape, generator=g, device=dev).to(torch.bfloat16)
+    lt = torch.from_numpy(lw.table.view(np.int64).copy()).to(dev)
+    lo = torch.empty((lw.batch, lw.kv_heads, lw.n, lw.width), dtype=torch.bfloat16, device=dev)
+    ms = med_ms(lambda: hp.hp_lane_gather(lpool, lt, lw.capacity, lw.page_tokens, lw.batch,
+                                          lw.kv_heads, lw.width, "bf16", lw.n, lo, status))
+    out["lane_gather"] = entry(2 * lw.lanes * lw.n * lw.width * 2 + lw.pages * 8, ms)
+    lnew = torch.randn((lw.batch, lw.kv_heads, 1, lw.width), device=dev).to(torch.bfloat16)
+    ms = med_ms(lambda: hp.hp_lane_append(lpool, lt, lw.capacity, lw.page_tokens, lw.batch,
+                                          lw.kv_heads, lw.width, "bf16", lw.n, 1, lnew, status),
+                n=50)
+    out["lane_append_step"] = {"us_per_step": round(ms * 1e3, 2)}
+    assert int(status.item()) == 0
+    return out
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-ops", action="store_true", help="skip the per-operation measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from paged_kv_cache_hp_gb300 import inputs
+    w = inputs.config("decode_gather")
+    T = w.total_tokens
+    step_bytes_copy, spans = gather_bytes(w)
+    step_bytes = step_bytes_copy + validate_bytes(w)
+    config = {"workload": "decode_gather", "num_pages": w.num_pages, "page_size": w.page_size,
+              "num_heads": w.num_heads, "head_dim": w.head_dim, "pool_dtype": w.dtype,
+              "num_seqs": w.num_seqs, "total_tokens": T, "index": "u32",
+              "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (%.2f GB per step)"
+              % (step_bytes / 1e9), "parallelism": "replicas x%d" % args.gpus}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        host_pool = inputs.host_pool(w) if w.pool_bytes <= (64 << 20) else None
+        if host_pool is None:
+            import torch
+            host_pool = inputs.device_pool(w, "cpu", force_device_rng=True).numpy() \
+                if not torch.cuda.is_available() else inputs.device_pool(w, "cuda").cpu().numpy()
+        per_step = max(0.002, 120.0 / (args.steps + args.warmup))
+        gbps, dt, Ts, lens = time_oracle(w, host_pool, oracle, per_step)
+        d, _ = _oracle_desc_for(w, host_pool, w.num_seqs, int(lens.sum()), oracle)
+        for _ in range(args.warmup):
+            d.gather()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            d.gather()
+        el = time.perf_counter() - t0
+        b, _ = gather_bytes(w, lens)
+        value = b * args.steps / el / 1e9
+        sample = "oracle gather of the first %d tokens of the batch per step" % int(lens.sum())
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 3),
+                          "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": w.dtype, "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1,
+                                           "kind": "oracle", "sample": sample},
+                          "e2e": {"value": round(value, 3), "unit": UNIT,
+                                  "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    from paged_kv_cache_hp_gb300 import build, hp
+    build.build()
+    hp.lib()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = "cuda:%d" % (local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    step = GatherStep(w, dev, hp, inputs)
+    with ClockSampler(local) as clk:
+        step_ms, copy_ms, wall = time_steps(step, args.steps, args.warmup, stream, dist)
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = peak_hbm()
+    copy_mean = statistics.mean(copy_ms)
+    achieved = step_bytes_copy / (copy_mean * 1e-3) / 1e9
+
+    # a same-bytes device-to-device copy as the practical ceiling
+    a = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)
+    bb = torch.empty_like(a)
+    for _ in range(3):
+        bb.copy_(a)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(20):
+        bb.copy_(a)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    d2d_gbps = 2 * a.numel() / (e0.elapsed_time(e1) / 20 * 1e-3) / 1e9
+    del a, bb
+
+    traffic = recorded_traffic("gather_decode_gather", spans)
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; pool ~N(0,1) drawn on the device)", "config": config,
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic is None else int(traffic),
+                     "kernel": "copy_kernel<gather> (hp_gather_planned)",
+                     "peak_kind": peak_kind + " (hbm_gbs, copy)",
+                     "algorithmic_bytes_per_launch": step_bytes_copy,
+                     "launch_ms_mean": round(copy_mean, 4),
+                     "frac_of_nominal_8000": round(achieved / 8000.0, 4),
+                     "d2d_copy_same_bytes_gbps": round(d2d_gbps, 1)},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_e2e:
+        ms, h2d, d2h = e2e_gather(w, dev, hp, inputs, steps=5)
+        result["e2e"] = {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "ms_per_step": round(ms, 3)}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        host_pool = step.pool.cpu().numpy()
+        gbps, dt, Ts, lens = time_oracle(w, host_pool, oracle, budget_s=12.0)
+        result["cpu_baseline"] = {"value": round(gbps, 3), "unit": UNIT, "cores": 1,
+                                  "kind": "oracle",
+                                  "sample": "oracle gather (one thread) of the first %d of %d "
+                                            "tokens, %.1f s" % (Ts, T, dt)}
+    if rank == 0 and not args.no_ops:
+        del step
+        torch.cuda.empty_cache()
+        result["ops"] = ops_measurements(dev, hp, inputs, peak)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+if __name__ == "__main__":
+    main()

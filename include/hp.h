@@ -1,0 +1,302 @@
+/*
+ * hp.h -- C ABI of the block-paged KV-cache library (libhp.so) for GB300 (sm_103a).
+ *
+ * The library implements the data path of the block-paged layout defined in
+ * "Block-Paged Layout -- Hurray Format Specification" (cited below as [HF]) and
+ * of the per-lane page layout in "Keep token order across cache pages"
+ * (practical-ch20-paged-kv-layout, cited as [CH]):
+ *
+ *   - a planner/validator for a block-paged descriptor,
+ *   - a gather of a ragged batch into the logical [total_tokens, H, D] tensor,
+ *   - the inverse scatter that appends new K/V rows into their pages,
+ *   - a dequantising gather of an int8 pool with per-page-slot fp32 scales,
+ *   - gather and append for the [N, B, H_kv, P, d] per-lane layout.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All functions return an int status: HP_OK (0) or a negative hp_status code.
+ *   hp_status_string() names it.  Nothing aborts or prints.
+ * - Pointers named d_* or described as "device" point to GPU memory of the
+ *   current CUDA device; pointers described as "host" point to CPU memory.
+ *   The caller owns every buffer.  The library allocates no device memory and
+ *   keeps no state between calls; it is safe to call from several host threads
+ *   on different streams.
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *   stream.  Functions marked ASYNC only enqueue work on `stream` and return
+ *   once it is enqueued; functions marked SYNC wait for their own work.
+ * - Errors the host can see (bad descriptor fields, null or misaligned
+ *   pointers, a short workspace) are returned before anything is enqueued and
+ *   leave every output untouched.  Errors that depend on device-resident data
+ *   (seq_ptr, block_table, token counts) are found on the device: the ASYNC
+ *   operations then write nothing to their outputs and store the status code
+ *   in *d_status (an optional caller-owned device int).  When d_status is
+ *   non-NULL the operation first stores HP_OK there, then the first error
+ *   found, if any.  In permissive mode (HP_PERMISSIVE) the storage invariants
+ *   are not validated; a row whose lookup would leave its slice, the table or
+ *   the pool is then skipped (its output row is left as it was) and one of the
+ *   codes of the skipped rows is stored in *d_status.  No device code traps,
+ *   asserts or waits on another agent.
+ * - Launch errors reported by the CUDA runtime map to HP_ERR_CUDA.
+ */
+#ifndef HP_H
+#define HP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+typedef enum hp_status {
+    HP_OK = 0,
+    /* structural descriptor checks, always made on the host, in this order */
+    HP_ERR_RANK = -1,           /* [HF] Description: rank is not 3                          */
+    HP_ERR_PAGED_AXIS = -2,     /* [HF] Logical Shape, invariant (6): paged_axis is not 0    */
+    HP_ERR_SHARD = -3,          /* [HF] Sharding: a shard descriptor is attached              */
+    HP_ERR_INDEX_TYPE = -4,     /* [HF] Additional Descriptor Fields: index type not 0x00/0x01,
+                                   or uint32 with more than 2^32 pages / 2^32-1 table entries */
+    HP_ERR_DTYPE = -5,          /* unknown element type (or not int8 for a dequantising gather) */
+    HP_ERR_ZERO_DIM = -6,       /* page_size, num_heads or head_dim is 0                      */
+    HP_ERR_SCALES = -7,         /* [HF] Scale-buffer size: HP_HAS_QUANT without
+                                   num_pages*page_size fp32 scales                            */
+    HP_ERR_NULL = -8,           /* a required buffer pointer is NULL                          */
+    HP_ERR_ALIGN = -9,          /* [HF] Alignment: a descriptor buffer is not 64-byte aligned  */
+    HP_ERR_OVERFLOW = -10,      /* [HF] invariant (4): the pool's byte size exceeds 2^64      */
+    /* storage invariants, checked on the device, in this order */
+    HP_ERR_SEQ_PTR_START = -11, /* [HF] invariant (1): seq_ptr[0] != 0                        */
+    HP_ERR_SEQ_PTR_ORDER = -12, /* [HF] invariant (2): seq_ptr[s] > seq_ptr[s+1]               */
+    HP_ERR_SEQ_PTR_END = -13,   /* [HF] invariant (1): seq_ptr[num_seqs] != table_len          */
+    HP_ERR_PAGE_ID = -14,       /* [HF] invariant (3): block_table[k] >= num_pages             */
+    HP_ERR_LEN = -15,           /* [HF] Partial trailing page: seq_lens[s] exceeds the slots of
+                                   the sequence's slice, (seq_ptr[s+1]-seq_ptr[s])*page_size   */
+    /* append checks, after the storage invariants */
+    HP_ERR_NEW_PTR_START = -16, /* new_ptr[0] != 0                                            */
+    HP_ERR_NEW_PTR_ORDER = -17, /* new_ptr[s] > new_ptr[s+1]                                  */
+    HP_ERR_NEW_PTR_END = -18,   /* new_ptr[num_seqs] != total_new                             */
+    HP_ERR_CAPACITY = -19,      /* seq_lens[s] + new rows exceed the slice's slots            */
+    /* argument checks */
+    HP_ERR_OUT_SIZE = -20,      /* out_tokens != sum of seq_lens (or the sum exceeds 2^64)     */
+    /* per-lane layout, [CH] PagedKvLayout::new and the live length */
+    HP_ERR_ZERO_CAPACITY = -21,
+    HP_ERR_ZERO_PAGE_SIZE = -22,
+    HP_ERR_LANE_OVERFLOW = -23, /* ceil(C/P)*P or a buffer size exceeds 2^64                  */
+    HP_ERR_PAGE_COUNT = -24,    /* table length != ceil(C/P)                                  */
+    HP_ERR_PHYSICAL_PAGE = -25, /* a table entry >= ceil(C/P)                                 */
+    HP_ERR_ALIASED_PAGE = -26,  /* a table entry repeats                                      */
+    HP_ERR_LENGTH = -27,        /* live length (plus appended rows) exceeds the capacity      */
+    HP_ERR_ALLOCATION_FAILED = -28, /* host scratch for the lane table check unavailable     */
+    /* library */
+    HP_ERR_WORKSPACE = -29,     /* workspace NULL, misaligned (256 B) or smaller than required */
+    HP_ERR_ARG = -30,           /* another argument is invalid (see the function)            */
+    HP_ERR_CUDA = -31           /* the CUDA runtime rejected a launch or a copy               */
+} hp_status;
+
+/* Name of a status code ("HP_OK", "HP_ERR_RANK", ...); "HP_ERR_UNKNOWN" otherwise. */
+const char* hp_status_string(int status);
+
+/* --------------------------------------------------------------- descriptor */
+typedef enum hp_dtype {     /* element type of the page pool */
+    HP_F32 = 0, HP_F16 = 1, HP_BF16 = 2, HP_I8 = 3, HP_U8 = 4, HP_F64 = 5
+} hp_dtype;
+
+typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of seq_ptr,
+                                seq_lens and an append's new_ptr */
+    HP_IDX_U32 = 0x00, HP_IDX_U64 = 0x01
+} hp_index_type;
+
+#define HP_PERMISSIVE 0x1u /* [HF] Storage Invariants: a reader in permissive mode does not
+                              reject descriptors that violate invariants (1)-(3)          */
+#define HP_HAS_QUANT 0x2u  /* [HF] Buffer Table: quantisation parameters present          */
+
+/*
+ * A block-paged descriptor ([HF] Buffer Table, Additional Descriptor Fields):
+ * one batch of one {kv_role, layer_index}, a static snapshot.
+ *
+ *   page_pool    device, [num_pages, page_size, num_heads, head_dim] elements of
+ *                `dtype`, row-major; num_pages*page_size*num_heads*head_dim*width
+ *                bytes ([HF] invariant (4)).  Written only by hp_scatter_append.
+ *   block_table  device, table_len entries of the index type: physical page IDs,
+ *                the per-sequence slices concatenated.  May be NULL iff
+ *                table_len == 0 ([HF] Buffer Table, empty batch).
+ *   seq_ptr      device, num_seqs+1 entries: sequence s owns block_table
+ *                [seq_ptr[s], seq_ptr[s+1]) ([HF] Description, CSR-style).
+ *   seq_lens     device, num_seqs entries: the token count of each sequence (the
+ *                count that bounds a reader, [HF] Partial trailing page).  May be
+ *                NULL iff num_seqs == 0.
+ *   scales       device, scales_len fp32 per-page-slot scales, required iff
+ *                flags has HP_HAS_QUANT; scales_len must be num_pages*page_size
+ *                ([HF] Per-page-slot parameters, Scale-buffer size).
+ *
+ * Every present buffer must be 64-byte aligned ([HF] Alignment).
+ * rank must be 3, paged_axis 0 and has_shard 0 ([HF] Description, Logical
+ * Shape, Sharding).  Aliased page IDs (prefix sharing) are allowed and never
+ * checked ([HF] Prefix Sharing).
+ */
+typedef struct hp_paged_desc {
+    uint32_t rank;
+    uint32_t paged_axis;
+    uint32_t has_shard;
+    uint32_t flags;        /* HP_PERMISSIVE | HP_HAS_QUANT */
+    uint32_t dtype;        /* hp_dtype */
+    uint32_t index_type;   /* hp_index_type */
+    uint64_t num_pages;
+    uint64_t page_size;
+    uint64_t num_heads;
+    uint64_t head_dim;
+    uint64_t num_seqs;
+    uint64_t table_len;
+    uint64_t scales_len;
+    const void* page_pool;
+    const void* block_table;
+    const void* seq_ptr;
+    const void* seq_lens;
+    const float* scales;
+} hp_paged_desc;
+
+/* ----------------------------------------------------------------- planning */
+/*
+ * Bytes of device workspace the planned operations need for `desc`
+ * (256 + 2 * 256-rounded 8*(num_seqs+1)).  Host only; no GPU work.
+ * The workspace must be 256-byte aligned.  Returns HP_ERR_NULL if an argument
+ * is NULL, HP_ERR_OVERFLOW if the size does not fit in 64 bits.
+ */
+int hp_workspace_bytes(const hp_paged_desc* desc, uint64_t* bytes);
+
+/*
+ * SYNC.  Validate a block-paged descriptor the way a conforming reader does
+ * ([HF] Storage Invariants): the structural checks on the host, then -- unless
+ * HP_PERMISSIVE -- invariants (1)-(3) and the token-count rule on the device
+ * (one pass over seq_ptr/seq_lens and one over block_table), with the first
+ * failing rule in the order of hp_status and, within it, the first failing
+ * index.  Returns that rule's code (HP_OK if none) and stores the index in
+ * *first_bad (host, may be NULL; 0 for structural errors).  Uses `workspace`
+ * (hp_workspace_bytes) as scratch.  Waits for `stream`.
+ */
+int hp_validate(const hp_paged_desc* desc, void* workspace, uint64_t workspace_bytes,
+                uint64_t* first_bad, void* stream);
+
+/*
+ * ASYNC.  Plan a gather: validate as hp_validate does (without waiting), check
+ * that out_tokens equals the sum of seq_lens ([HF] Logical Shape: total_tokens
+ * is that sum), and store in `workspace` the exclusive prefix sums of the token
+ * counts (each sequence's first output row) and of ceil(seq_lens[s]/page_size)
+ * (each sequence's first page span).  hp_gather_planned and
+ * hp_gather_dequant_planned consume the workspace, in stream order.
+ */
+int hp_plan(const hp_paged_desc* desc, uint64_t out_tokens, void* workspace,
+            uint64_t workspace_bytes, int* d_status, void* stream);
+
+/* ------------------------------------------------------------------- gather */
+/*
+ * ASYNC.  Gather the ragged batch into `out` (device, out_tokens rows of
+ * num_heads*head_dim elements of desc->dtype, row-major): row tok_off[s]+t holds
+ * token t of sequence s for t < seq_lens[s], element (h, d) of it being
+ * page_pool[((phys*page_size + t % page_size)*num_heads + h)*head_dim + d] with
+ * phys = block_table[seq_ptr[s] + t / page_size] ([HF] Element Lookup).
+ * Elements are copied as bytes.  No slot past a sequence's token count is read
+ * ([HF] Partial trailing page).  Equivalent to hp_plan then hp_gather_planned.
+ * `out` must be 16-byte aligned for the vector path (any alignment works).
+ */
+int hp_gather(const hp_paged_desc* desc, void* out, uint64_t out_tokens, void* workspace,
+              uint64_t workspace_bytes, int* d_status, void* stream);
+
+/* ASYNC.  The copy step of hp_gather, for a workspace hp_plan filled with the same
+ * descriptor earlier on the same stream.  Does nothing if that plan failed. */
+int hp_gather_planned(const hp_paged_desc* desc, void* out, const void* workspace,
+                      int* d_status, void* stream);
+
+/*
+ * ASYNC.  Dequantising gather of an int8 pool (desc->dtype == HP_I8, flags with
+ * HP_HAS_QUANT): like hp_gather, but element (h, d) of token t of sequence s is
+ * the bfloat16 nearest (ties to even) to the exact product
+ * value * scales[phys*page_size + t % page_size] ([HF] Element Lookup, quantized
+ * case; Per-page-slot parameters; a symmetric scheme, no zero point).
+ * `out_bf16` (device) holds out_tokens rows of num_heads*head_dim bfloat16.
+ */
+int hp_gather_dequant(const hp_paged_desc* desc, void* out_bf16, uint64_t out_tokens,
+                      void* workspace, uint64_t workspace_bytes, int* d_status, void* stream);
+
+/* ASYNC.  The copy step of hp_gather_dequant, after hp_plan on the same stream. */
+int hp_gather_dequant_planned(const hp_paged_desc* desc, void* out_bf16, const void* workspace,
+                              int* d_status, void* stream);
+
+/* ------------------------------------------------------------------- append */
+/*
+ * ASYNC.  Append new K (or V) rows to their sequences: new row new_ptr[s]+i of
+ * `new_rows` (device, total_new rows of num_heads*head_dim elements of
+ * desc->dtype) becomes token t = seq_lens[s] + i of sequence s, written to the
+ * pool slot the Element Lookup names for t ([HF] Element Lookup, used as a
+ * store).  desc->seq_lens holds the counts BEFORE the append; the library does
+ * not update them.  new_ptr (device, num_seqs+1 entries of the index type) is a
+ * CSR offset array over the new rows.  Validation (device, unless permissive):
+ * the storage invariants, then new_ptr[0] = 0, non-decreasing,
+ * new_ptr[num_seqs] = total_new, then seq_lens[s] + rows of s <= the slice's
+ * slots.  Rows whose targets alias (two sequences naming one page and slot)
+ * land in an unspecified order.  `new_rows` must be 16-byte aligned for the
+ * vector path.
+ */
+int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, const void* new_ptr,
+                      uint64_t total_new, void* workspace, uint64_t workspace_bytes,
+                      int* d_status, void* stream);
+
+/* ASYNC.  The validation and planning step of hp_scatter_append. */
+int hp_append_plan(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,
+                   void* workspace, uint64_t workspace_bytes, int* d_status, void* stream);
+
+/* ASYNC.  The copy step of hp_scatter_append, after hp_append_plan on the same stream. */
+int hp_scatter_append_planned(const hp_paged_desc* desc, const void* new_rows,
+                              const void* new_ptr, const void* workspace, int* d_status,
+                              void* stream);
+
+/* SYNC.  The verdict hp_append_plan reaches, returned like hp_validate's. */
+int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,
+                       void* workspace, uint64_t workspace_bytes, uint64_t* first_bad,
+                       void* stream);
+
+/* ------------------------------------------------------------ per-lane layout */
+/*
+ * Host only.  The checks of [CH] PagedKvLayout::new for a layout of logical
+ * capacity `capacity` with `page_tokens` positions per page and page table
+ * `table` (host, table_len entries): zero capacity, zero page size, an
+ * overflowing ceil(C/P)*P, table_len != ceil(C/P), an entry >= ceil(C/P), a
+ * repeated entry -- in that order, first failing entry first.  detail (host,
+ * 2 entries, may be NULL) receives (expected, actual) for HP_ERR_PAGE_COUNT,
+ * (logical page, physical page) for HP_ERR_PHYSICAL_PAGE, (physical page, 0)
+ * for HP_ERR_ALIASED_PAGE.  A table that passes is a permutation of
+ * 0..ceil(C/P)-1.
+ */
+int hp_lane_validate(uint64_t capacity, uint64_t page_tokens, const uint64_t* table,
+                     uint64_t table_len, uint64_t* detail);
+
+/*
+ * ASYNC.  Logical snapshot of the per-lane layout ([CH] "Include the batch,
+ * shared head and feature"): `pool` (device) is [N, B, H_kv, P, d] elements of
+ * `dtype` with N = ceil(capacity/page_tokens), P = page_tokens, B = batch,
+ * H_kv = kv_heads, d = width; `table` (device, N uint64 entries) maps logical
+ * page q to physical page table[q].  `out` (device) receives [B, H_kv, n, d]:
+ * element (b, h, p, f) = pool scalar ((table[p/P]*B*H_kv + b*H_kv + h)*P +
+ * p%P)*d + f, for the n live positions p < n.  Requires n <= capacity
+ * (HP_ERR_LENGTH).  The table is not validated here (hp_lane_validate does
+ * that once); an entry >= N skips its rows and stores HP_ERR_PHYSICAL_PAGE in
+ * *d_status.
+ */
+int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capacity,
+                   uint64_t page_tokens, uint64_t batch, uint64_t kv_heads, uint64_t width,
+                   uint32_t dtype, uint64_t n, void* out, int* d_status, void* stream);
+
+/*
+ * ASYNC.  Append m rows per lane at positions n..n+m-1 (a decode step appends
+ * one): element (b, h, i, f) of `new_rows` (device, [B, H_kv, m, d]) is written
+ * to pool scalar ((table[p/P]*B*H_kv + b*H_kv + h)*P + p%P)*d + f with p = n+i.
+ * Requires n + m <= capacity (HP_ERR_LENGTH, nothing written).
+ */
+int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity, uint64_t page_tokens,
+                   uint64_t batch, uint64_t kv_heads, uint64_t width, uint32_t dtype,
+                   uint64_t n, uint64_t m, const void* new_rows, int* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HP_H */

@@ -1,0 +1,503 @@
+// hp_abi.cu -- the extern "C" entry points of libhp.so (declared in include/hp.h):
+// host-side argument checks, then the plan and copy launches on the caller's stream.
+//
+// The structural checks follow "Block-Paged Layout -- Hurray Format Specification":
+// Description (rank 3), Logical Shape (paged_axis 0), Sharding (no shard descriptor),
+// Additional Descriptor Fields (index type 0x00 / 0x01; uint32 addresses at most
+// 0xFFFFFFFF pages), Scale-buffer size (num_pages * page_size scales), Alignment
+// (64 bytes) and Storage Invariants (4) (the pool's byte size).  The lane checks follow
+// the constructor of "Keep token order across cache pages" (PagedKvLayout::new).
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <vector>
+
+#include "hp_internal.cuh"
+
+#define HP_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using u64 = uint64_t;
+using u128 = unsigned __int128;
+
+u64 elem_bytes(uint32_t dtype)
+{
+    switch (dtype) {
+    case HP_F32: return 4;
+    case HP_F16: return 2;
+    case HP_BF16: return 2;
+    case HP_I8: return 1;
+    case HP_U8: return 1;
+    case HP_F64: return 8;
+    default: return 0;
+    }
+}
+
+bool misaligned(const void* p, u64 a) { return reinterpret_cast<uintptr_t>(p) % a != 0; }
+
+int check_desc(const hp_paged_desc* d)
+{
+    if (!d) return HP_ERR_NULL;
+    if (d->rank != 3) return HP_ERR_RANK;
+    if (d->paged_axis != 0) return HP_ERR_PAGED_AXIS;
+    if (d->has_shard) return HP_ERR_SHARD;
+    if (d->index_type != HP_IDX_U32 && d->index_type != HP_IDX_U64) return HP_ERR_INDEX_TYPE;
+    if (d->index_type == HP_IDX_U32 && (d->num_pages > (1ull << 32) || d->table_len > 0xFFFFFFFFull))
+        return HP_ERR_INDEX_TYPE;
+    const u64 es = elem_bytes(d->dtype);
+    if (!es) return HP_ERR_DTYPE;
+    if (!d->page_size || !d->num_heads || !d->head_dim) return HP_ERR_ZERO_DIM;
+    const bool quant = d->flags & HP_HAS_QUANT;
+    if (quant && (!d->scales || (u128)d->scales_len != (u128)d->num_pages * d->page_size))
+        return HP_ERR_SCALES;
+    if ((d->num_pages && !d->page_pool) || !d->seq_ptr || (d->num_seqs && !d->seq_lens) ||
+        (d->table_len && !d->block_table))
+        return HP_ERR_NULL;
+    if (misaligned(d->page_pool, 64) || misaligned(d->block_table, 64) ||
+        misaligned(d->seq_ptr, 64) || misaligned(d->seq_lens, 64) ||
+        (quant && misaligned(d->scales, 64)))
+        return HP_ERR_ALIGN;
+    u128 bytes = (u128)d->num_pages * d->page_size;
+    bytes *= d->num_heads;
+    if (bytes >> 64) return HP_ERR_OVERFLOW;
+    bytes *= d->head_dim;
+    if (bytes >> 64) return HP_ERR_OVERFLOW;
+    bytes *= es;
+    if (bytes >> 64) return HP_ERR_OVERFLOW;
+    return HP_OK;
+}
+
+u64 row_bytes_of(const hp_paged_desc* d)
+{
+    return d->num_heads * d->head_dim * elem_bytes(d->dtype);
+}
+
+int ws_bytes(const hp_paged_desc* d, u64* out)
+{
+    if (d->num_seqs >= (1ull << 58)) return HP_ERR_OVERFLOW;
+    *out = hp::kWsHeaderBytes + 2 * hp::round_up_256(8 * (d->num_seqs + 1));
+    return HP_OK;
+}
+
+int check_ws(const hp_paged_desc* d, const void* ws, u64 have)
+{
+    u64 need = 0;
+    int rc = ws_bytes(d, &need);
+    if (rc) return rc;
+    if (!ws || misaligned(ws, 256) || have < need) return HP_ERR_WORKSPACE;
+    return HP_OK;
+}
+
+// Widest power-of-two vector (<= 16 bytes) that divides the row and both bases.
+int pick_vec(u64 row_bytes, const void* a, const void* b)
+{
+    const uintptr_t m = static_cast<uintptr_t>(row_bytes) | reinterpret_cast<uintptr_t>(a) |
+                        reinterpret_cast<uintptr_t>(b);
+    for (int v = 16; v > 1; v >>= 1)
+        if (m % v == 0) return v;
+    return 1;
+}
+
+hp::PlanArgs plan_args(const hp_paged_desc* d, void* ws, int* d_status)
+{
+    hp::PlanArgs a{};
+    a.seq_ptr = d->seq_ptr;
+    a.lens = d->seq_lens;
+    a.table = d->block_table;
+    a.num_seqs = d->num_seqs;
+    a.page_size = d->page_size;
+    a.table_len = d->table_len;
+    a.num_pages = d->num_pages;
+    a.strict = !(d->flags & HP_PERMISSIVE);
+    a.d_status = d_status;
+    a.ws = hp::ws_view(ws, d->num_seqs);
+    return a;
+}
+
+hp::CopyArgs copy_args(const hp_paged_desc* d, const void* ws, int* d_status)
+{
+    hp::CopyArgs a{};
+    a.seq_ptr = d->seq_ptr;
+    a.lens = d->seq_lens;
+    a.table = d->block_table;
+    a.scales = d->scales;
+    a.num_seqs = d->num_seqs;
+    a.page_size = d->page_size;
+    a.table_len = d->table_len;
+    a.num_pages = d->num_pages;
+    const hp::WsView v = hp::ws_view(const_cast<void*>(ws), d->num_seqs);
+    a.hdr = v.hdr;
+    a.rows_off = v.rows_off;
+    a.units_off = v.units_off;
+    a.row_bytes = row_bytes_of(d);
+    a.row_elems = d->num_heads * d->head_dim;
+    a.d_status = d_status;
+    return a;
+}
+
+int sync_verdict(const void* ws, u64* first_bad, void* stream)
+{
+    unsigned long long key = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&key, &static_cast<const hp::WsHeader*>(ws)->verdict, sizeof(key),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return HP_ERR_CUDA;
+    if (first_bad) *first_bad = key == hp::kVerdictOk ? 0 : (key & hp::kIndexMask);
+    return hp::key_status(key);
+}
+
+int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_status,
+                   void* stream, bool dequant)
+{
+    int rc = check_desc(d);
+    if (rc) return rc;
+    if (dequant) {
+        if (d->dtype != HP_I8) return HP_ERR_DTYPE;
+        if (!(d->flags & HP_HAS_QUANT)) return HP_ERR_SCALES;
+    }
+    if (!ws || misaligned(ws, 256)) return HP_ERR_WORKSPACE;
+    if (d->num_seqs == 0) return HP_OK;
+    if (!out) return HP_ERR_NULL;
+    hp::CopyArgs a = copy_args(d, ws, d_status);
+    a.src = static_cast<const char*>(d->page_pool);
+    a.dst = static_cast<char*>(out);
+    int vec;
+    if (dequant) {
+        const bool v16 = a.row_elems % 16 == 0 && !misaligned(out, 16) &&
+                         (u128)d->page_size * a.row_elems < ((u128)1 << 36);
+        vec = v16 ? 16 : 1;
+        return hp::launch_copy(hp::kDequant, d->index_type == HP_IDX_U64, a, vec, stream);
+    }
+    vec = pick_vec(a.row_bytes, d->page_pool, out);
+    return hp::launch_copy(hp::kGather, d->index_type == HP_IDX_U64, a, vec, stream);
+}
+
+int plan_gather(const hp_paged_desc* d, u64 out_tokens, void* ws, u64 wsb, int* d_status,
+                void* stream, bool check_out)
+{
+    int rc = check_ws(d, ws, wsb);
+    if (rc) return rc;
+    if (check_out) {
+        const u128 out_bytes = (u128)out_tokens * d->num_heads * d->head_dim *
+                               ((d->flags & HP_HAS_QUANT) && d->dtype == HP_I8 ? 2 : elem_bytes(d->dtype));
+        if (out_bytes >> 64) return HP_ERR_OUT_SIZE;
+    }
+    hp::PlanArgs a = plan_args(d, ws, d_status);
+    a.out_tokens = out_tokens;
+    a.check_out = check_out;
+    return hp::launch_plan(hp::kPlanGather, d->index_type == HP_IDX_U64, a, stream);
+}
+
+int plan_append(const hp_paged_desc* d, const void* new_ptr, u64 total_new, void* ws, u64 wsb,
+                int* d_status, void* stream)
+{
+    int rc = check_ws(d, ws, wsb);
+    if (rc) return rc;
+    if (!new_ptr) return HP_ERR_NULL;
+    if (misaligned(new_ptr, d->index_type == HP_IDX_U64 ? 8 : 4)) return HP_ERR_ALIGN;
+    if ((u128)total_new * row_bytes_of(d) >> 64) return HP_ERR_OVERFLOW;
+    hp::PlanArgs a = plan_args(d, ws, d_status);
+    a.new_ptr = new_ptr;
+    a.total_new = total_new;
+    return hp::launch_plan(hp::kPlanAppend, d->index_type == HP_IDX_U64, a, stream);
+}
+
+int append_planned(const hp_paged_desc* d, const void* new_rows, const void* new_ptr,
+                   const void* ws, int* d_status, void* stream)
+{
+    if (!ws || misaligned(ws, 256)) return HP_ERR_WORKSPACE;
+    if (d->num_seqs == 0) return HP_OK;
+    if (!new_ptr) return HP_ERR_NULL;
+    hp::CopyArgs a = copy_args(d, ws, d_status);
+    a.new_ptr = new_ptr;
+    a.src = static_cast<const char*>(new_rows);
+    a.dst = static_cast<char*>(const_cast<void*>(d->page_pool));
+    if (!a.src) a.src = reinterpret_cast<const char*>(d->page_pool);  // no rows: never read
+    const int vec = pick_vec(a.row_bytes, a.src, d->page_pool);
+    return hp::launch_copy(hp::kAppend, d->index_type == HP_IDX_U64, a, vec, stream);
+}
+
+// Lane-layout argument checks shared by gather and append.
+int check_lane(const void* pool, const uint64_t* table, u64 capacity, u64 page_tokens, u64 batch,
+               u64 kv_heads, u64 width, uint32_t dtype, u64* pages, u64* row_bytes)
+{
+    const u64 es = elem_bytes(dtype);
+    if (!es) return HP_ERR_DTYPE;
+    if (capacity == 0) return HP_ERR_ZERO_CAPACITY;
+    if (page_tokens == 0) return HP_ERR_ZERO_PAGE_SIZE;
+    if (!batch || !kv_heads || !width) return HP_ERR_ZERO_DIM;
+    const u64 n_pages = capacity / page_tokens + (capacity % page_tokens != 0);
+    u128 total = (u128)n_pages * page_tokens;
+    if (total >> 64) return HP_ERR_LANE_OVERFLOW;
+    total *= batch;
+    if (total >> 64) return HP_ERR_LANE_OVERFLOW;
+    total *= kv_heads;
+    if (total >> 64) return HP_ERR_LANE_OVERFLOW;
+    total *= width;
+    if (total >> 64) return HP_ERR_LANE_OVERFLOW;
+    total *= es;
+    if (total >> 64) return HP_ERR_LANE_OVERFLOW;
+    if (!pool || !table) return HP_ERR_NULL;
+    if (misaligned(table, 8)) return HP_ERR_ALIGN;
+    *pages = n_pages;
+    *row_bytes = width * es;
+    return HP_OK;
+}
+
+int reset_status(int* d_status, void* stream)
+{
+    if (!d_status) return HP_OK;
+    return cudaMemsetAsync(d_status, 0, sizeof(int), static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? HP_OK
+               : HP_ERR_CUDA;
+}
+
+}  // namespace
+
+// ============================================================================ API
+
+HP_API const char* hp_status_string(int s)
+{
+    switch (s) {
+#define HP_NAME(c) \
+    case c: return #c;
+        HP_NAME(HP_OK)
+        HP_NAME(HP_ERR_RANK)
+        HP_NAME(HP_ERR_PAGED_AXIS)
+        HP_NAME(HP_ERR_SHARD)
+        HP_NAME(HP_ERR_INDEX_TYPE)
+        HP_NAME(HP_ERR_DTYPE)
+        HP_NAME(HP_ERR_ZERO_DIM)
+        HP_NAME(HP_ERR_SCALES)
+        HP_NAME(HP_ERR_NULL)
+        HP_NAME(HP_ERR_ALIGN)
+        HP_NAME(HP_ERR_OVERFLOW)
+        HP_NAME(HP_ERR_SEQ_PTR_START)
+        HP_NAME(HP_ERR_SEQ_PTR_ORDER)
+        HP_NAME(HP_ERR_SEQ_PTR_END)
+        HP_NAME(HP_ERR_PAGE_ID)
+        HP_NAME(HP_ERR_LEN)
+        HP_NAME(HP_ERR_NEW_PTR_START)
+        HP_NAME(HP_ERR_NEW_PTR_ORDER)
+        HP_NAME(HP_ERR_NEW_PTR_END)
+        HP_NAME(HP_ERR_CAPACITY)
+        HP_NAME(HP_ERR_OUT_SIZE)
+        HP_NAME(HP_ERR_ZERO_CAPACITY)
+        HP_NAME(HP_ERR_ZERO_PAGE_SIZE)
+        HP_NAME(HP_ERR_LANE_OVERFLOW)
+        HP_NAME(HP_ERR_PAGE_COUNT)
+        HP_NAME(HP_ERR_PHYSICAL_PAGE)
+        HP_NAME(HP_ERR_ALIASED_PAGE)
+        HP_NAME(HP_ERR_LENGTH)
+        HP_NAME(HP_ERR_ALLOCATION_FAILED)
+        HP_NAME(HP_ERR_WORKSPACE)
+        HP_NAME(HP_ERR_ARG)
+        HP_NAME(HP_ERR_CUDA)
+#undef HP_NAME
+    default: return "HP_ERR_UNKNOWN";
+    }
+}
+
+HP_API int hp_workspace_bytes(const hp_paged_desc* desc, uint64_t* bytes)
+{
+    if (!desc || !bytes) return HP_ERR_NULL;
+    return ws_bytes(desc, bytes);
+}
+
+HP_API int hp_validate(const hp_paged_desc* desc, void* workspace, uint64_t workspace_bytes,
+                       uint64_t* first_bad, void* stream)
+{
+    if (first_bad) *first_bad = 0;
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (desc->flags & HP_PERMISSIVE) return HP_OK;
+    rc = plan_gather(desc, 0, workspace, workspace_bytes, nullptr, stream, false);
+    if (rc) return rc;
+    return sync_verdict(workspace, first_bad, stream);
+}
+
+HP_API int hp_plan(const hp_paged_desc* desc, uint64_t out_tokens, void* workspace,
+                   uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    return plan_gather(desc, out_tokens, workspace, workspace_bytes, d_status, stream, true);
+}
+
+HP_API int hp_gather_planned(const hp_paged_desc* desc, void* out, const void* workspace,
+                             int* d_status, void* stream)
+{
+    return gather_planned(desc, out, workspace, d_status, stream, false);
+}
+
+HP_API int hp_gather(const hp_paged_desc* desc, void* out, uint64_t out_tokens, void* workspace,
+                     uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (out_tokens && !out) return HP_ERR_NULL;
+    rc = plan_gather(desc, out_tokens, workspace, workspace_bytes, d_status, stream, true);
+    if (rc) return rc;
+    return gather_planned(desc, out, workspace, d_status, stream, false);
+}
+
+HP_API int hp_gather_dequant_planned(const hp_paged_desc* desc, void* out_bf16,
+                                     const void* workspace, int* d_status, void* stream)
+{
+    return gather_planned(desc, out_bf16, workspace, d_status, stream, true);
+}
+
+HP_API int hp_gather_dequant(const hp_paged_desc* desc, void* out_bf16, uint64_t out_tokens,
+                             void* workspace, uint64_t workspace_bytes, int* d_status,
+                             void* stream)
+{
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (desc->dtype != HP_I8) return HP_ERR_DTYPE;
+    if (!(desc->flags & HP_HAS_QUANT)) return HP_ERR_SCALES;
+    if (out_tokens && !out_bf16) return HP_ERR_NULL;
+    rc = plan_gather(desc, out_tokens, workspace, workspace_bytes, d_status, stream, true);
+    if (rc) return rc;
+    return gather_planned(desc, out_bf16, workspace, d_status, stream, true);
+}
+
+HP_API int hp_append_plan(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,
+                          void* workspace, uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    return plan_append(desc, new_ptr, total_new, workspace, workspace_bytes, d_status, stream);
+}
+
+HP_API int hp_scatter_append_planned(const hp_paged_desc* desc, const void* new_rows,
+                                     const void* new_ptr, const void* workspace, int* d_status,
+                                     void* stream)
+{
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    return append_planned(desc, new_rows, new_ptr, workspace, d_status, stream);
+}
+
+HP_API int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, const void* new_ptr,
+                             uint64_t total_new, void* workspace, uint64_t workspace_bytes,
+                             int* d_status, void* stream)
+{
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (total_new && !new_rows) return HP_ERR_NULL;
+    rc = plan_append(desc, new_ptr, total_new, workspace, workspace_bytes, d_status, stream);
+    if (rc) return rc;
+    return append_planned(desc, new_rows, new_ptr, workspace, d_status, stream);
+}
+
+HP_API int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,
+                              void* workspace, uint64_t workspace_bytes, uint64_t* first_bad,
+                              void* stream)
+{
+    if (first_bad) *first_bad = 0;
+    int rc = check_desc(desc);
+    if (rc) return rc;
+    if (desc->flags & HP_PERMISSIVE) return HP_OK;
+    rc = plan_append(desc, new_ptr, total_new, workspace, workspace_bytes, nullptr, stream);
+    if (rc) return rc;
+    return sync_verdict(workspace, first_bad, stream);
+}
+
+HP_API int hp_lane_validate(uint64_t capacity, uint64_t page_tokens, const uint64_t* table,
+                            uint64_t table_len, uint64_t* detail)
+{
+    uint64_t scratch[2];
+    uint64_t* det = detail ? detail : scratch;
+    det[0] = det[1] = 0;
+    if (capacity == 0) return HP_ERR_ZERO_CAPACITY;
+    if (page_tokens == 0) return HP_ERR_ZERO_PAGE_SIZE;
+    const u64 pages = capacity / page_tokens + (capacity % page_tokens != 0);
+    if (((u128)pages * page_tokens) >> 64) return HP_ERR_LANE_OVERFLOW;
+    if (table_len != pages) {
+        det[0] = pages;
+        det[1] = table_len;
+        return HP_ERR_PAGE_COUNT;
+    }
+    if (pages && !table) return HP_ERR_NULL;
+    std::vector<unsigned char> seen;
+    try {
+        seen.assign(pages, 0);
+    } catch (...) {
+        return HP_ERR_ALLOCATION_FAILED;
+    }
+    for (u64 q = 0; q < pages; ++q) {
+        const u64 p = table[q];
+        if (p >= pages) {
+            det[0] = q;
+            det[1] = p;
+            return HP_ERR_PHYSICAL_PAGE;
+        }
+        if (seen[p]) {
+            det[0] = p;
+            return HP_ERR_ALIASED_PAGE;
+        }
+        seen[p] = 1;
+    }
+    return HP_OK;
+}
+
+HP_API int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capacity,
+                          uint64_t page_tokens, uint64_t batch, uint64_t kv_heads, uint64_t width,
+                          uint32_t dtype, uint64_t n, void* out, int* d_status, void* stream)
+{
+    u64 pages = 0, rb = 0;
+    int rc = check_lane(pool, table, capacity, page_tokens, batch, kv_heads, width, dtype, &pages,
+                        &rb);
+    if (rc) return rc;
+    if (n > capacity) return HP_ERR_LENGTH;
+    if (n && !out) return HP_ERR_NULL;
+    rc = reset_status(d_status, stream);
+    if (rc || n == 0) return rc;
+    hp::CopyArgs a{};
+    a.table = table;
+    a.num_pages = pages;
+    a.page_size = page_tokens;
+    a.lanes = batch * kv_heads;
+    a.lane_n = n;
+    a.lane_pages = n / page_tokens + (n % page_tokens != 0);
+    a.lane_first_page = 0;
+    a.lane_units = a.lanes * a.lane_pages;
+    a.src = static_cast<const char*>(pool);
+    a.dst = static_cast<char*>(out);
+    a.row_bytes = rb;
+    a.d_status = d_status;
+    return hp::launch_copy(hp::kLaneGather, 1, a, pick_vec(rb, pool, out), stream);
+}
+
+HP_API int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity,
+                          uint64_t page_tokens, uint64_t batch, uint64_t kv_heads, uint64_t width,
+                          uint32_t dtype, uint64_t n, uint64_t m, const void* new_rows,
+                          int* d_status, void* stream)
+{
+    u64 pages = 0, rb = 0;
+    int rc = check_lane(pool, table, capacity, page_tokens, batch, kv_heads, width, dtype, &pages,
+                        &rb);
+    if (rc) return rc;
+    if (n > capacity || m > capacity - n) return HP_ERR_LENGTH;
+    if (m && !new_rows) return HP_ERR_NULL;
+    rc = reset_status(d_status, stream);
+    if (rc || m == 0) return rc;
+    hp::CopyArgs a{};
+    a.table = table;
+    a.num_pages = pages;
+    a.page_size = page_tokens;
+    a.lanes = batch * kv_heads;
+    a.lane_n = n;
+    a.lane_m = m;
+    a.lane_first_page = n / page_tokens;
+    a.lane_pages = (n + m - 1) / page_tokens - n / page_tokens + 1;
+    a.lane_units = a.lanes * a.lane_pages;
+    a.src = static_cast<const char*>(new_rows);
+    a.dst = static_cast<char*>(pool);
+    a.row_bytes = rb;
+    a.d_status = d_status;
+    return hp::launch_copy(hp::kLaneAppend, 1, a, pick_vec(rb, new_rows, pool), stream);
+}

@@ -1,0 +1,135 @@
+// hp_internal.cuh -- shared declarations of the libhp CUDA sources (not installed).
+//
+// Workspace layout (device, 256-byte aligned, hp_workspace_bytes() bytes):
+//   [0, 64)          WsHeader: verdict key, totals
+//   [256, 256+A)     rows_off[S+1]  exclusive prefix of the token counts (first output
+//                    row of each sequence), A = round_up(8*(S+1), 256)
+//   [256+A, 256+2A)  units_off[S+1] exclusive prefix of each sequence's copy units
+//                    (page spans of a gather, pages touched by an append)
+#pragma once
+
+#include <cstdint>
+
+#include "hp.h"
+
+namespace hp {
+
+// Rule ranks: the order in which the checks of a descriptor apply.  A verdict
+// key is (rank << 58) | index; the smallest key is the first failing rule at
+// its first failing index.  kVerdictOk means no rule failed.
+enum Rank : unsigned {
+    kRankSeqPtrStart = 1,
+    kRankSeqPtrOrder = 2,
+    kRankSeqPtrEnd = 3,
+    kRankPageId = 4,
+    kRankLen = 5,
+    kRankNewPtrStart = 6,
+    kRankNewPtrOrder = 7,
+    kRankNewPtrEnd = 8,
+    kRankCapacity = 9,
+    kRankOutSize = 10,
+};
+constexpr unsigned long long kVerdictOk = ~0ull;
+constexpr unsigned long long kIndexMask = (1ull << 58) - 1;
+
+__host__ __device__ inline unsigned long long verdict_key(unsigned rank, unsigned long long index)
+{
+    return ((unsigned long long)rank << 58) | (index < kIndexMask ? index : kIndexMask);
+}
+
+__host__ __device__ inline int rank_status(unsigned rank)
+{
+    switch (rank) {
+    case kRankSeqPtrStart: return HP_ERR_SEQ_PTR_START;
+    case kRankSeqPtrOrder: return HP_ERR_SEQ_PTR_ORDER;
+    case kRankSeqPtrEnd: return HP_ERR_SEQ_PTR_END;
+    case kRankPageId: return HP_ERR_PAGE_ID;
+    case kRankLen: return HP_ERR_LEN;
+    case kRankNewPtrStart: return HP_ERR_NEW_PTR_START;
+    case kRankNewPtrOrder: return HP_ERR_NEW_PTR_ORDER;
+    case kRankNewPtrEnd: return HP_ERR_NEW_PTR_END;
+    case kRankCapacity: return HP_ERR_CAPACITY;
+    case kRankOutSize: return HP_ERR_OUT_SIZE;
+    default: return HP_OK;
+    }
+}
+
+__host__ __device__ inline int key_status(unsigned long long key)
+{
+    return key == kVerdictOk ? HP_OK : rank_status((unsigned)(key >> 58));
+}
+
+struct WsHeader {
+    unsigned long long verdict;      // smallest failing key, kVerdictOk if none
+    unsigned long long total_rows;   // sum of token counts (gather)
+    unsigned long long total_units;  // units_off[S]
+    unsigned long long pad[5];
+};
+
+constexpr uint64_t kWsHeaderBytes = 256;
+
+inline uint64_t round_up_256(uint64_t x) { return (x + 255) & ~255ull; }
+
+struct WsView {
+    WsHeader* hdr;
+    unsigned long long* rows_off;
+    unsigned long long* units_off;
+};
+
+inline WsView ws_view(void* ws, uint64_t num_seqs)
+{
+    char* base = static_cast<char*>(ws);
+    uint64_t a = round_up_256(8 * (num_seqs + 1));
+    return WsView{reinterpret_cast<WsHeader*>(base),
+                  reinterpret_cast<unsigned long long*>(base + kWsHeaderBytes),
+                  reinterpret_cast<unsigned long long*>(base + kWsHeaderBytes + a)};
+}
+
+// ------------------------------------------------------------------ plan step
+enum PlanMode { kPlanGather = 0, kPlanAppend = 1 };
+
+struct PlanArgs {
+    const void* seq_ptr;
+    const void* lens;
+    const void* new_ptr;      // append only
+    const void* table;
+    uint64_t num_seqs, page_size, table_len, num_pages;
+    uint64_t out_tokens;      // gather: expected total rows
+    uint64_t total_new;       // append: expected new_ptr[S]
+    int strict;               // check the storage invariants
+    int check_out;            // gather: compare the total with out_tokens
+    int* d_status;
+    WsView ws;
+};
+
+// Launches the plan (and, when strict, the block-table check) on `stream`.
+int launch_plan(PlanMode mode, int index_u64, const PlanArgs& a, void* stream);
+
+// ------------------------------------------------------------------ copy step
+enum CopyMode { kGather = 0, kDequant = 1, kAppend = 2, kLaneGather = 3, kLaneAppend = 4 };
+
+struct CopyArgs {
+    // block-paged descriptor data
+    const void* seq_ptr;
+    const void* lens;
+    const void* new_ptr;
+    const void* table;
+    const float* scales;
+    uint64_t num_seqs, page_size, table_len, num_pages;
+    uint64_t total_new;
+    const WsHeader* hdr;
+    const unsigned long long* rows_off;
+    const unsigned long long* units_off;
+    // per-lane layout
+    uint64_t lanes, lane_n, lane_m, lane_units, lane_first_page, lane_pages;
+    // data movement
+    const char* src;          // gather: pool; append: new rows
+    char* dst;                // gather: out; append: pool
+    uint64_t row_bytes;       // bytes of one source row
+    uint64_t row_elems;       // elements of one row (dequant)
+    int* d_status;
+};
+
+int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* stream);
+
+}  // namespace hp

@@ -317,6 +317,8 @@ def _host_values(dist, seed, count, dtype):
 
 
 def _to_bytes(v, dtype):
+    if dtype in ("i8", "u8"):  # a normal draw on an integer pool: 32 steps per unit, clipped
+        return np.clip(np.rint(v * 32), -127, 127).astype(np.int8).view(np.uint8)
     if dtype == "f32":
         return v.astype(np.float32).view(np.uint8)
     if dtype == "f64":

@@ -30,3 +30,28 @@ def oracle():
     import oracle as o
     o.build()
     return o
+
+
+@pytest.fixture(scope="session")
+def hp():
+    """The CUDA library binding, built in-tree for sm_103a if it is stale."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from paged_kv_cache_hp_gb300 import build, hp as binding
+    build.build()
+    binding.lib()
+    return binding
+
+
+def guarded(nbytes, device="cuda", guard=256, fill=0xEE):
+    """A byte buffer with `guard` bytes of `fill` on both sides of an nbytes window;
+    returns (buffer, window)."""
+    import torch
+    buf = torch.full((guard + nbytes + guard,), fill, dtype=torch.uint8, device=device)
+    return buf, buf[guard:guard + nbytes]
+
+
+def guards_intact(buf, nbytes, guard=256, fill=0xEE):
+    b = buf.cpu().numpy()
+    return bool((b[:guard] == fill).all() and (b[guard + nbytes:] == fill).all())

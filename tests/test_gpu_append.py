@@ -1,0 +1,185 @@
+"""GPU parity: hp_scatter_append against the CPU oracle -- the whole pool after the
+append, byte for byte."""
+import numpy as np
+import pytest
+
+from helpers import Batch, index_tensor, lib_name, sub_batch
+from paged_kv_cache_hp_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def append_case(hp, oracle, w, lens_before, new_ptr, new_rows_host, it=None):
+    """Runs the device append and the oracle append on copies of the same pool;
+    returns (device pool bytes, oracle pool bytes, status name)."""
+    import torch
+    b = Batch(w, lens=lens_before)
+    host = b.host_pool().copy()
+    new_dev = torch.from_numpy(np.ascontiguousarray(new_rows_host)).to("cuda")
+    np_dev = index_tensor(np.asarray(new_ptr, dtype=w.index_dtype), "cuda")
+    total = int(new_ptr[-1])
+    rc = hp.hp_scatter_append(b.desc, new_dev, np_dev, total, b.ws, b.status)
+    torch.cuda.synchronize()
+    assert hp.status_name(rc) == "HP_OK"
+    o = b.oracle_desc(pool_host=host, lens=np.asarray(lens_before, dtype=w.index_dtype))
+    assert o.validate_append(new_ptr, total) == ("OK", 0)
+    assert o.scatter_append(new_rows_host, new_ptr) == "OK"
+    return b.pool.cpu().numpy(), host, hp.status_name(b.status_value()), b
+
+
+def test_decode_step_append_small(hp, oracle):
+    w = inputs.config("decode_append", "small")
+    got, want, st, _ = append_case(hp, oracle, w, w.lens_before, w.new_ptr, inputs.host_new_rows(w))
+    assert st == "HP_OK"
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_multi_row_append_crossing_pages(hp, oracle, seed):
+    """Several rows per sequence, starting anywhere in a page and crossing page
+    boundaries; some sequences append nothing."""
+    rng = np.random.default_rng(seed)
+    P = [1, 3, 16, 5, 16, 7][seed]
+    w = inputs.decode_gather(seed=50 + seed, num_pages=900, page_size=P, num_heads=2,
+                             head_dim=[8, 16, 4, 3, 64, 5][seed], num_seqs=7, len_lo=0,
+                             len_hi=90, dtype=["bf16", "f32", "i8", "f16", "f16", "f64"][seed],
+                             index_dtype=np.uint64 if seed % 2 else np.uint32)
+    full = w.lens.astype(np.int64)
+    before = np.array([rng.integers(0, n + 1) for n in full])
+    new_n = full - before
+    new_n[rng.integers(0, len(new_n))] = 0
+    before = full - new_n
+    new_ptr = np.concatenate([[0], np.cumsum(new_n)]).astype(w.index_dtype)
+    rows = np.random.default_rng(seed + 7).integers(0, 256, (int(new_ptr[-1]), w.row_bytes),
+                                                    dtype=np.uint8)
+    got, want, st, b = append_case(hp, oracle, w, before.astype(w.index_dtype), new_ptr, rows)
+    assert st == "HP_OK"
+    assert np.array_equal(got, want)
+
+
+def test_bulk_append_then_gather_round_trip(hp, oracle):
+    """Prefill-style: every row of the batch appended into empty slices, then gathered
+    back -- the gather returns the appended rows."""
+    import torch
+    w = inputs.config("prefix_sharing", "small")
+    # give every sequence private pages (appending into shared pages is undefined)
+    w = inputs.decode_gather(seed=77, num_pages=700, num_heads=8, head_dim=128, num_seqs=6,
+                             len_lo=1, len_hi=300, dtype="bf16")
+    T = w.total_tokens
+    rows = np.random.default_rng(1).integers(0, 256, (T, w.row_bytes), dtype=np.uint8)
+    new_ptr = np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))]).astype(np.uint32)
+    zeros = np.zeros(w.num_seqs, dtype=np.uint32)
+    got, want, st, b = append_case(hp, oracle, w, zeros, new_ptr, rows)
+    assert st == "HP_OK" and np.array_equal(got, want)
+    g = Batch(w, pool=b.pool)
+    out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device="cuda")
+    assert hp.hp_gather(g.desc, out, T, g.ws, g.status) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().reshape(T, -1), rows)
+
+
+def test_full_size_decode_step_then_gather(hp, oracle):
+    """The decode step at full size (256 sequences, one new row each, a new page
+    where the row starts one), then the gather of the grown batch; sampled checks."""
+    import torch
+    w = inputs.config("decode_append", "full")
+    b = Batch(w, lens=w.lens_before)
+    new = inputs.device_new_rows(w, "cuda")
+    np_dev = index_tensor(w.new_ptr, "cuda")
+    rc = hp.hp_scatter_append(b.desc, new, np_dev, w.total_new, b.ws, b.status)
+    torch.cuda.synchronize()
+    assert rc == 0 and b.status_value() == 0
+    # every new row sits where the oracle's Element Lookup puts token len_before[s]
+    o = b.oracle_desc(pool_host=b.pool.cpu().numpy(), lens=w.lens)
+    new_h = new.cpu().numpy()
+    es = 2
+    rng = np.random.default_rng(3)
+    for s in range(w.num_seqs):
+        t = int(w.lens_before[s])
+        for h, d in zip(rng.integers(0, 8, 6), rng.integers(0, 128, 6)):
+            code, v = o.lookup(s, t, int(h), int(d))
+            assert code == "OK"
+            k = (int(h) * 128 + int(d)) * es
+            assert np.array_equal(v, new_h[s, k:k + es])
+    # the grown batch gathers consistently with the oracle
+    g = Batch(w, pool=b.pool)
+    T = w.total_tokens
+    out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device="cuda")
+    assert hp.hp_gather(g.desc, out, T, g.ws, g.status) == 0
+    torch.cuda.synchronize()
+    assert g.status_value() == 0
+    got = out.cpu().numpy().reshape(T, -1)
+    tok_off = np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))])
+    last_rows = tok_off[1:] - 1
+    assert np.array_equal(got[last_rows], new_h)
+    seqs = [0, 100, 255]
+    table, seq_ptr, lens = sub_batch(w, seqs)
+    sub = oracle.Desc(o.pool, table, seq_ptr, lens, num_pages=w.num_pages, page_size=16,
+                      num_heads=8, head_dim=128, dtype="bf16", index_type=0)
+    want = sub.gather()[0]
+    rows = np.concatenate([np.arange(tok_off[s], tok_off[s + 1]) for s in seqs])
+    assert np.array_equal(got[rows], want)
+
+
+@pytest.mark.parametrize("case,want", [
+    ({}, ("OK", 0)),
+    ({"new_ptr": [1, 1, 2]}, ("NEW_PTR_START", 0)),
+    ({"new_ptr": [0, 2, 1]}, ("NEW_PTR_ORDER", 1)),
+    ({"total_new": 3}, ("NEW_PTR_END", 2)),
+    ({"lens": [8, 2]}, ("CAPACITY", 0)),
+    ({"lens": [7, 3]}, ("OK", 0)),
+    ({"lens": [5, 4]}, ("CAPACITY", 1)),
+    ({"table": [0, 9, 2]}, ("PAGE_ID", 1)),
+    ({"seq_ptr": [0, 3, 2]}, ("SEQ_PTR_ORDER", 1)),
+])
+@pytest.mark.parametrize("it", [0, 1])
+def test_append_verdicts(hp, oracle, case, want, it):
+    import torch
+    dt = np.uint32 if it == 0 else np.uint64
+    table = case.get("table", [0, 1, 2])
+    seq_ptr = case.get("seq_ptr", [0, 2, 3])
+    lens = case.get("lens", [5, 2])
+    new_ptr = case.get("new_ptr", [0, 1, 2])
+    total = case.get("total_new", 2)
+    pool = torch.full((4 * 4 * 8,), 0x33, dtype=torch.uint8, device="cuda")
+    d = hp.PagedDesc(pool, index_tensor(np.asarray(table, dt), "cuda"),
+                     index_tensor(np.asarray(seq_ptr, dt), "cuda"),
+                     index_tensor(np.asarray(lens, dt), "cuda"), num_pages=4, page_size=4,
+                     num_heads=2, head_dim=2, dtype="f16", index_type=it)
+    ws = hp.workspace_for(d)
+    npd = index_tensor(np.asarray(new_ptr, dt), "cuda")
+    rc, first = hp.hp_validate_append(d, npd, total, ws)
+    o = oracle.Desc(pool.cpu().numpy(), table, seq_ptr, lens, num_pages=4, page_size=4,
+                    num_heads=2, head_dim=2, dtype="f16", index_type=it)
+    assert o.validate_append(new_ptr, total) == want
+    assert (hp.status_name(rc), first) == (lib_name(want[0]), want[1])
+    if want[0] != "OK":
+        st = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+        rows = torch.full((max(total, 3) * 8,), 0x44, dtype=torch.uint8, device="cuda")
+        assert hp.hp_scatter_append(d, rows, npd, total, ws, st) == 0
+        torch.cuda.synchronize()
+        assert hp.status_name(st.item()) == lib_name(want[0])
+        assert (pool.cpu().numpy() == 0x33).all()  # nothing written
+
+
+def test_permissive_append_skips_unwritable_rows(hp, oracle):
+    import torch
+    w = inputs.decode_gather(seed=31, num_pages=200, num_heads=2, head_dim=8, num_seqs=5,
+                             len_lo=1, len_hi=60)
+    full = w.lens.astype(np.int64)
+    before = full // 2
+    new_n = full - before
+    new_n[1] += 3 * w.page_size  # runs past its slice
+    new_ptr = np.concatenate([[0], np.cumsum(new_n)]).astype(np.uint32)
+    rows = np.random.default_rng(5).integers(0, 256, (int(new_ptr[-1]), w.row_bytes),
+                                             dtype=np.uint8)
+    b = Batch(w, flags=1, lens=before.astype(np.uint32))
+    host = b.host_pool().copy()
+    rc = hp.hp_scatter_append(b.desc, torch.from_numpy(rows).to("cuda"),
+                              index_tensor(new_ptr, "cuda"), int(new_ptr[-1]), b.ws, b.status)
+    torch.cuda.synchronize()
+    assert rc == 0
+    o = b.oracle_desc(pool_host=host, lens=before.astype(np.uint32))
+    assert o.scatter_append(rows, new_ptr) == "LEN"
+    assert np.array_equal(b.pool.cpu().numpy(), host)
+    assert hp.status_name(b.status_value()) == "HP_ERR_LEN"
