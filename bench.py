@@ -169,7 +169,7 @@ class GatherStep:
         self.T = w.total_tokens
         ob = self.T * w.num_heads * w.head_dim * (2 if self.dequant else inputs.ELEM_BYTES[w.dtype])
         self.out = torch.empty(ob, dtype=torch.uint8, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.status = torch.full((1,), -12345, dtype=torch.int32, device=dev)
 
     def plan(self, stream):
         rc = self.hp.hp_plan(self.desc, self.T, self.ws, self.status, stream=stream)
@@ -332,6 +332,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     w = inputs.config("prefix_sharing")
     st = GatherStep(w, dev, hp, inputs)
     b, spans = gather_bytes(w)
+    st.plan(stream)
     ms = med_ms(lambda: st.copy(stream))
     out["prefix_sharing_gather"] = entry(b, ms, note="logical bytes; the 128 shared pages are "
                                          "read from L2 after their first use")
@@ -344,6 +345,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     T = w.total_tokens
     spans = int((-(-w.lens.astype(np.int64) // w.page_size)).sum())
     b = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
+    st.plan(stream)
     ms = med_ms(lambda: st.copy(stream), n=10)
     out["quantized_pool_dequant_gather"] = entry(b, ms)
     st.check_status()

@@ -58,7 +58,8 @@ def test_lane_gather_append_random(hp, oracle, seed):
     assert rc == 0 and st.item() == 0
     want = oracle.lane_gather(pool_t, C, P, T, B, H, W, n)
     o = out.cpu().numpy()
-    assert np.array_equal(o[:B * H * n * W * es].view(npdt).reshape(B, H, n, W), want)
+    # compare bytes: random bit patterns include NaNs
+    assert np.array_equal(o[:B * H * n * W * es], np.ascontiguousarray(want).view(np.uint8).reshape(-1))
     assert (o[B * H * n * W * es:] == 0xEE).all()
     m = int(rng.integers(0, C - n + 1))
     new = rng.integers(0, 256, (B, H, m, W * es), dtype=np.uint8)
@@ -67,7 +68,7 @@ def test_lane_gather_append_random(hp, oracle, seed):
     assert rc == 0 and st.item() == 0
     host = pool_t.copy()
     assert oracle.lane_append(host, C, P, T, B, H, W, n, new.view(npdt).reshape(B, H, m, W)) == "OK"
-    assert np.array_equal(dpool.cpu().numpy().view(npdt).reshape(host.shape), host)
+    assert np.array_equal(dpool.cpu().numpy().reshape(-1), host.view(np.uint8).reshape(-1))
 
 
 def test_lane_length_and_table_errors(hp, oracle):
