@@ -89,7 +89,9 @@ typedef enum hp_status {
     /* library */
     HP_ERR_WORKSPACE = -29,     /* workspace NULL, misaligned (256 B) or smaller than required */
     HP_ERR_ARG = -30,           /* another argument is invalid (see the function)            */
-    HP_ERR_CUDA = -31           /* the CUDA runtime rejected a launch or a copy               */
+    HP_ERR_CUDA = -31,          /* the CUDA runtime rejected a launch or a copy               */
+    HP_ERR_TIMEOUT = -32        /* a kernel's bounded wait for its own asynchronous copies ran
+                                   out (about 2 s); its output is incomplete                   */
 } hp_status;
 
 /* Name of a status code ("HP_OK", "HP_ERR_RANK", ...); "HP_ERR_UNKNOWN" otherwise. */

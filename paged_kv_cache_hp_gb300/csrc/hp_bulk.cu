@@ -1,0 +1,304 @@
+// hp_bulk.cu -- the TMA bulk-copy engine for pure data movement (gather, append and the
+// per-lane layout) when every row is a multiple of 16 bytes and both bases are 16-byte
+// aligned (the alignment cp.async.bulk requires).
+//
+// One CTA per SM owns a contiguous range of copy units (see hp_copy.cu for the units).
+// Inside the CTA the work is split by role:
+//   warps 1..3  resolve units into a double-buffered descriptor ring in shared memory
+//               (sequence by binary search over the unit prefix, block-table entry,
+//               source/destination offsets, bytes) and hand each batch over through a
+//               "full" mbarrier; they refill a buffer once the "empty" mbarrier says the
+//               producer is done with it;
+//   thread 0    streams the described bytes through a ring of shared-memory stages:
+//               cp.async.bulk global->shared (completion counted on the stage's mbarrier),
+//               then cp.async.bulk shared->global from the same stage.  Up to
+//               kStages-1 loads are in flight while one store drains, across unit and
+//               batch boundaries, so the pipeline never empties until the range ends.
+// Bytes in flight per SM: (kStages-1) * kStage, far above what HBM latency x per-SM
+// bandwidth needs.  Every wait is bounded (about 2 s of %globaltimer); a wait that runs
+// out stores HP_ERR_TIMEOUT in *d_status, stops issuing, waits (again bounded) for the
+// copies already in flight and returns.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "hp_internal.cuh"
+#include "hp_resolve.cuh"
+
+namespace hp {
+namespace {
+
+#ifndef HP_BULK_STAGE
+#define HP_BULK_STAGE 8192
+#endif
+#ifndef HP_BULK_STAGES
+#define HP_BULK_STAGES 24
+#endif
+#ifndef HP_BULK_CTAS_PER_SM
+#define HP_BULK_CTAS_PER_SM 1
+#endif
+#ifndef HP_BULK_STORE_EVICT_FIRST
+#define HP_BULK_STORE_EVICT_FIRST 0
+#endif
+
+constexpr int kThreads = 128;          // warp 0: producer; warps 1-3: resolvers
+constexpr int kResolvers = kThreads - 32;
+constexpr int kBatch = 256;            // units per descriptor buffer
+constexpr uint32_t kStage = HP_BULK_STAGE;  // bytes per ring stage
+constexpr int kStages = HP_BULK_STAGES;     // ring of kStages * kStage bytes
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long now_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false after ~2 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = now_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (now_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes,
+                                           unsigned long long policy)
+{
+#if HP_BULK_STORE_EVICT_FIRST
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(dst), "r"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+#else
+    (void)policy;
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+#endif
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+struct Desc {
+    unsigned long long src[2][kBatch];
+    unsigned long long dst[2][kBatch];
+    unsigned long long bytes[2][kBatch];
+};
+
+template <int MODE, typename IndexT>
+__global__ void __launch_bounds__(kThreads, HP_BULK_CTAS_PER_SM) bulk_kernel(const CopyArgs a)
+{
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) unsigned long long stage_bar[kStages];
+    __shared__ __align__(8) unsigned long long full_bar[2], empty_bar[2];
+    __shared__ Desc desc;
+    __shared__ unsigned long long chunk_dst[kStages];
+    __shared__ uint32_t chunk_bytes[kStages];
+
+    uint64_t total;
+    if (MODE == kGather || MODE == kAppend) {
+        if (a.hdr->verdict != kVerdictOk) return;  // the plan rejected the batch
+        total = a.hdr->total_units;
+    } else {
+        total = a.lane_units;
+    }
+    const uint64_t G = gridDim.x, b = blockIdx.x;
+    const uint64_t per = total / G, rem = total % G;
+    const uint64_t lo = b * per + umin(b, rem);
+    const uint64_t hi = lo + per + (b < rem ? 1 : 0);
+    if (lo >= hi) return;
+    const uint64_t nbatches = (hi - lo + kBatch - 1) / kBatch;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&stage_bar[i]), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), kResolvers);
+            mbar_init(smem_u32(&empty_bar[i]), 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (threadIdx.x >= 32) {
+        // ---------------------------------------------------------------- resolvers
+        const int r = threadIdx.x - 32;
+        for (uint64_t bt = 0; bt < nbatches; ++bt) {
+            const int buf = (int)(bt & 1);
+            if (bt >= 2 && !mbar_wait(smem_u32(&empty_bar[buf]), (uint32_t)((bt / 2 - 1) & 1)))
+                return;  // the producer stopped (it has reported why)
+            const uint64_t base = lo + bt * kBatch;
+            for (int i = r; i < kBatch; i += kResolvers) {
+                const uint64_t u = base + i;
+                if (u < hi) {
+                    const Unit un = resolve<MODE, IndexT>(a, u);
+                    desc.src[buf][i] = un.src;
+                    desc.dst[buf][i] = un.dst;
+                    desc.bytes[buf][i] = (unsigned long long)un.rows * a.row_bytes;
+                }
+            }
+            mbar_arrive(smem_u32(&full_bar[buf]));
+        }
+        return;
+    }
+    if (threadIdx.x != 0) return;
+
+    // -------------------------------------------------------------------- producer
+    // Loads walk the units of batch lb (descriptors in buffer lb & 1); each load records
+    // its destination and size with its stage, so stores need no descriptors.  A
+    // batch's buffer is handed back as soon as its last load is issued.
+    const uint32_t ring0 = smem_u32(ring);
+    uint64_t L = 0, S = 0;   // chunks loaded / stored so far
+    uint64_t lb = 0;         // batch of the load cursor
+    uint32_t li = 0;         // unit of the load cursor within its batch
+    uint64_t loff = 0;       // byte offset of the load cursor within that unit
+    bool have = false;       // descriptors of batch lb observed
+    bool ok = true;
+    unsigned long long policy = 0;
+#if HP_BULK_STORE_EVICT_FIRST
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+#endif
+    while (true) {
+        while (lb < nbatches && L - S < kStages - 1) {
+            const int buf = (int)(lb & 1);
+            if (!have) {
+                const uint32_t fb = smem_u32(&full_bar[buf]);
+                const uint32_t par = (uint32_t)((lb / 2) & 1);
+                // block only when nothing else can progress (no chunk left to store)
+                if (!(S == L ? mbar_wait(fb, par) : mbar_try_wait(fb, par))) {
+                    if (S == L) ok = false;
+                    break;
+                }
+                have = true;
+                li = 0;
+                loff = 0;
+            }
+            if (li == umin(kBatch, hi - lo - lb * kBatch)) {
+                mbar_arrive(smem_u32(&empty_bar[buf]));  // buffer free for batch lb + 2
+                ++lb;
+                have = false;
+                continue;
+            }
+            const unsigned long long nbytes = desc.bytes[buf][li];
+            if (loff >= nbytes) {
+                ++li;
+                loff = 0;
+                continue;
+            }
+            const uint32_t bytes = (uint32_t)umin(kStage, nbytes - loff);
+            const uint32_t st = (uint32_t)(L % kStages);
+            // chunk L - kStages used this stage; its store is at least one group old
+            if (L >= kStages) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            chunk_dst[st] = desc.dst[buf][li] + loff;
+            chunk_bytes[st] = bytes;
+            const uint32_t bar = smem_u32(&stage_bar[st]);
+            mbar_expect_tx(bar, bytes);
+            bulk_load(ring0 + st * kStage, a.src + desc.src[buf][li] + loff, bytes, bar);
+            ++L;
+            loff += bytes;
+        }
+        if (!ok) break;
+        if (S == L) {
+            if (lb >= nbatches) break;  // everything loaded and stored
+            continue;                   // blocks on the next batch's descriptors above
+        }
+        const uint32_t st = (uint32_t)(S % kStages);
+        if (!mbar_wait(smem_u32(&stage_bar[st]), (uint32_t)((S / kStages) & 1))) {
+            ok = false;
+            break;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        bulk_store(a.dst + chunk_dst[st], ring0 + st * kStage, chunk_bytes[st], policy);
+        ++S;
+    }
+    if (!ok) {
+        report(a.d_status, HP_ERR_TIMEOUT);
+        for (; S < L; ++S)  // let the loads in flight land before the CTA's shared memory goes
+            if (!mbar_wait(smem_u32(&stage_bar[S % kStages]), (uint32_t)((S / kStages) & 1))) break;
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int MODE, typename IndexT>
+int launch_t(const CopyArgs& a, cudaStream_t st)
+{
+    auto kern = bulk_kernel<MODE, IndexT>;
+    const int smem = kStages * kStage;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return HP_ERR_CUDA;
+    uint64_t grid = (uint64_t)sms * HP_BULK_CTAS_PER_SM;
+    if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
+    if (grid == 0) return HP_OK;
+    kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, void* stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (mode) {
+    case kGather:
+        return index_u64 ? launch_t<kGather, unsigned long long>(a, st)
+                         : launch_t<kGather, unsigned int>(a, st);
+    case kAppend:
+        return index_u64 ? launch_t<kAppend, unsigned long long>(a, st)
+                         : launch_t<kAppend, unsigned int>(a, st);
+    case kLaneGather:
+        return launch_t<kLaneGather, unsigned long long>(a, st);
+    case kLaneAppend:
+        return launch_t<kLaneAppend, unsigned long long>(a, st);
+    default:
+        return HP_ERR_ARG;
+    }
+}
+
+}  // namespace hp

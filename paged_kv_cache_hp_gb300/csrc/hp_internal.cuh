@@ -132,4 +132,7 @@ struct CopyArgs {
 
 int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* stream);
 
+// The TMA bulk engine (hp_bulk.cu): pure copies whose rows and bases are 16-byte aligned.
+int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, void* stream);
+
 }  // namespace hp
