@@ -186,31 +186,46 @@ class GatherStep:
 
 
 def time_steps(step, steps, warmup, stream, dist=None):
-    """Warm-up, then `steps` timed steps bracketed by barrier + synchronize.
-    Returns (step ms list, copy-kernel ms list, wall seconds of the timed region)."""
+    """Warm-up, then `steps` timed steps (plan + copy, nothing between them) bracketed
+    by barrier + synchronize.  Returns (per-step ms list, wall seconds)."""
     import torch
     for _ in range(warmup):
         step.plan(stream)
         step.copy(stream)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for e0, e1, e2 in ev:
+    for e0, e1 in ev:
         e0.record(stream)
         step.plan(stream)
-        e1.record(stream)
         step.copy(stream)
-        e2.record(stream)
+        e1.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     wall = time.perf_counter() - t0
     step.check_status()
-    return ([a.elapsed_time(c) for a, b, c in ev], [b.elapsed_time(c) for a, b, c in ev], wall)
+    return [a.elapsed_time(b) for a, b in ev], wall
+
+
+def time_copy_kernel(step, launches, stream):
+    """The copy kernel alone, each launch between its own pair of events on the
+    launching stream (the plan of the last step stays valid)."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(launches)]
+    torch.cuda.synchronize()
+    for e0, e1 in ev:
+        e0.record(stream)
+        step.copy(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    step.check_status()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def e2e_gather(w, dev, hp, inputs, steps):
@@ -414,6 +429,10 @@ def main():
     ap.add_argument("--no-ops", action="store_true", help="skip the per-operation measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--workload", default="decode_gather",
+                    choices=["decode_gather", "decode_append", "prefix_sharing", "quantized_pool",
+                             "quantized_pool_mid"],
+                    help="batch the timed steps gather (default: the decode-sized gather)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -422,13 +441,19 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     from paged_kv_cache_hp_gb300 import inputs
-    w = inputs.config("decode_gather")
+    if args.workload == "quantized_pool_mid":
+        w = inputs.config("quantized_pool", "mid")
+    else:
+        w = inputs.config(args.workload)
     T = w.total_tokens
     step_bytes_copy, spans = gather_bytes(w)
+    if w.scales_seed is not None:  # int8 in, 4-byte scale per row, bf16 out
+        step_bytes_copy = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
     step_bytes = step_bytes_copy + validate_bytes(w)
-    config = {"workload": "decode_gather", "num_pages": w.num_pages, "page_size": w.page_size,
+    config = {"workload": w.name, "num_pages": w.num_pages, "page_size": w.page_size,
               "num_heads": w.num_heads, "head_dim": w.head_dim, "pool_dtype": w.dtype,
-              "num_seqs": w.num_seqs, "total_tokens": T, "index": "u32",
+              "num_seqs": w.num_seqs, "total_tokens": T,
+              "index": "u32" if w.index_dtype == np.uint32 else "u64",
               "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (%.2f GB per step)"
               % (step_bytes / 1e9), "parallelism": "replicas x%d" % args.gpus}
 
@@ -480,7 +505,8 @@ def main():
 
     step = GatherStep(w, dev, hp, inputs)
     with ClockSampler(local) as clk:
-        step_ms, copy_ms, wall = time_steps(step, args.steps, args.warmup, stream, dist)
+        step_ms, wall = time_steps(step, args.steps, args.warmup, stream, dist)
+        copy_ms = time_copy_kernel(step, min(args.steps, 500), stream)
     total_ms = sum(step_ms)
     if dist is not None:
         t = torch.tensor([total_ms], device=dev)
@@ -506,7 +532,7 @@ def main():
     d2d_gbps = 2 * a.numel() / (e0.elapsed_time(e1) / 20 * 1e-3) / 1e9
     del a, bb
 
-    traffic = recorded_traffic("gather_decode_gather", spans)
+    traffic = recorded_traffic("gather_" + w.name, spans)
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -517,7 +543,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if traffic is None else int(traffic),
-                     "kernel": "copy_kernel<gather> (hp_gather_planned)",
+                     "kernel": ("copy_kernel<dequant> (hp_gather_dequant_planned)"
+                                if step.dequant else "bulk_kernel<gather> (hp_gather_planned)"),
+                     "kernel_timing": "CUDA events around each of %d copy-only launches "
+                                      "after the timed steps" % len(copy_ms),
                      "peak_kind": peak_kind + " (hbm_gbs, copy)",
                      "algorithmic_bytes_per_launch": step_bytes_copy,
                      "launch_ms_mean": round(copy_mean, 4),
@@ -525,12 +554,12 @@ def main():
                      "d2d_copy_same_bytes_gbps": round(d2d_gbps, 1)},
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_e2e:
+    if rank == 0 and world == 1 and not args.no_e2e and args.workload == "decode_gather":
         ms, h2d, d2h = e2e_gather(w, dev, hp, inputs, steps=5)
         result["e2e"] = {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": round(ms, 3)}
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and w.scales_seed is None:
         import oracle
         oracle.build()
         host_pool = step.pool.cpu().numpy()

@@ -132,6 +132,7 @@ hp::CopyArgs copy_args(const hp_paged_desc* d, const void* ws, int* d_status)
     a.units_off = v.units_off;
     a.row_bytes = row_bytes_of(d);
     a.row_elems = d->num_heads * d->head_dim;
+    a.unit_bytes = d->page_size * a.row_bytes;
     a.d_status = d_status;
     return a;
 }
@@ -165,9 +166,18 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
     a.dst = static_cast<char*>(out);
     int vec;
     if (dequant) {
-        const bool v16 = a.row_elems % 16 == 0 && !misaligned(out, 16) &&
-                         (u128)d->page_size * a.row_elems < ((u128)1 << 36);
-        vec = v16 ? 16 : 1;
+        // groups of 8 elements per thread when rows split into them and a unit's groups
+        // fit 32-bit indices; element by element otherwise
+        const u64 g = a.row_elems / 8;
+        const bool v8 = a.row_elems % 8 == 0 && !misaligned(out, 16) && g <= (1ull << 31) &&
+                        (u128)d->page_size * g < ((u128)1 << 32);
+        if (v8) {
+            uint32_t l = 0;
+            while ((1ull << l) < g) ++l;  // ceil(log2 g)
+            a.div_l = l;
+            a.div_m = (uint32_t)(((((u128)1) << 32) * ((((u128)1) << l) - g)) / g + 1);
+        }
+        vec = v8 ? 16 : 1;
         return hp::launch_copy(hp::kDequant, d->index_type == HP_IDX_U64, a, vec, stream);
     }
     vec = pick_vec(a.row_bytes, d->page_pool, out);
@@ -469,6 +479,7 @@ HP_API int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capa
     a.src = static_cast<const char*>(pool);
     a.dst = static_cast<char*>(out);
     a.row_bytes = rb;
+    a.unit_bytes = page_tokens * rb;
     a.d_status = d_status;
     return hp::launch_copy(hp::kLaneGather, 1, a, pick_vec(rb, pool, out), stream);
 }
@@ -499,6 +510,7 @@ HP_API int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity,
     a.src = static_cast<const char*>(new_rows);
     a.dst = static_cast<char*>(pool);
     a.row_bytes = rb;
+    a.unit_bytes = page_tokens * rb;
     a.d_status = d_status;
     return hp::launch_copy(hp::kLaneAppend, 1, a, pick_vec(rb, new_rows, pool), stream);
 }

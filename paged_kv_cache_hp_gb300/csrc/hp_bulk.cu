@@ -28,15 +28,6 @@
 namespace hp {
 namespace {
 
-#ifndef HP_BULK_STAGE
-#define HP_BULK_STAGE 8192
-#endif
-#ifndef HP_BULK_STAGES
-#define HP_BULK_STAGES 24
-#endif
-#ifndef HP_BULK_CTAS_PER_SM
-#define HP_BULK_CTAS_PER_SM 1
-#endif
 #ifndef HP_BULK_STORE_EVICT_FIRST
 #define HP_BULK_STORE_EVICT_FIRST 0
 #endif
@@ -44,8 +35,6 @@ namespace {
 constexpr int kThreads = 128;          // warp 0: producer; warps 1-3: resolvers
 constexpr int kResolvers = kThreads - 32;
 constexpr int kBatch = 256;            // units per descriptor buffer
-constexpr uint32_t kStage = HP_BULK_STAGE;  // bytes per ring stage
-constexpr int kStages = HP_BULK_STAGES;     // ring of kStages * kStage bytes
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -130,8 +119,10 @@ struct Desc {
     unsigned long long bytes[2][kBatch];
 };
 
-template <int MODE, typename IndexT>
-__global__ void __launch_bounds__(kThreads, HP_BULK_CTAS_PER_SM) bulk_kernel(const CopyArgs a)
+// The ring holds kStages stages of kStage bytes (192 KiB either way): 8 KiB stages
+// suit copy units of 64 KiB and more, 32 KiB stages units of 16-64 KiB (measured).
+template <int MODE, typename IndexT, uint32_t kStage, int kStages>
+__global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const CopyArgs a)
 {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) unsigned long long stage_bar[kStages];
@@ -142,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, HP_BULK_CTAS_PER_SM) bulk_kernel(con
 
     uint64_t total;
     if (MODE == kGather || MODE == kAppend) {
+        pdl_wait();  // the plan (and table check) before this launch must be complete
         if (a.hdr->verdict != kVerdictOk) return;  // the plan rejected the batch
         total = a.hdr->total_units;
     } else {
@@ -263,39 +255,51 @@ __global__ void __launch_bounds__(kThreads, HP_BULK_CTAS_PER_SM) bulk_kernel(con
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-template <int MODE, typename IndexT>
+template <int MODE, typename IndexT, uint32_t kStage, int kStages>
 int launch_t(const CopyArgs& a, cudaStream_t st)
 {
-    auto kern = bulk_kernel<MODE, IndexT>;
+    auto kern = bulk_kernel<MODE, IndexT, kStage, kStages>;
     const int smem = kStages * kStage;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return HP_ERR_CUDA;
-    uint64_t grid = (uint64_t)sms * HP_BULK_CTAS_PER_SM;
+    uint64_t grid = (uint64_t)sms;
     if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
     if (grid == 0) return HP_OK;
-    kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+    if (MODE == kLaneGather || MODE == kLaneAppend) {
+        kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
+        return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+    }
+    return launch_dependent(kern, (unsigned)grid, kThreads, (size_t)smem, st, a) == cudaSuccess
+               ? HP_OK
+               : HP_ERR_CUDA;
+}
+
+template <int MODE, typename IndexT>
+int launch_ring(const CopyArgs& a, int big_stages, cudaStream_t st)
+{
+    return big_stages ? launch_t<MODE, IndexT, 32768, 6>(a, st)
+                      : launch_t<MODE, IndexT, 8192, 24>(a, st);
 }
 
 }  // namespace
 
-int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, void* stream)
+int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, int big_stages, void* stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (mode) {
     case kGather:
-        return index_u64 ? launch_t<kGather, unsigned long long>(a, st)
-                         : launch_t<kGather, unsigned int>(a, st);
+        return index_u64 ? launch_ring<kGather, unsigned long long>(a, big_stages, st)
+                         : launch_ring<kGather, unsigned int>(a, big_stages, st);
     case kAppend:
-        return index_u64 ? launch_t<kAppend, unsigned long long>(a, st)
-                         : launch_t<kAppend, unsigned int>(a, st);
+        return index_u64 ? launch_ring<kAppend, unsigned long long>(a, big_stages, st)
+                         : launch_ring<kAppend, unsigned int>(a, big_stages, st);
     case kLaneGather:
-        return launch_t<kLaneGather, unsigned long long>(a, st);
+        return launch_ring<kLaneGather, unsigned long long>(a, big_stages, st);
     case kLaneAppend:
-        return launch_t<kLaneAppend, unsigned long long>(a, st);
+        return launch_ring<kLaneAppend, unsigned long long>(a, big_stages, st);
     default:
         return HP_ERR_ARG;
     }

@@ -88,6 +88,31 @@ __device__ __forceinline__ void copy_run(const char* __restrict__ src, char* __r
     }
 }
 
+// One warp copies `n` vectors (units small enough that a CTA-wide copy would leave
+// most of each thread's unrolled loads unused).
+template <int VEC>
+__device__ __forceinline__ void copy_run_warp(const char* __restrict__ src, char* __restrict__ dst,
+                                              uint64_t n)
+{
+    using T = typename Vec<VEC>::T;
+    const T* s = reinterpret_cast<const T*>(src);
+    T* d = reinterpret_cast<T*>(dst);
+    const unsigned lane = threadIdx.x & 31;
+    for (uint64_t v0 = lane; v0 < n; v0 += 32 * kUnroll) {
+        T r[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const uint64_t v = v0 + (uint64_t)k * 32;
+            if (v < n) r[k] = ld_stream(s + v);
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const uint64_t v = v0 + (uint64_t)k * 32;
+            if (v < n) st_stream(d + v, r[k]);
+        }
+    }
+}
+
 // The bfloat16 nearest to the exact product q*s (ties to even).  The binary32
 // product p = RN(q*s) rounds to the same bfloat16 as the exact value unless p is
 // itself a bfloat16 midpoint (low 16 bits 0x8000): every midpoint is a binary32
@@ -107,49 +132,90 @@ __device__ __forceinline__ unsigned dq_bf16(float q, float s)
     return r;
 }
 
-__device__ __forceinline__ unsigned dq_pair(unsigned w, int k, float s)
+// Quotient n / d for an invariant divisor d <= 2^31 from a multiply-high and shifts:
+// m = floor(2^32 (2^l - d) / d) + 1 with l = ceil(log2 d), computed on the host
+// (Granlund and Montgomery, "Division by invariant integers using multiplication",
+// PLDI 1994, round-up method).
+__device__ __forceinline__ uint32_t div_invariant(uint32_t n, uint32_t m, uint32_t l)
 {
-    const float lo = (float)(signed char)(w >> (16 * k));
-    const float hi = (float)(signed char)(w >> (16 * k + 8));
-    return dq_bf16(lo, s) | (dq_bf16(hi, s) << 16);
+    if (l == 0) return n;
+    const uint32_t t1 = __umulhi(m, n);
+    return (t1 + ((n - t1) >> 1)) >> (l - 1);
 }
 
-// int8 rows -> bfloat16 rows, 16 elements per vector; rows of `vpr` vectors.
-__device__ __forceinline__ void dequant_run16(const char* __restrict__ src, char* __restrict__ dst,
-                                              const float* __restrict__ scales, uint32_t n,
-                                              uint32_t vpr)
+// Signed byte k of w as a float, exactly: with the sign bit flipped the byte is
+// x + 128 in [0, 255]; placed under the exponent of 2^23 it reads 2^23 + x + 128.
+__device__ __forceinline__ float i8_to_f32(uint32_t w_flipped, uint32_t k)
 {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-    uint4* d = reinterpret_cast<uint4*>(dst);
-    for (uint32_t v0 = threadIdx.x; v0 < n; v0 += kThreads * kUnroll) {
-        uint4 q[kUnroll];
+    return __uint_as_float(__byte_perm(w_flipped, 0x4B000000u, 0x7650u | k)) - 8388736.0f;
+}
+
+// Eight int8 values times one scale -> eight bfloat16 values, each the bfloat16 nearest
+// the exact product.  The fast path rounds the binary32 products with one packed
+// conversion per pair; a product whose low 16 bits are 0x8000 (a bfloat16 midpoint,
+// found with a zero-halfword test over each packed pair) sends the group to dq_bf16.
+__device__ __forceinline__ uint4 dq8(uint2 q, float s)
+{
+    const uint32_t w0 = q.x ^ 0x80808080u, w1 = q.y ^ 0x80808080u;
+    float f[8];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
+    for (int k = 0; k < 4; ++k) {
+        f[k] = i8_to_f32(w0, k);
+        f[4 + k] = i8_to_f32(w1, k);
+    }
+    uint32_t o[4];
+    uint32_t mid = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float p0 = __fmul_rn(f[2 * k], s), p1 = __fmul_rn(f[2 * k + 1], s);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        o[k] = *reinterpret_cast<const uint32_t*>(&h);
+        const uint32_t y =
+            __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x5410u) ^ 0x80008000u;
+        mid |= (y - 0x00010001u) & ~y & 0x80008000u;
+    }
+    if (mid) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = dq_bf16(f[2 * k], s) | (dq_bf16(f[2 * k + 1], s) << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint2 ld_stream8(const uint2* p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+constexpr int kDqUnroll = 16;
+
+// int8 rows -> bfloat16 rows, 8 elements per thread step; `n8` groups of 8, rows of
+// row_elems/8 groups (the row of group v is div_invariant(v, m, l)).
+__device__ __forceinline__ void dequant_run8(const char* __restrict__ src, char* __restrict__ dst,
+                                             const float* __restrict__ scales, uint32_t n8,
+                                             uint32_t m, uint32_t l)
+{
+    const uint2* s = reinterpret_cast<const uint2*>(src);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kDqUnroll) {
+        uint2 q[kDqUnroll];
+#pragma unroll
+        for (int k = 0; k < kDqUnroll; ++k) {
             const uint32_t v = v0 + k * kThreads;
-            if (v < n) q[k] = ld_stream(s + v);
+            if (v < n8) q[k] = ld_stream8(s + v);
         }
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
+        for (int k = 0; k < kDqUnroll; ++k) {
             const uint32_t v = v0 + k * kThreads;
-            if (v < n) {
-                const float sc = __ldg(scales + v / vpr);
-                uint4 o0, o1;
-                o0.x = dq_pair(q[k].x, 0, sc);
-                o0.y = dq_pair(q[k].x, 1, sc);
-                o0.z = dq_pair(q[k].y, 0, sc);
-                o0.w = dq_pair(q[k].y, 1, sc);
-                o1.x = dq_pair(q[k].z, 0, sc);
-                o1.y = dq_pair(q[k].z, 1, sc);
-                o1.z = dq_pair(q[k].w, 0, sc);
-                o1.w = dq_pair(q[k].w, 1, sc);
-                st_stream(d + 2 * v, o0);
-                st_stream(d + 2 * v + 1, o1);
-            }
+            if (v < n8) st_stream(d + v, dq8(q[k], __ldg(scales + div_invariant(v, m, l))));
         }
     }
 }
 
-// Element-wise fallback for rows whose length is not a multiple of 16 elements.
+// Element-wise fallback for rows whose length is not a multiple of 8 elements.
 __device__ __forceinline__ void dequant_run1(const char* __restrict__ src, char* __restrict__ dst,
                                              const float* __restrict__ scales, uint64_t n,
                                              uint64_t row_elems)
@@ -160,7 +226,7 @@ __device__ __forceinline__ void dequant_run1(const char* __restrict__ src, char*
         d[e] = (unsigned short)dq_bf16((float)s[e], __ldg(scales + e / row_elems));
 }
 
-template <int MODE, typename IndexT, int VEC>
+template <int MODE, typename IndexT, int VEC, bool WARP_UNITS>
 __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
 {
     __shared__ unsigned long long s_src[kThreads], s_dst[kThreads], s_scale[kThreads];
@@ -168,6 +234,7 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
 
     uint64_t total;
     if (MODE == kGather || MODE == kDequant || MODE == kAppend) {
+        pdl_wait();  // the plan (and table check) before this launch must be complete
         if (a.hdr->verdict != kVerdictOk) return;  // the plan rejected the batch
         total = a.hdr->total_units;
     } else {
@@ -189,14 +256,21 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
         }
         __syncthreads();
         const int nb = (int)umin(kThreads, hi - u0);
+        if (WARP_UNITS) {
+            for (int i = threadIdx.x >> 5; i < nb; i += kThreads / 32)
+                if (s_rows[i])
+                    copy_run_warp<VEC>(a.src + s_src[i], a.dst + s_dst[i],
+                                       s_rows[i] * a.row_bytes / VEC);
+            __syncthreads();
+            continue;
+        }
         for (int i = 0; i < nb; ++i) {
             const unsigned rows = s_rows[i];
             if (rows == 0) continue;
             if (MODE == kDequant) {
                 if (VEC == 16)
-                    dequant_run16(a.src + s_src[i], a.dst + s_dst[i], a.scales + s_scale[i],
-                                  (uint32_t)(rows * a.row_elems / 16),
-                                  (uint32_t)(a.row_elems / 16));
+                    dequant_run8(a.src + s_src[i], a.dst + s_dst[i], a.scales + s_scale[i],
+                                 (uint32_t)(rows * a.row_elems / 8), a.div_m, a.div_l);
                 else
                     dequant_run1(a.src + s_src[i], a.dst + s_dst[i], a.scales + s_scale[i],
                                  rows * a.row_elems, a.row_elems);
@@ -208,10 +282,10 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
     }
 }
 
-template <int MODE, typename IndexT, int VEC>
+template <int MODE, typename IndexT, int VEC, bool WARP_UNITS>
 int launch_t(const CopyArgs& a, cudaStream_t st)
 {
-    auto kern = copy_kernel<MODE, IndexT, VEC>;
+    auto kern = copy_kernel<MODE, IndexT, VEC, WARP_UNITS>;
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -220,21 +294,36 @@ int launch_t(const CopyArgs& a, cudaStream_t st)
     uint64_t grid = (uint64_t)sms * (uint64_t)std::max(per_sm, 1);
     if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
     if (grid == 0) return HP_OK;
-    kern<<<(unsigned)grid, kThreads, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+    if (MODE == kLaneGather || MODE == kLaneAppend) {
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(a);
+        return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+    }
+    return launch_dependent(kern, (unsigned)grid, kThreads, 0, st, a) == cudaSuccess ? HP_OK
+                                                                                    : HP_ERR_CUDA;
 }
 
+template <int MODE, typename IndexT, bool W>
+int launch_vec_w(const CopyArgs& a, int vec, cudaStream_t st)
+{
+    switch (vec) {
+    case 16: return launch_t<MODE, IndexT, 16, W>(a, st);
+    case 8: return launch_t<MODE, IndexT, 8, W>(a, st);
+    case 4: return launch_t<MODE, IndexT, 4, W>(a, st);
+    case 2: return launch_t<MODE, IndexT, 2, W>(a, st);
+    default: return launch_t<MODE, IndexT, 1, W>(a, st);
+    }
+}
+
+// Units of at most 8 KiB go one per warp; larger ones are copied by the whole CTA.
 template <int MODE, typename IndexT>
 int launch_vec(const CopyArgs& a, int vec, cudaStream_t st)
 {
-    if (MODE == kDequant) return vec == 16 ? launch_t<MODE, IndexT, 16>(a, st)
-                                           : launch_t<MODE, IndexT, 1>(a, st);
-    switch (vec) {
-    case 16: return launch_t<MODE, IndexT, 16>(a, st);
-    case 8: return launch_t<MODE, IndexT, 8>(a, st);
-    case 4: return launch_t<MODE, IndexT, 4>(a, st);
-    case 2: return launch_t<MODE, IndexT, 2>(a, st);
-    default: return launch_t<MODE, IndexT, 1>(a, st);
+    if constexpr (MODE == kDequant) {
+        return vec == 16 ? launch_t<MODE, IndexT, 16, false>(a, st)
+                         : launch_t<MODE, IndexT, 1, false>(a, st);
+    } else {
+        return a.unit_bytes <= 8192 ? launch_vec_w<MODE, IndexT, true>(a, vec, st)
+                                    : launch_vec_w<MODE, IndexT, false>(a, vec, st);
     }
 }
 
@@ -243,8 +332,11 @@ int launch_vec(const CopyArgs& a, int vec, cudaStream_t st)
 int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Engine by copy-unit size (measured on GB300): the TMA ring with 8 KiB stages for
+    // units of 64 KiB and more, with 32 KiB stages for 16-64 KiB, registers below.
 #ifndef HP_COPY_ENGINE_LDG
-    if (vec == 16 && mode != kDequant) return launch_bulk(mode, index_u64, a, stream);
+    if (vec == 16 && mode != kDequant && a.unit_bytes >= 16384)
+        return launch_bulk(mode, index_u64, a, a.unit_bytes < 65536 ? 1 : 0, stream);
 #endif
     switch (mode) {
     case kGather:

@@ -8,6 +8,8 @@
 //                    (page spans of a gather, pages touched by an append)
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 
 #include "hp.h"
@@ -127,12 +129,45 @@ struct CopyArgs {
     char* dst;                // gather: out; append: pool
     uint64_t row_bytes;       // bytes of one source row
     uint64_t row_elems;       // elements of one row (dequant)
+    uint64_t unit_bytes;      // largest unit: page_size rows of row_bytes
+    uint32_t div_m, div_l;    // dequant: divide a group index by row_elems/8
     int* d_status;
 };
 
 int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* stream);
 
 // The TMA bulk engine (hp_bulk.cu): pure copies whose rows and bases are 16-byte aligned.
-int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, void* stream);
+// big_stages selects 32 KiB ring stages (else 8 KiB).
+int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, int big_stages, void* stream);
+
+// ------------------------------------------------------- dependent launches
+// The plan, the block-table check and the copy go into the stream back to back.  The
+// check and the copy are launched as programmatic dependents of the kernel before
+// them, so their CTAs are scheduled while it finishes; each waits (griddepcontrol.wait)
+// before it touches anything that kernel writes, and writes nothing before that wait.
+// The plan itself is launched normally: it overwrites the workspace a previous copy
+// may still be reading.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_dependent(Kernel kernel, unsigned grid, unsigned block, size_t smem,
+                                    cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 }  // namespace hp

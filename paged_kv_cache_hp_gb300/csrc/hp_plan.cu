@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a)
     __shared__ unsigned long long s_key;
     __shared__ int s_fault;
     __shared__ unsigned long long s_carry_rows, s_carry_units;
+    pdl_trigger();  // let the table check start scanning now
     if (threadIdx.x == 0) {
         s_key = kVerdictOk;
         s_fault = HP_OK;
@@ -205,6 +206,8 @@ __global__ void __launch_bounds__(256) table_kernel(const IndexT* __restrict__ t
     __syncthreads();
     if ((threadIdx.x & 31) == 0 && first != ~0ull) atomicMin(&s_first, first);
     __syncthreads();
+    pdl_trigger();  // the copy may be scheduled; it waits for this grid to finish
+    pdl_wait();     // the plan's verdict store must land before it is lowered
     if (threadIdx.x == 0 && s_first != ~0ull) {
         const unsigned long long key = verdict_key(kRankPageId, s_first);
         const unsigned long long old = atomicMin(&hdr->verdict, key);
@@ -230,9 +233,10 @@ int launch_plan_t(PlanMode mode, const PlanArgs& a, cudaStream_t st)
         uint64_t blocks = (a.table_len + 255) / 256;
         const uint64_t cap = (uint64_t)sms * 8;
         if (blocks > cap) blocks = cap;
-        table_kernel<IndexT><<<(unsigned)blocks, 256, 0, st>>>(
-            static_cast<const IndexT*>(a.table), a.table_len, a.num_pages, a.ws.hdr, a.d_status);
-        if (cudaGetLastError() != cudaSuccess) return HP_ERR_CUDA;
+        if (launch_dependent(table_kernel<IndexT>, (unsigned)blocks, 256, 0, st,
+                             static_cast<const IndexT*>(a.table), a.table_len, a.num_pages,
+                             a.ws.hdr, a.d_status) != cudaSuccess)
+            return HP_ERR_CUDA;
     }
     return HP_OK;
 }

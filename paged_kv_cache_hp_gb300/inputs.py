@@ -293,6 +293,8 @@ def config(name: str, scale: str = "full") -> Workload:
         return prefix_sharing(num_pages=700, num_seqs=6, prompt_tokens=200, suf_lo=1,
                               suf_hi=300, name="prefix_sharing_small") if small else prefix_sharing()
     if name == "quantized_pool":
+        if scale == "mid":  # about 2.5 GB moved: small enough for a full profiler capture
+            return quantized_pool(num_pages=50000, num_seqs=128, name="quantized_pool_mid")
         return quantized_pool(num_pages=1500, num_seqs=11, len_lo=1, len_hi=900,
                               name="quantized_pool_small") if small else quantized_pool()
     raise KeyError(name)
