@@ -37,7 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "effective HBM GB/s (bytes read+written) of paged gather/scatter, % of roofline"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-COPY_KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_hp_gb300", "csrc", "hp_copy.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_hp_gb300", "csrc", f)
+                  for f in ("hp_bulk.cu", "hp_resolve.cuh")]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -49,9 +50,12 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(paths):
+    m = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            m.update(f.read())
+    return m.hexdigest()[:16]
 
 
 def recorded_traffic(kernel_key, units_now):
@@ -63,7 +67,8 @@ def recorded_traffic(kernel_key, units_now):
             rec = json.load(f)[kernel_key]
     except Exception:
         return None
-    if rec.get("source_sha256_16") != source_hash(COPY_KERNEL_SOURCE):
+    srcs = [os.path.join(ROOT, p) for p in rec.get("source", [])]
+    if not srcs or rec.get("source_sha256_16") != source_hash(srcs):
         return None
     return rec["dram_bytes_per_unit"] * units_now
 
