@@ -185,11 +185,13 @@ def _need(n, P):
 def _draw_lens(rng, num_seqs, lo, hi, P, num_pages, extra=0):
     """Token counts ~ U[lo, hi] (inclusive); redrawn from the same stream while
     the batch's pages (plus ``extra`` per-sequence slack) exceed the pool."""
-    while True:
+    for _ in range(1000):
         lens = rng.integers(lo, hi, size=num_seqs, endpoint=True)
-        need = sum(_need(n + extra, P) for n in lens)
+        need = int(np.sum(-(-(lens.astype(np.int64) + extra) // P)))
         if need <= num_pages:
             return lens
+    raise ValueError("%d pages cannot hold %d sequences of U[%d, %d] tokens"
+                     % (num_pages, num_seqs, lo, hi))
 
 
 def tiny_prefix_gather() -> Workload:
