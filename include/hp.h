@@ -90,8 +90,9 @@ typedef enum hp_status {
     HP_ERR_WORKSPACE = -29,     /* workspace NULL, misaligned (256 B) or smaller than required */
     HP_ERR_ARG = -30,           /* another argument is invalid (see the function)            */
     HP_ERR_CUDA = -31,          /* the CUDA runtime rejected a launch or a copy               */
-    HP_ERR_TIMEOUT = -32        /* a kernel's bounded wait for its own asynchronous copies ran
+    HP_ERR_TIMEOUT = -32,       /* a kernel's bounded wait for its own asynchronous copies ran
                                    out (about 2 s); its output is incomplete                   */
+    HP_ERR_NOALLOC_LIMIT = -33  /* hp_gather_noalloc: more than HP_NOALLOC_MAX_SEQS sequences */
 } hp_status;
 
 /* Name of a status code ("HP_OK", "HP_ERR_RANK", ...); "HP_ERR_UNKNOWN" otherwise. */
@@ -296,6 +297,33 @@ int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capacity,
 int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity, uint64_t page_tokens,
                    uint64_t batch, uint64_t kv_heads, uint64_t width, uint32_t dtype,
                    uint64_t n, uint64_t m, const void* new_rows, int* d_status, void* stream);
+
+/* ---------------------------------------------------- no-allocation variant */
+/*
+ * ASYNC.  hp_gather without a caller-provided workspace.  (The pages have no counterpart:
+ * this is a convenience of this library.)
+ *
+ * Who needs it: callers that cannot allocate device memory -- a plugin inside a framework
+ * that owns the device's memory budget and gives its plugins buffers but no allocator, or
+ * a latency-critical loop that must not call cudaMalloc/cudaFree (they can block, and
+ * cudaFree synchronises the device).  Inputs and output are as for hp_gather; the plan's
+ * workspace lives instead in one fixed array of device memory inside the library,
+ * sized for HP_NOALLOC_MAX_SEQS sequences (about 257 KiB).  Every device that loads the
+ * library holds that array until the process exits.  This function allocates nothing.
+ *
+ * - num_seqs > HP_NOALLOC_MAX_SEQS returns HP_ERR_NOALLOC_LIMIT before anything else is
+ *   checked; use hp_gather with your own workspace for larger batches.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, which may also load the library's device code on that
+ *   device); make that first call before any stream capture.
+ * - All calls on a device share the one array.  Two calls whose work overlaps on the
+ *   GPU (different streams, or different host threads, without ordering between them)
+ *   race on it and may produce wrong output; order them, e.g. on one stream.  A call
+ *   does not depend on what an earlier call left in the array.
+ */
+#define HP_NOALLOC_MAX_SEQS 16384
+int hp_gather_noalloc(const hp_paged_desc* desc, void* out, uint64_t out_tokens,
+                      int* d_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -307,6 +307,7 @@ HP_API const char* hp_status_string(int s)
         HP_NAME(HP_ERR_ARG)
         HP_NAME(HP_ERR_CUDA)
         HP_NAME(HP_ERR_TIMEOUT)
+        HP_NAME(HP_ERR_NOALLOC_LIMIT)
 #undef HP_NAME
     default: return "HP_ERR_UNKNOWN";
     }

@@ -67,6 +67,7 @@ def lib():
                                        vp, vp, vp]),
                 "hp_lane_append": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32, u64,
                                        u64, vp, vp, vp]),
+                "hp_gather_noalloc": (i, [D, vp, u64, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -206,6 +207,13 @@ def hp_lane_append(pool, table, capacity, page_tokens, batch, kv_heads, width, d
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     return lib().hp_lane_append(_p(pool), _p(table), capacity, page_tokens, batch, kv_heads,
                                 width, dt, n, m, _p(new_rows), _p(d_status), _stream(stream))
+
+
+def hp_gather_noalloc(desc, out, out_tokens, d_status=None, stream=None):
+    """hp_gather with the library's built-in scratch instead of a caller workspace, for
+    callers that cannot allocate device memory (at most 16384 sequences; calls must not
+    overlap on the GPU)."""
+    return lib().hp_gather_noalloc(desc.ref, _p(out), out_tokens, _p(d_status), _stream(stream))
 
 
 def workspace_for(desc: PagedDesc, device="cuda"):
