@@ -152,6 +152,22 @@ def validate_bytes(w):
     return len(w.table) * ib + (2 * w.num_seqs + 1) * ib
 
 
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(step_bytes, steps, world, total_ms):
+    """Every rank moves step_bytes per step (weak scaling); the job's time is the
+    slowest rank's."""
+    return world * step_bytes * steps / (total_ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- device arm
 class GatherStep:
     """Resident device buffers of one gather batch and the two C-ABI calls of a step."""
@@ -512,12 +528,8 @@ def main():
     with ClockSampler(local) as clk:
         step_ms, wall = time_steps(step, args.steps, args.warmup, stream, dist)
         copy_ms = time_copy_kernel(step, min(args.steps, 500), stream)
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    value = whole_job_gbps(step_bytes, args.steps, world, total_ms)
     peak, peak_kind = peak_hbm()
     copy_mean = statistics.mean(copy_ms)
     achieved = step_bytes_copy / (copy_mean * 1e-3) / 1e9
