@@ -353,6 +353,43 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
             ts.append(a.elapsed_time(b))
         return statistics.median(ts)
 
+    def step_us(fn, n=300):
+        """Steps issued back to back, as a decode loop issues them: (issue-bound) time
+        per step, and the same step captured once in a CUDA graph and replayed."""
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        loop = a.elapsed_time(b) / n * 1e3
+        graph = None
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                fn()
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                fn()
+            for _ in range(5):
+                g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(n):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            graph = round(a.elapsed_time(b) / n * 1e3, 2)
+        except Exception as e:  # report, do not hide, a capture failure
+            graph = "capture failed: %s" % str(e).splitlines()[0][:80]
+        return {"us_per_step_back_to_back": round(loop, 2), "us_per_step_graph": graph}
+
     def entry(bytes_, ms, **kw):
         gbps = bytes_ / (ms * 1e-3) / 1e9
         return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
@@ -360,8 +397,9 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     # tiny prefix-sharing gather: latency
     w = inputs.tiny_prefix_gather()
     st = GatherStep(w, dev, hp, inputs)
-    ms = med_ms(lambda: (st.plan(stream), st.copy(stream)))
-    out["tiny_prefix_gather"] = {"us_per_step": round(ms * 1e3, 2)}
+    # stream=None: the binding uses torch's current stream, the capture stream inside a graph
+    out["tiny_prefix_gather"] = step_us(lambda: (st.plan(None), st.copy(None)))
+    st.check_status()
     del st
 
     # prefix sharing at scale
@@ -400,9 +438,9 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     d_app = hp.PagedDesc(pool, table, sp, before, **kw)
     ws = hp.workspace_for(d_app, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ms = med_ms(lambda: hp.hp_scatter_append(d_app, new, new_ptr, w.total_new, ws, status), n=50)
-    out["decode_append_step"] = {"us_per_step": round(ms * 1e3, 2), "rows": w.total_new,
-                                 "bytes": 2 * w.total_new * w.row_bytes}
+    out["decode_append_step"] = dict(
+        step_us(lambda: hp.hp_scatter_append(d_app, new, new_ptr, w.total_new, ws, status)),
+        rows=w.total_new, bytes=2 * w.total_new * w.row_bytes)
     d_g = hp.PagedDesc(pool, table, sp, after, **kw)
     T = w.total_tokens
     o = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)
@@ -415,7 +453,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     d_bulk = hp.PagedDesc(pool, table, sp, zeros, **kw)
     np_bulk = idx_tensor(np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))]).astype(np.uint32), dev)
     assert hp.hp_append_plan(d_bulk, np_bulk, T, ws, status) == 0
-    ms = med_ms(lambda: hp.hp_scatter_append_planned(d_bulk, o, np_bulk, ws, status), n=10)
+    ms = med_ms(lambda: hp.hp_scatter_append_planned(d_bulk, o, np_bulk, T, ws, status), n=10)
     out["bulk_scatter_append"] = entry(b, ms)
     assert int(status.item()) == 0, hp.status_name(int(status.item()))
     del pool, o, new
@@ -432,10 +470,9 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
                                           lw.kv_heads, lw.width, "bf16", lw.n, lo, status))
     out["lane_gather"] = entry(2 * lw.lanes * lw.n * lw.width * 2 + lw.pages * 8, ms)
     lnew = torch.randn((lw.batch, lw.kv_heads, 1, lw.width), device=dev).to(torch.bfloat16)
-    ms = med_ms(lambda: hp.hp_lane_append(lpool, lt, lw.capacity, lw.page_tokens, lw.batch,
-                                          lw.kv_heads, lw.width, "bf16", lw.n, 1, lnew, status),
-                n=50)
-    out["lane_append_step"] = {"us_per_step": round(ms * 1e3, 2)}
+    out["lane_append_step"] = step_us(
+        lambda: hp.hp_lane_append(lpool, lt, lw.capacity, lw.page_tokens, lw.batch, lw.kv_heads,
+                                  lw.width, "bf16", lw.n, 1, lnew, status))
     assert int(status.item()) == 0
     return out
 

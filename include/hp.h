@@ -18,9 +18,10 @@
  *   hp_status_string() names it.  Nothing aborts or prints.
  * - Pointers named d_* or described as "device" point to GPU memory of the
  *   current CUDA device; pointers described as "host" point to CPU memory.
- *   The caller owns every buffer.  The library allocates no device memory and
- *   keeps no state between calls; it is safe to call from several host threads
- *   on different streams.
+ *   The caller owns every buffer.  The library allocates no device memory; the
+ *   only state it keeps between calls is a per-device cache of launch facts (SM
+ *   count, resident CTAs per kernel), filled on first use.  It is safe to call from
+ *   several host threads on different streams.
  * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *   stream.  Functions marked ASYNC only enqueue work on `stream` and return
  *   once it is enqueued; functions marked SYNC wait for their own work.
@@ -247,10 +248,11 @@ int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, const voi
 int hp_append_plan(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,
                    void* workspace, uint64_t workspace_bytes, int* d_status, void* stream);
 
-/* ASYNC.  The copy step of hp_scatter_append, after hp_append_plan on the same stream. */
+/* ASYNC.  The copy step of hp_scatter_append, after hp_append_plan (with the same
+ * new_ptr and total_new) on the same stream. */
 int hp_scatter_append_planned(const hp_paged_desc* desc, const void* new_rows,
-                              const void* new_ptr, const void* workspace, int* d_status,
-                              void* stream);
+                              const void* new_ptr, uint64_t total_new, const void* workspace,
+                              int* d_status, void* stream);
 
 /* SYNC.  The verdict hp_append_plan reaches, returned like hp_validate's. */
 int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,

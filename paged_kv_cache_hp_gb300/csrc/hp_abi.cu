@@ -215,13 +215,17 @@ int plan_append(const hp_paged_desc* d, const void* new_ptr, u64 total_new, void
 }
 
 int append_planned(const hp_paged_desc* d, const void* new_rows, const void* new_ptr,
-                   const void* ws, int* d_status, void* stream)
+                   u64 total_new, const void* ws, int* d_status, void* stream)
 {
     if (!ws || misaligned(ws, 256)) return HP_ERR_WORKSPACE;
     if (d->num_seqs == 0) return HP_OK;
     if (!new_ptr) return HP_ERR_NULL;
     hp::CopyArgs a = copy_args(d, ws, d_status);
     a.new_ptr = new_ptr;
+    // a unit is at most one page of rows, and on average total_new / num_seqs rows: a
+    // decode step's single rows take the low-latency register path
+    const u64 avg_rows = total_new / d->num_seqs + (total_new % d->num_seqs != 0);
+    if (avg_rows < d->page_size) a.unit_bytes = avg_rows * a.row_bytes;
     a.src = static_cast<const char*>(new_rows);
     a.dst = static_cast<char*>(const_cast<void*>(d->page_pool));
     if (!a.src) a.src = reinterpret_cast<const char*>(d->page_pool);  // no rows: never read
@@ -385,12 +389,12 @@ HP_API int hp_append_plan(const hp_paged_desc* desc, const void* new_ptr, uint64
 }
 
 HP_API int hp_scatter_append_planned(const hp_paged_desc* desc, const void* new_rows,
-                                     const void* new_ptr, const void* workspace, int* d_status,
-                                     void* stream)
+                                     const void* new_ptr, uint64_t total_new,
+                                     const void* workspace, int* d_status, void* stream)
 {
     int rc = check_desc(desc);
     if (rc) return rc;
-    return append_planned(desc, new_rows, new_ptr, workspace, d_status, stream);
+    return append_planned(desc, new_rows, new_ptr, total_new, workspace, d_status, stream);
 }
 
 HP_API int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, const void* new_ptr,
@@ -402,7 +406,7 @@ HP_API int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, co
     if (total_new && !new_rows) return HP_ERR_NULL;
     rc = plan_append(desc, new_ptr, total_new, workspace, workspace_bytes, d_status, stream);
     if (rc) return rc;
-    return append_planned(desc, new_rows, new_ptr, workspace, d_status, stream);
+    return append_planned(desc, new_rows, new_ptr, total_new, workspace, d_status, stream);
 }
 
 HP_API int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,

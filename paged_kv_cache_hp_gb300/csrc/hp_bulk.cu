@@ -260,10 +260,9 @@ int launch_t(const CopyArgs& a, cudaStream_t st)
 {
     auto kern = bulk_kernel<MODE, IndexT, kStage, kStages>;
     const int smem = kStages * kStage;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms == 0 || !allow_dynamic_smem<bulk_kernel<MODE, IndexT, kStage, kStages>>(dev, smem))
         return HP_ERR_CUDA;
     uint64_t grid = (uint64_t)sms;
     if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);

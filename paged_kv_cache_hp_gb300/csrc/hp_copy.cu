@@ -286,12 +286,12 @@ template <int MODE, typename IndexT, int VEC, bool WARP_UNITS>
 int launch_t(const CopyArgs& a, cudaStream_t st)
 {
     auto kern = copy_kernel<MODE, IndexT, VEC, WARP_UNITS>;
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess)
-        return HP_ERR_CUDA;
-    uint64_t grid = (uint64_t)sms * (uint64_t)std::max(per_sm, 1);
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    const int per_sm =
+        sms ? resident_ctas<copy_kernel<MODE, IndexT, VEC, WARP_UNITS>>(dev, kThreads, 0) : 0;
+    if (sms == 0 || per_sm == 0) return HP_ERR_CUDA;
+    uint64_t grid = (uint64_t)sms * (uint64_t)per_sm;
     if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
     if (grid == 0) return HP_OK;
     if (MODE == kLaneGather || MODE == kLaneAppend) {

@@ -10,6 +10,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "hp.h"
@@ -139,6 +140,53 @@ int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* 
 // The TMA bulk engine (hp_bulk.cu): pure copies whose rows and bases are 16-byte aligned.
 // big_stages selects 32 KiB ring stages (else 8 KiB).
 int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, int big_stages, void* stream);
+
+// ------------------------------------------------------- per-device launch facts
+// Looked up on first use on each device and kept for the process: the launch path then
+// costs no runtime queries (a decode step's latency is mostly launch overhead).
+constexpr int kMaxDevices = 256;
+
+// SM count of the current device (0 if it cannot be read); *dev receives the ordinal.
+inline int current_sms(int* dev)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return 0;
+    int v = cache[*dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+            return 0;
+        cache[*dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Resident CTAs per SM of `kernel` on `dev` (one cache per kernel).
+template <auto kernel>
+inline int resident_ctas(int dev, int threads, size_t smem)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, smem) != cudaSuccess)
+            return 0;
+        if (v < 1) v = 1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Raises `kernel`'s dynamic shared-memory limit on `dev` once.
+template <auto kernel>
+inline bool allow_dynamic_smem(int dev, int bytes)
+{
+    static std::atomic<int> done[kMaxDevices];
+    if (done[dev].load(std::memory_order_acquire)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return false;
+    done[dev].store(1, std::memory_order_release);
+    return true;
+}
 
 // ------------------------------------------------------- dependent launches
 // The plan, the block-table check and the copy go into the stream back to back.  The

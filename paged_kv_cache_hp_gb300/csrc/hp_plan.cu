@@ -226,10 +226,9 @@ int launch_plan_t(PlanMode mode, const PlanArgs& a, cudaStream_t st)
         plan_kernel<IndexT, kPlanAppend><<<1, kPlanThreads, 0, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return HP_ERR_CUDA;
     if (a.strict && a.table_len > 0) {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return HP_ERR_CUDA;
+        int dev = 0;
+        const int sms = current_sms(&dev);
+        if (sms == 0) return HP_ERR_CUDA;
         uint64_t blocks = (a.table_len + 255) / 256;
         const uint64_t cap = (uint64_t)sms * 8;
         if (blocks > cap) blocks = cap;

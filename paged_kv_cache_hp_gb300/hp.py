@@ -60,7 +60,7 @@ def lib():
                 "hp_gather_dequant_planned": (i, [D, vp, vp, vp, vp]),
                 "hp_scatter_append": (i, [D, vp, vp, u64, vp, u64, vp, vp]),
                 "hp_append_plan": (i, [D, vp, u64, vp, u64, vp, vp]),
-                "hp_scatter_append_planned": (i, [D, vp, vp, vp, vp, vp]),
+                "hp_scatter_append_planned": (i, [D, vp, vp, u64, vp, vp, vp]),
                 "hp_validate_append": (i, [D, vp, u64, vp, u64, pu64, vp]),
                 "hp_lane_validate": (i, [u64, u64, vp, u64, pu64]),
                 "hp_lane_gather": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32, u64,
@@ -181,9 +181,10 @@ def hp_append_plan(desc, new_ptr, total_new, workspace, d_status=None, stream=No
                                 _p(d_status), _stream(stream))
 
 
-def hp_scatter_append_planned(desc, new_rows, new_ptr, workspace, d_status=None, stream=None):
-    return lib().hp_scatter_append_planned(desc.ref, _p(new_rows), _p(new_ptr), _p(workspace),
-                                           _p(d_status), _stream(stream))
+def hp_scatter_append_planned(desc, new_rows, new_ptr, total_new, workspace, d_status=None,
+                              stream=None):
+    return lib().hp_scatter_append_planned(desc.ref, _p(new_rows), _p(new_ptr), total_new,
+                                           _p(workspace), _p(d_status), _stream(stream))
 
 
 def hp_lane_validate(capacity, page_tokens, table_host):

@@ -183,3 +183,19 @@ def test_permissive_append_skips_unwritable_rows(hp, oracle):
     assert o.scatter_append(rows, new_ptr) == "LEN"
     assert np.array_equal(b.pool.cpu().numpy(), host)
     assert hp.status_name(b.status_value()) == "HP_ERR_LEN"
+
+
+def test_planned_append_steps_equal_one_call(hp, oracle):
+    """hp_append_plan + hp_scatter_append_planned on one stream is hp_scatter_append."""
+    import torch
+    w = inputs.config("decode_append", "small")
+    b1 = Batch(w, lens=w.lens_before)
+    b2 = Batch(w, lens=w.lens_before, pool=b1.pool.clone())
+    new = inputs.device_new_rows(w, "cuda")
+    npd = index_tensor(w.new_ptr, "cuda")
+    assert hp.hp_scatter_append(b1.desc, new, npd, w.total_new, b1.ws, b1.status) == 0
+    assert hp.hp_append_plan(b2.desc, npd, w.total_new, b2.ws, b2.status) == 0
+    assert hp.hp_scatter_append_planned(b2.desc, new, npd, w.total_new, b2.ws, b2.status) == 0
+    torch.cuda.synchronize()
+    assert b1.status_value() == 0 and b2.status_value() == 0
+    assert torch.equal(b1.pool, b2.pool)
