@@ -55,6 +55,16 @@ class OrDesc(ctypes.Structure):
                 ("addr_pool", "addr_table", "addr_seq_ptr", "addr_lens", "addr_scales")]
 
 
+class OrQuant(ctypes.Structure):
+    _fields_ = [("scheme_tag", ctypes.c_uint32), ("axis", ctypes.c_uint32),
+                ("block_size", ctypes.c_uint64), ("count", ctypes.c_uint64),
+                ("scales", ctypes.c_void_p), ("zero_points", ctypes.c_void_p),
+                ("addr_scales", ctypes.c_uint64), ("addr_zero_points", ctypes.c_uint64)]
+
+
+PER_TENSOR, PER_CHANNEL, PER_BLOCK_AFFINE = 0x01, 0x02, 0x03
+
+
 def lib():
     global _lib
     with _lock:
@@ -97,6 +107,14 @@ def lib():
             L.or_lane_gather.argtypes = [vp, u64, u64, vp, u64, u64, u64, u64, u64, vp]
             L.or_lane_append.restype = i32
             L.or_lane_append.argtypes = [vp, u64, u64, vp, u64, u64, u64, u64, u64, u64, vp]
+            Q = P(OrQuant)
+            L.or_validate_quant.restype = i32
+            L.or_validate_quant.argtypes = [P(OrDesc), Q]
+            L.or_lookup_dequant_q.restype = i32
+            L.or_lookup_dequant_q.argtypes = [P(OrDesc), Q, u64, u64, u64, u64,
+                                              P(ctypes.c_uint16)]
+            L.or_gather_dequant_q.restype = i32
+            L.or_gather_dequant_q.argtypes = [P(OrDesc), Q, vp, vp]
             L.or_payload.restype = i32
             L.or_payload.argtypes = [u64, u64, u64, u64, u64, u64, P(u64)]
             _lib = L
@@ -203,6 +221,43 @@ class Desc:
             out = np.zeros((T, self.c.num_heads * self.c.head_dim), dtype=np.uint16)
         written = np.zeros(max(T, 1), dtype=np.uint8)
         c = lib().or_gather_dequant(ctypes.byref(self.c), _ptr(out), _ptr(written))
+        return out, written[:T].astype(bool), code_name(c)
+
+    # -- quantization schemes ----------------------------------------------
+    @staticmethod
+    def quant(scheme_tag, scales, zero_points=None, axis=0, block_size=0, count=None,
+              addrs=None):
+        """An OrQuant over host arrays (kept alive on the returned object's `keep`)."""
+        sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.float32)
+        zp = None if zero_points is None else np.ascontiguousarray(zero_points)
+        q = OrQuant()
+        q.scheme_tag, q.axis, q.block_size = scheme_tag, axis, block_size
+        q.count = (0 if sc is None else len(sc)) if count is None else count
+        q.scales, q.zero_points = _ptr(sc), _ptr(zp)
+        a = {"scales": 64 * 8 if sc is not None else 0, "zero_points": 64 * 9 if zp is not None else 0}
+        if addrs:
+            a.update(addrs)
+        q.addr_scales, q.addr_zero_points = a["scales"], a["zero_points"]
+        q.keep = (sc, zp)
+        return q
+
+    def validate_quant(self, q):
+        return code_name(lib().or_validate_quant(ctypes.byref(self.c), ctypes.byref(q)))
+
+    def lookup_dequant_q(self, q, s, t, h, d):
+        v = ctypes.c_uint16(0)
+        c = lib().or_lookup_dequant_q(ctypes.byref(self.c), ctypes.byref(q), s, t, h, d,
+                                      ctypes.byref(v))
+        return code_name(c), v.value
+
+    def gather_dequant_q(self, q, out=None):
+        """Returns (out uint16 bf16 codes [T, H*D], rows_written mask, fault name)."""
+        T = self.total_tokens()
+        if out is None:
+            out = np.zeros((T, self.c.num_heads * self.c.head_dim), dtype=np.uint16)
+        written = np.zeros(max(T, 1), dtype=np.uint8)
+        c = lib().or_gather_dequant_q(ctypes.byref(self.c), ctypes.byref(q), _ptr(out),
+                                      _ptr(written))
         return out, written[:T].astype(bool), code_name(c)
 
     def scatter_append(self, new_rows, new_ptr):

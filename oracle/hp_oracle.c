@@ -62,6 +62,9 @@ enum {
     OR_ALIASED_PAGE,
     OR_LENGTH,
     OR_ALLOCATION_FAILED,
+    /* quantization schemes ([HF] Per-scheme composition) */
+    OR_QUANT_SCHEME,
+    OR_QUANT_BLOCK,
     OR_NCODES
 };
 
@@ -71,7 +74,7 @@ static const char* const or_names[OR_NCODES] = {
     "SEQ_PTR_END", "PAGE_ID", "LEN", "NEW_PTR_START", "NEW_PTR_ORDER",
     "NEW_PTR_END", "CAPACITY", "OUT_SIZE", "ZERO_CAPACITY", "ZERO_PAGE_SIZE",
     "LANE_OVERFLOW", "PAGE_COUNT", "PHYSICAL_PAGE", "ALIASED_PAGE", "LENGTH",
-    "ALLOCATION_FAILED"};
+    "ALLOCATION_FAILED", "QUANT_SCHEME", "QUANT_BLOCK"};
 
 const char* or_code_name(int code)
 {
@@ -338,6 +341,104 @@ int or_gather_dequant(const or_desc* d, uint16_t* out, unsigned char* row_writte
             for (uint64_t h = 0; h < H; ++h)
                 for (uint64_t dd = 0; dd < D; ++dd) {
                     or_lookup_dequant(d, s, t, h, dd, &v);
+                    out[(row * H + h) * D + dd] = v;
+                }
+        }
+    }
+    return first_fault;
+}
+
+/* ------------------------------------------------- quantization schemes -- */
+/* [HF] Quantization Compatibility, Per-scheme composition.  A scheme tag with its axis
+ * and block size, the scale count, fp32 scales and optional zero points of the pool's
+ * element type (host copies), and the addresses a reader sees. */
+typedef struct or_quant {
+    uint32_t scheme_tag, axis;
+    uint64_t block_size, count;
+    const float* scales;
+    const void* zero_points; /* NULL: symmetric, zero point 0 */
+    uint64_t addr_scales, addr_zero_points;
+} or_quant;
+
+enum { OR_PER_TENSOR = 0x01, OR_PER_CHANNEL = 0x02, OR_PER_BLOCK_AFFINE = 0x03 };
+
+/* The checks on a scheme, in this order: the pool holds 8-bit integers; the tag is one
+ * of 0x01, 0x02, 0x03; a per-channel axis is 1 (num_heads) or 2 (head_dim) -- the paged
+ * axis must not be quantized per channel; a per-block-affine scheme has axis 0 and
+ * block_size == page_size (a reader must reject it otherwise); the count is what the
+ * scheme needs (1; num_heads or head_dim; num_pages*page_size per [HF] Scale-buffer
+ * size); scales are present; both buffers are 64-byte aligned ([HF] Alignment). */
+int or_validate_quant(const or_desc* d, const or_quant* q)
+{
+    if (d->dtype != OR_I8 && d->dtype != OR_U8) return OR_DTYPE;
+    uint64_t want;
+    if (q->scheme_tag == OR_PER_TENSOR) {
+        want = 1;
+    } else if (q->scheme_tag == OR_PER_CHANNEL) {
+        if (q->axis == 1) want = d->num_heads;
+        else if (q->axis == 2) want = d->head_dim;
+        else return OR_QUANT_SCHEME;
+    } else if (q->scheme_tag == OR_PER_BLOCK_AFFINE) {
+        if (q->axis != 0 || q->block_size != d->page_size) return OR_QUANT_BLOCK;
+        unsigned __int128 n = (unsigned __int128)d->num_pages * d->page_size;
+        if (n >> 64) return OR_SCALES;
+        want = (uint64_t)n;
+    } else {
+        return OR_QUANT_SCHEME;
+    }
+    if (q->count != want) return OR_SCALES;
+    if (q->addr_scales == 0) return OR_NULL;
+    if (q->addr_scales % 64 || q->addr_zero_points % 64) return OR_ALIGN;
+    return OR_OK;
+}
+
+/* [HF] Element Lookup, quantized case, under a scheme: the pool element q at (s,t,h,d),
+ * the parameter entry the scheme assigns it (0; h or d; phys_page*page_size +
+ * offset_in_page), and the bfloat16 nearest the exact (q - zero_point) * scale -- formed
+ * in double, exact for 8-bit integers and a 24-bit significand, rounded once. */
+int or_lookup_dequant_q(const or_desc* d, const or_quant* q, uint64_t s, uint64_t t,
+                        uint64_t h, uint64_t dd, uint16_t* value)
+{
+    uint64_t flat, phys, off;
+    int c = lookup_flat(d, s, t, h, dd, &flat, &phys, &off);
+    if (c != OR_OK) return c;
+    uint64_t k;
+    if (q->scheme_tag == OR_PER_TENSOR) k = 0;
+    else if (q->scheme_tag == OR_PER_CHANNEL) k = q->axis == 1 ? h : dd;
+    else k = phys * d->page_size + off;
+    double qv, zp = 0.0;
+    if (d->dtype == OR_I8) {
+        qv = ((const int8_t*)d->page_pool)[flat];
+        if (q->zero_points) zp = ((const int8_t*)q->zero_points)[k];
+    } else {
+        qv = ((const uint8_t*)d->page_pool)[flat];
+        if (q->zero_points) zp = ((const uint8_t*)q->zero_points)[k];
+    }
+    *value = or_bf16_rne((qv - zp) * (double)q->scales[k]);
+    return OR_OK;
+}
+
+/* The dequantising gather under a scheme: or_gather with each element replaced by
+ * or_lookup_dequant_q's value. */
+int or_gather_dequant_q(const or_desc* d, const or_quant* q, uint16_t* out,
+                        unsigned char* row_written)
+{
+    const uint64_t H = d->num_heads, D = d->head_dim;
+    int first_fault = OR_OK;
+    uint64_t row = 0;
+    for (uint64_t s = 0; s < d->num_seqs; ++s) {
+        const uint64_t len = ix(d, d->seq_lens, s);
+        for (uint64_t t = 0; t < len; ++t, ++row) {
+            uint16_t v;
+            int c = or_lookup_dequant_q(d, q, s, t, 0, 0, &v);
+            if (row_written) row_written[row] = (c == OR_OK);
+            if (c != OR_OK) {
+                if (first_fault == OR_OK) first_fault = c;
+                continue;
+            }
+            for (uint64_t h = 0; h < H; ++h)
+                for (uint64_t dd = 0; dd < D; ++dd) {
+                    or_lookup_dequant_q(d, q, s, t, h, dd, &v);
                     out[(row * H + h) * D + dd] = v;
                 }
         }
