@@ -423,6 +423,24 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     ms = med_ms(lambda: st.copy(stream), n=10)
     out["quantized_pool_dequant_gather"] = entry(b, ms)
     st.check_status()
+    # the other schemes of [HF] Per-scheme composition on the same pool, with zero points
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.scales_seed + 1)
+    for name, tag, axis, count in (("per_tensor", 0x01, 0, 1),
+                                   ("per_channel_heads", 0x02, 1, w.num_heads),
+                                   ("per_channel_head_dim", 0x02, 2, w.head_dim),
+                                   ("per_slot_affine", 0x03, 0, w.num_pages * w.page_size)):
+        sc = torch.rand(count, generator=g, device=dev) * 0.049 + 0.001
+        zp = torch.randint(-20, 21, (count,), generator=g, device=dev,
+                           dtype=torch.int8).view(torch.uint8)
+        q = hp.quant_desc(tag, sc, zp, axis=axis, block_size=w.page_size if tag == 3 else 0)
+        ms = med_ms(lambda: hp.hp_gather_dequant_q_planned(st.desc, q, st.out, st.ws, st.status),
+                    n=5)
+        # b counts a 4-byte scale per row; per-slot zero points add one byte per row, the
+        # other schemes' parameters are a few hundred bytes read from cache
+        nbytes = b + T if tag == 3 else b - 4 * T
+        out["quantized_pool_dequant_" + name + "_zp"] = entry(nbytes, ms)
+        st.check_status()
     del st
     torch.cuda.empty_cache()
 

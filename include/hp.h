@@ -93,7 +93,11 @@ typedef enum hp_status {
     HP_ERR_CUDA = -31,          /* the CUDA runtime rejected a launch or a copy               */
     HP_ERR_TIMEOUT = -32,       /* a kernel's bounded wait for its own asynchronous copies ran
                                    out (about 2 s); its output is incomplete                   */
-    HP_ERR_NOALLOC_LIMIT = -33  /* hp_gather_noalloc: more than HP_NOALLOC_MAX_SEQS sequences */
+    HP_ERR_NOALLOC_LIMIT = -33, /* hp_gather_noalloc: more than HP_NOALLOC_MAX_SEQS sequences */
+    HP_ERR_QUANT_SCHEME = -34,  /* unknown scheme tag, or per-channel on an axis other than
+                                   1 (num_heads) or 2 (head_dim)                             */
+    HP_ERR_QUANT_BLOCK = -35    /* [HF] Per-scheme composition: per-block-affine whose axis is
+                                   not 0 or whose block_size is not page_size                */
 } hp_status;
 
 /* Name of a status code ("HP_OK", "HP_ERR_RANK", ...); "HP_ERR_UNKNOWN" otherwise. */
@@ -224,6 +228,61 @@ int hp_gather_dequant(const hp_paged_desc* desc, void* out_bf16, uint64_t out_to
 /* ASYNC.  The copy step of hp_gather_dequant, after hp_plan on the same stream. */
 int hp_gather_dequant_planned(const hp_paged_desc* desc, void* out_bf16, const void* workspace,
                               int* d_status, void* stream);
+
+/* ------------------------------------------------------ quantization schemes */
+/*
+ * [HF] Quantization Compatibility, Per-scheme composition: how a quantization scheme
+ * composes with the paged structure.
+ *   HP_QUANT_PER_TENSOR (0x01)        one scale (and zero point) for the whole tensor;
+ *   HP_QUANT_PER_CHANNEL (0x02)       one per channel along axis 1 (num_heads) or 2
+ *                                     (head_dim), independent of the pages; axis 0 is
+ *                                     rejected (a writer must not quantize the paged axis
+ *                                     per channel);
+ *   HP_QUANT_PER_BLOCK_AFFINE (0x03)  only with axis 0 and block_size == page_size, where
+ *                                     its blocks are the page slots: scale of page p, slot i
+ *                                     at p*page_size + i ([HF] Per-page-slot parameters);
+ *                                     any other axis or block size is rejected.
+ * The value of element (s, t, h, d) is the bfloat16 nearest (ties to even) to the exact
+ * (q - zero_point) * scale, where q is the pool element the Element Lookup names and the
+ * scale and zero point are the entries the scheme assigns it; zero_points == NULL is the
+ * symmetric case (zero point 0).  The affine form (q - zero_point) * scale is this
+ * library's reading of the scheme bodies, which the specification keeps in a separate
+ * document.
+ */
+typedef enum hp_quant_scheme {
+    HP_QUANT_PER_TENSOR = 0x01,
+    HP_QUANT_PER_CHANNEL = 0x02,
+    HP_QUANT_PER_BLOCK_AFFINE = 0x03
+} hp_quant_scheme;
+
+typedef struct hp_quant_desc {
+    uint32_t scheme_tag;      /* hp_quant_scheme */
+    uint32_t axis;            /* per-channel: 1 or 2; per-block-affine: must be 0 */
+    uint64_t block_size;      /* per-block-affine: must equal page_size */
+    uint64_t count;           /* entries in scales (and zero_points): 1, num_heads or
+                                 head_dim, or num_pages*page_size ([HF] Scale-buffer size) */
+    const float* scales;      /* device, fp32, 64-byte aligned */
+    const void* zero_points;  /* device, `count` entries of the pool's element type (int8 or
+                                 uint8), 64-byte aligned; NULL for a symmetric scheme */
+} hp_quant_desc;
+
+/*
+ * ASYNC.  Dequantising gather under an explicit scheme.  desc->dtype must be HP_I8 or
+ * HP_U8; the parameters come from `quant` (desc->flags' HP_HAS_QUANT, desc->scales and
+ * desc->scales_len are not used).  Host checks, in order: quant NULL (HP_ERR_NULL),
+ * element type (HP_ERR_DTYPE), scheme tag and per-channel axis (HP_ERR_QUANT_SCHEME),
+ * per-block-affine axis and block size (HP_ERR_QUANT_BLOCK), count (HP_ERR_SCALES),
+ * NULL scales (HP_ERR_NULL), alignment (HP_ERR_ALIGN); then as hp_gather_dequant.
+ * `out_bf16` holds out_tokens rows of num_heads*head_dim bfloat16.
+ */
+int hp_gather_dequant_q(const hp_paged_desc* desc, const hp_quant_desc* quant, void* out_bf16,
+                        uint64_t out_tokens, void* workspace, uint64_t workspace_bytes,
+                        int* d_status, void* stream);
+
+/* ASYNC.  The copy step of hp_gather_dequant_q, after hp_plan on the same stream. */
+int hp_gather_dequant_q_planned(const hp_paged_desc* desc, const hp_quant_desc* quant,
+                                void* out_bf16, const void* workspace, int* d_status,
+                                void* stream);
 
 /* ------------------------------------------------------------------- append */
 /*

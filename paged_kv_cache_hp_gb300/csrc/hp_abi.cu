@@ -149,12 +149,53 @@ int sync_verdict(const void* ws, u64* first_bad, void* stream)
     return hp::key_status(key);
 }
 
+// (m, l) with n / g = div_invariant(n, m, l) for 32-bit n (Granlund and Montgomery's
+// round-up method; g <= 2^31).
+void invariant_divisor(u64 g, uint32_t* m, uint32_t* l)
+{
+    uint32_t ll = 0;
+    while ((1ull << ll) < g) ++ll;  // ceil(log2 g)
+    *l = ll;
+    *m = (uint32_t)(((((u128)1) << 32) * ((((u128)1) << ll) - g)) / g + 1);
+}
+
+// [HF] Per-scheme composition, for hp_gather_dequant_q, in the order hp.h lists.
+int check_quant(const hp_paged_desc* d, const hp_quant_desc* q)
+{
+    if (!q) return HP_ERR_NULL;
+    if (d->dtype != HP_I8 && d->dtype != HP_U8) return HP_ERR_DTYPE;
+    u64 want;
+    if (q->scheme_tag == HP_QUANT_PER_TENSOR) {
+        want = 1;
+    } else if (q->scheme_tag == HP_QUANT_PER_CHANNEL) {
+        if (q->axis == 1) want = d->num_heads;
+        else if (q->axis == 2) want = d->head_dim;
+        else return HP_ERR_QUANT_SCHEME;
+    } else if (q->scheme_tag == HP_QUANT_PER_BLOCK_AFFINE) {
+        if (q->axis != 0 || q->block_size != d->page_size) return HP_ERR_QUANT_BLOCK;
+        const u128 n = (u128)d->num_pages * d->page_size;
+        if (n >> 64) return HP_ERR_SCALES;
+        want = (u64)n;
+    } else {
+        return HP_ERR_QUANT_SCHEME;
+    }
+    if (q->count != want) return HP_ERR_SCALES;
+    if (!q->scales) return HP_ERR_NULL;
+    if (misaligned(q->scales, 64) || misaligned(q->zero_points, 64)) return HP_ERR_ALIGN;
+    return HP_OK;
+}
+
+// The copy step of a gather; `dequant` selects the dequantising forms, with the
+// parameters of `quant` or (quant == NULL) the descriptor's per-slot scales.
 int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_status,
-                   void* stream, bool dequant)
+                   void* stream, bool dequant, const hp_quant_desc* quant = nullptr)
 {
     int rc = check_desc(d);
     if (rc) return rc;
-    if (dequant) {
+    if (dequant && quant) {
+        rc = check_quant(d, quant);
+        if (rc) return rc;
+    } else if (dequant) {
         if (d->dtype != HP_I8) return HP_ERR_DTYPE;
         if (!(d->flags & HP_HAS_QUANT)) return HP_ERR_SCALES;
     }
@@ -166,16 +207,30 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
     a.dst = static_cast<char*>(out);
     int vec;
     if (dequant) {
-        // groups of 8 elements per thread when rows split into them and a unit's groups
-        // fit 32-bit indices; element by element otherwise
+        int scheme = 0;  // per page slot
+        if (quant) {
+            a.scales = quant->scales;
+            a.q_zp = static_cast<const unsigned char*>(quant->zero_points);
+            if (quant->scheme_tag == HP_QUANT_PER_TENSOR) scheme = 1;
+            else if (quant->scheme_tag == HP_QUANT_PER_CHANNEL) scheme = quant->axis == 1 ? 2 : 3;
+        }
+        a.q_kind = scheme * 2 + (a.q_zp != nullptr);
+        a.q_signed = d->dtype == HP_I8;
+        a.q_head_dim = d->head_dim;
+        // groups of 8 elements per thread when rows (and, per channel, heads) split into
+        // them and a unit's groups fit 32-bit indices; element by element otherwise
         const u64 g = a.row_elems / 8;
+        const bool per_channel = scheme >= 2;
         const bool v8 = a.row_elems % 8 == 0 && !misaligned(out, 16) && g <= (1ull << 31) &&
-                        (u128)d->page_size * g < ((u128)1 << 32);
+                        (u128)d->page_size * g < ((u128)1 << 32) &&
+                        (!per_channel || d->head_dim % 8 == 0);
         if (v8) {
-            uint32_t l = 0;
-            while ((1ull << l) < g) ++l;  // ceil(log2 g)
-            a.div_l = l;
-            a.div_m = (uint32_t)(((((u128)1) << 32) * ((((u128)1) << l) - g)) / g + 1);
+            invariant_divisor(g, &a.div_m, &a.div_l);
+            a.q_gpr = (uint32_t)g;
+            if (per_channel) {
+                a.q_gph = (uint32_t)(d->head_dim / 8);
+                invariant_divisor(a.q_gph, &a.q_hd_m, &a.q_hd_l);
+            }
         }
         vec = v8 ? 16 : 1;
         return hp::launch_copy(hp::kDequant, d->index_type == HP_IDX_U64, a, vec, stream);
@@ -184,14 +239,24 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
     return hp::launch_copy(hp::kGather, d->index_type == HP_IDX_U64, a, vec, stream);
 }
 
+// The descriptor a scheme-driven dequantising gather validates: its quantisation
+// parameters come from the hp_quant_desc, so the descriptor's own flag is dropped.
+hp_paged_desc without_quant_flag(const hp_paged_desc* d)
+{
+    hp_paged_desc c = *d;
+    c.flags &= ~HP_HAS_QUANT;
+    return c;
+}
+
 int plan_gather(const hp_paged_desc* d, u64 out_tokens, void* ws, u64 wsb, int* d_status,
                 void* stream, bool check_out)
 {
     int rc = check_ws(d, ws, wsb);
     if (rc) return rc;
     if (check_out) {
-        const u128 out_bytes = (u128)out_tokens * d->num_heads * d->head_dim *
-                               ((d->flags & HP_HAS_QUANT) && d->dtype == HP_I8 ? 2 : elem_bytes(d->dtype));
+        // a dequantising gather writes 2-byte elements from 1-byte codes
+        const u64 es = elem_bytes(d->dtype) < 2 ? 2 : elem_bytes(d->dtype);
+        const u128 out_bytes = (u128)out_tokens * d->num_heads * d->head_dim * es;
         if (out_bytes >> 64) return HP_ERR_OUT_SIZE;
     }
     hp::PlanArgs a = plan_args(d, ws, d_status);
@@ -312,6 +377,8 @@ HP_API const char* hp_status_string(int s)
         HP_NAME(HP_ERR_CUDA)
         HP_NAME(HP_ERR_TIMEOUT)
         HP_NAME(HP_ERR_NOALLOC_LIMIT)
+        HP_NAME(HP_ERR_QUANT_SCHEME)
+        HP_NAME(HP_ERR_QUANT_BLOCK)
 #undef HP_NAME
     default: return "HP_ERR_UNKNOWN";
     }
@@ -378,6 +445,31 @@ HP_API int hp_gather_dequant(const hp_paged_desc* desc, void* out_bf16, uint64_t
     rc = plan_gather(desc, out_tokens, workspace, workspace_bytes, d_status, stream, true);
     if (rc) return rc;
     return gather_planned(desc, out_bf16, workspace, d_status, stream, true);
+}
+
+HP_API int hp_gather_dequant_q(const hp_paged_desc* desc, const hp_quant_desc* quant,
+                               void* out_bf16, uint64_t out_tokens, void* workspace,
+                               uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    if (!desc) return HP_ERR_NULL;
+    const hp_paged_desc d = without_quant_flag(desc);
+    int rc = check_desc(&d);
+    if (rc) return rc;
+    rc = check_quant(&d, quant);
+    if (rc) return rc;
+    if (out_tokens && !out_bf16) return HP_ERR_NULL;
+    rc = plan_gather(&d, out_tokens, workspace, workspace_bytes, d_status, stream, true);
+    if (rc) return rc;
+    return gather_planned(&d, out_bf16, workspace, d_status, stream, true, quant);
+}
+
+HP_API int hp_gather_dequant_q_planned(const hp_paged_desc* desc, const hp_quant_desc* quant,
+                                       void* out_bf16, const void* workspace, int* d_status,
+                                       void* stream)
+{
+    if (!desc) return HP_ERR_NULL;
+    const hp_paged_desc d = without_quant_flag(desc);
+    return gather_planned(&d, out_bf16, workspace, d_status, stream, true, quant);
 }
 
 HP_API int hp_append_plan(const hp_paged_desc* desc, const void* new_ptr, uint64_t total_new,

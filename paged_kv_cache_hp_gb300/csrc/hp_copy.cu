@@ -143,31 +143,47 @@ __device__ __forceinline__ uint32_t div_invariant(uint32_t n, uint32_t m, uint32
     return (t1 + ((n - t1) >> 1)) >> (l - 1);
 }
 
-// Signed byte k of w as a float, exactly: with the sign bit flipped the byte is
-// x + 128 in [0, 255]; placed under the exponent of 2^23 it reads 2^23 + x + 128.
-__device__ __forceinline__ float i8_to_f32(uint32_t w_flipped, uint32_t k)
+// Quantization schemes of the dequantising gather; the copy kernel's Q template argument
+// is scheme * 2 + (zero points present).
+enum QScheme { kQSlot = 0, kQTensor = 1, kQHead = 2, kQDim = 3 };
+
+// Byte k of w as a float, exactly: placed under the exponent of 2^23 a byte u reads
+// 2^23 + u.  A signed byte x is first made x + 128 by flipping its sign bit.
+__device__ __forceinline__ float byte_to_f32(uint32_t w, uint32_t k, float bias)
 {
-    return __uint_as_float(__byte_perm(w_flipped, 0x4B000000u, 0x7650u | k)) - 8388736.0f;
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u | k)) - bias;
 }
 
-// Eight int8 values times one scale -> eight bfloat16 values, each the bfloat16 nearest
-// the exact product.  The fast path rounds the binary32 products with one packed
-// conversion per pair; a product whose low 16 bits are 0x8000 (a bfloat16 midpoint,
-// found with a zero-halfword test over each packed pair) sends the group to dq_bf16.
-__device__ __forceinline__ uint4 dq8(uint2 q, float s)
+// The eight 8-bit codes of q (signed or unsigned) as floats.
+__device__ __forceinline__ void codes_to_f32(uint2 q, bool sgn, float f[8])
 {
-    const uint32_t w0 = q.x ^ 0x80808080u, w1 = q.y ^ 0x80808080u;
-    float f[8];
+    const uint32_t flip = sgn ? 0x80808080u : 0u;
+    const float bias = sgn ? 8388736.0f : 8388608.0f;  // 2^23 + 128, or 2^23
+    const uint32_t w0 = q.x ^ flip, w1 = q.y ^ flip;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        f[k] = i8_to_f32(w0, k);
-        f[4 + k] = i8_to_f32(w1, k);
+        f[k] = byte_to_f32(w0, k, bias);
+        f[4 + k] = byte_to_f32(w1, k, bias);
     }
+}
+
+__device__ __forceinline__ float code_to_f32(unsigned char b, bool sgn)
+{
+    return sgn ? (float)(signed char)b : (float)b;
+}
+
+// Eight exact values f[i] (small integers) times their scales -> eight bfloat16 values,
+// each the bfloat16 nearest the exact product.  The fast path rounds the binary32
+// products with one packed conversion per pair; a product whose low 16 bits are 0x8000
+// (a bfloat16 midpoint, found with a zero-halfword test over each packed pair) sends
+// the group to dq_bf16.
+__device__ __forceinline__ uint4 round8(const float f[8], const float s[8])
+{
     uint32_t o[4];
     uint32_t mid = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float p0 = __fmul_rn(f[2 * k], s), p1 = __fmul_rn(f[2 * k + 1], s);
+        const float p0 = __fmul_rn(f[2 * k], s[2 * k]), p1 = __fmul_rn(f[2 * k + 1], s[2 * k + 1]);
         const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
         o[k] = *reinterpret_cast<const uint32_t*>(&h);
         const uint32_t y =
@@ -176,7 +192,8 @@ __device__ __forceinline__ uint4 dq8(uint2 q, float s)
     }
     if (mid) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o[k] = dq_bf16(f[2 * k], s) | (dq_bf16(f[2 * k + 1], s) << 16);
+        for (int k = 0; k < 4; ++k)
+            o[k] = dq_bf16(f[2 * k], s[2 * k]) | (dq_bf16(f[2 * k + 1], s[2 * k + 1]) << 16);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -192,12 +209,24 @@ __device__ __forceinline__ uint2 ld_stream8(const uint2* p)
 
 constexpr int kDqUnroll = 16;
 
-// int8 rows -> bfloat16 rows, 8 elements per thread step; `n8` groups of 8, rows of
-// row_elems/8 groups (the row of group v is div_invariant(v, m, l)).
-__device__ __forceinline__ void dequant_run8(const char* __restrict__ src, char* __restrict__ dst,
-                                             const float* __restrict__ scales, uint32_t n8,
-                                             uint32_t m, uint32_t l)
+// 8-bit rows -> bfloat16 rows, 8 elements per thread step.  `n8` groups of 8; the row of
+// group v within the unit is v / (row_elems/8) and, for per-channel schemes, its head is
+// (v mod row_elems/8) / (head_dim/8) (both by invariant-divisor multiplication).
+// `slot0` is the unit's first page-slot index (per-block-affine parameters).
+template <int Q>
+__device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __restrict__ src,
+                                             char* __restrict__ dst, uint64_t slot0, uint32_t n8)
 {
+    constexpr int kScheme = Q >> 1;
+    constexpr bool kZp = Q & 1;
+    const bool sgn = a.q_signed != 0;
+    const float* __restrict__ scales = a.scales;
+    const unsigned char* __restrict__ zps = a.q_zp;
+    float s_t = 0.0f, z_t = 0.0f;  // per-tensor parameters, loaded once
+    if (kScheme == kQTensor) {
+        s_t = __ldg(scales);
+        if (kZp) z_t = code_to_f32(__ldg(zps), sgn);
+    }
     const uint2* s = reinterpret_cast<const uint2*>(src);
     uint4* d = reinterpret_cast<uint4*>(dst);
     for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kDqUnroll) {
@@ -210,23 +239,75 @@ __device__ __forceinline__ void dequant_run8(const char* __restrict__ src, char*
 #pragma unroll
         for (int k = 0; k < kDqUnroll; ++k) {
             const uint32_t v = v0 + k * kThreads;
-            if (v < n8) st_stream(d + v, dq8(q[k], __ldg(scales + div_invariant(v, m, l))));
+            if (v >= n8) continue;
+            float sc[8], zc[8], f[8];
+            if (kScheme == kQSlot || kScheme == kQTensor) {
+                float s1 = s_t, z1 = z_t;
+                if (kScheme == kQSlot) {
+                    const uint64_t i = slot0 + div_invariant(v, a.div_m, a.div_l);
+                    s1 = __ldg(scales + i);
+                    if (kZp) z1 = code_to_f32(__ldg(zps + i), sgn);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sc[e] = s1;
+                    zc[e] = z1;
+                }
+            } else {
+                const uint32_t r = div_invariant(v, a.div_m, a.div_l);
+                const uint32_t g = v - r * a.q_gpr;          // group within the row
+                const uint32_t h = div_invariant(g, a.q_hd_m, a.q_hd_l);
+                if (kScheme == kQHead) {
+                    const float s1 = __ldg(scales + h);
+                    const float z1 = kZp ? code_to_f32(__ldg(zps + h), sgn) : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        sc[e] = s1;
+                        zc[e] = z1;
+                    }
+                } else {
+                    const uint32_t d0 = (g - h * a.q_gph) * 8;  // first feature of the group
+                    const float4 lo = __ldg(reinterpret_cast<const float4*>(scales + d0));
+                    const float4 hi = __ldg(reinterpret_cast<const float4*>(scales + d0 + 4));
+                    sc[0] = lo.x; sc[1] = lo.y; sc[2] = lo.z; sc[3] = lo.w;
+                    sc[4] = hi.x; sc[5] = hi.y; sc[6] = hi.z; sc[7] = hi.w;
+                    if (kZp) codes_to_f32(__ldg(reinterpret_cast<const uint2*>(zps + d0)), sgn, zc);
+                }
+            }
+            codes_to_f32(q[k], sgn, f);
+            if (kZp) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] -= zc[e];  // exact: |q - zp| <= 255
+            }
+            st_stream(d + v, round8(f, sc));
         }
     }
 }
 
-// Element-wise fallback for rows whose length is not a multiple of 8 elements.
-__device__ __forceinline__ void dequant_run1(const char* __restrict__ src, char* __restrict__ dst,
-                                             const float* __restrict__ scales, uint64_t n,
-                                             uint64_t row_elems)
+// Element-wise fallback for rows (or, per channel, heads) that do not split into groups
+// of 8 elements.
+template <int Q>
+__device__ __forceinline__ void dequant_run1(const CopyArgs& a, const char* __restrict__ src,
+                                             char* __restrict__ dst, uint64_t slot0, uint64_t n)
 {
-    const signed char* s = reinterpret_cast<const signed char*>(src);
+    constexpr int kScheme = Q >> 1;
+    constexpr bool kZp = Q & 1;
+    const bool sgn = a.q_signed != 0;
+    const unsigned char* s = reinterpret_cast<const unsigned char*>(src);
     unsigned short* d = reinterpret_cast<unsigned short*>(dst);
-    for (uint64_t e = threadIdx.x; e < n; e += kThreads)
-        d[e] = (unsigned short)dq_bf16((float)s[e], __ldg(scales + e / row_elems));
+    for (uint64_t e = threadIdx.x; e < n; e += kThreads) {
+        const uint64_t r = e / a.row_elems, c = e - r * a.row_elems;
+        uint64_t i = 0;
+        if (kScheme == kQSlot) i = slot0 + r;
+        else if (kScheme == kQHead) i = c / a.q_head_dim;
+        else if (kScheme == kQDim) i = c % a.q_head_dim;
+        float f = code_to_f32(s[e], sgn);
+        if (kZp) f -= code_to_f32(__ldg(a.q_zp + i), sgn);
+        d[e] = (unsigned short)dq_bf16(f, __ldg(a.scales + i));
+    }
 }
 
-template <int MODE, typename IndexT, int VEC, bool WARP_UNITS>
+template <int MODE, typename IndexT, int VEC, bool WARP_UNITS, int Q = 0>
 __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
 {
     __shared__ unsigned long long s_src[kThreads], s_dst[kThreads], s_scale[kThreads];
@@ -269,11 +350,11 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
             if (rows == 0) continue;
             if (MODE == kDequant) {
                 if (VEC == 16)
-                    dequant_run8(a.src + s_src[i], a.dst + s_dst[i], a.scales + s_scale[i],
-                                 (uint32_t)(rows * a.row_elems / 8), a.div_m, a.div_l);
+                    dequant_run8<Q>(a, a.src + s_src[i], a.dst + s_dst[i], s_scale[i],
+                                    (uint32_t)(rows * a.row_elems / 8));
                 else
-                    dequant_run1(a.src + s_src[i], a.dst + s_dst[i], a.scales + s_scale[i],
-                                 rows * a.row_elems, a.row_elems);
+                    dequant_run1<Q>(a, a.src + s_src[i], a.dst + s_dst[i], s_scale[i],
+                                    rows * a.row_elems);
             } else {
                 copy_run<VEC>(a.src + s_src[i], a.dst + s_dst[i], rows * a.row_bytes / VEC);
             }
@@ -282,14 +363,14 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
     }
 }
 
-template <int MODE, typename IndexT, int VEC, bool WARP_UNITS>
+template <int MODE, typename IndexT, int VEC, bool WARP_UNITS, int Q = 0>
 int launch_t(const CopyArgs& a, cudaStream_t st)
 {
-    auto kern = copy_kernel<MODE, IndexT, VEC, WARP_UNITS>;
+    auto kern = copy_kernel<MODE, IndexT, VEC, WARP_UNITS, Q>;
     int dev = 0;
     const int sms = current_sms(&dev);
     const int per_sm =
-        sms ? resident_ctas<copy_kernel<MODE, IndexT, VEC, WARP_UNITS>>(dev, kThreads, 0) : 0;
+        sms ? resident_ctas<copy_kernel<MODE, IndexT, VEC, WARP_UNITS, Q>>(dev, kThreads, 0) : 0;
     if (sms == 0 || per_sm == 0) return HP_ERR_CUDA;
     uint64_t grid = (uint64_t)sms * (uint64_t)per_sm;
     if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
@@ -319,8 +400,15 @@ template <int MODE, typename IndexT>
 int launch_vec(const CopyArgs& a, int vec, cudaStream_t st)
 {
     if constexpr (MODE == kDequant) {
-        return vec == 16 ? launch_t<MODE, IndexT, 16, false>(a, st)
-                         : launch_t<MODE, IndexT, 1, false>(a, st);
+        switch (a.q_kind) {
+#define HP_DQ(q)                                                                        \
+    case q:                                                                             \
+        return vec == 16 ? launch_t<MODE, IndexT, 16, false, q>(a, st)                  \
+                         : launch_t<MODE, IndexT, 1, false, q>(a, st);
+            HP_DQ(0) HP_DQ(1) HP_DQ(2) HP_DQ(3) HP_DQ(4) HP_DQ(5) HP_DQ(6) HP_DQ(7)
+#undef HP_DQ
+        default: return HP_ERR_ARG;
+        }
     } else {
         return a.unit_bytes <= 8192 ? launch_vec_w<MODE, IndexT, true>(a, vec, st)
                                     : launch_vec_w<MODE, IndexT, false>(a, vec, st);

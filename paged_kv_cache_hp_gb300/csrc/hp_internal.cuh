@@ -132,6 +132,14 @@ struct CopyArgs {
     uint64_t row_elems;       // elements of one row (dequant)
     uint64_t unit_bytes;      // largest unit: page_size rows of row_bytes
     uint32_t div_m, div_l;    // dequant: divide a group index by row_elems/8
+    // dequant scheme: q_kind = scheme * 2 + (zero points present), scheme 0 per page slot,
+    // 1 per tensor, 2 per head (axis 1), 3 per feature (axis 2)
+    int q_kind;
+    int q_signed;             // codes are int8 (1) or uint8 (0)
+    const unsigned char* q_zp;  // zero points, one byte each, or NULL
+    uint32_t q_gpr, q_gph;    // groups of 8 per row, per head
+    uint32_t q_hd_m, q_hd_l;  // divide a group-in-row index by q_gph
+    uint64_t q_head_dim;
     int* d_status;
 };
 

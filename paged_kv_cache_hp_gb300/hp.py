@@ -36,6 +36,25 @@ class HpPagedDesc(ctypes.Structure):
                 ("page_pool", "block_table", "seq_ptr", "seq_lens", "scales")]
 
 
+class HpQuantDesc(ctypes.Structure):
+    _fields_ = [("scheme_tag", ctypes.c_uint32), ("axis", ctypes.c_uint32),
+                ("block_size", ctypes.c_uint64), ("count", ctypes.c_uint64),
+                ("scales", ctypes.c_void_p), ("zero_points", ctypes.c_void_p)]
+
+
+PER_TENSOR, PER_CHANNEL, PER_BLOCK_AFFINE = 0x01, 0x02, 0x03
+
+
+def quant_desc(scheme_tag, scales, zero_points=None, axis=0, block_size=0, count=None):
+    """An hp_quant_desc over device tensors (kept alive on the result's `keep`)."""
+    q = HpQuantDesc()
+    q.scheme_tag, q.axis, q.block_size = scheme_tag, axis, block_size
+    q.count = (0 if scales is None else scales.numel()) if count is None else count
+    q.scales, q.zero_points = _p(scales), _p(zero_points)
+    q.keep = (scales, zero_points)
+    return q
+
+
 def lib():
     """The loaded library; raises RuntimeError when libhp.so is missing."""
     global _lib
@@ -68,6 +87,10 @@ def lib():
                 "hp_lane_append": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32, u64,
                                        u64, vp, vp, vp]),
                 "hp_gather_noalloc": (i, [D, vp, u64, vp, vp]),
+                "hp_gather_dequant_q": (i, [D, ctypes.POINTER(HpQuantDesc), vp, u64, vp, u64, vp,
+                                            vp]),
+                "hp_gather_dequant_q_planned": (i, [D, ctypes.POINTER(HpQuantDesc), vp, vp, vp,
+                                                    vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -208,6 +231,19 @@ def hp_lane_append(pool, table, capacity, page_tokens, batch, kv_heads, width, d
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     return lib().hp_lane_append(_p(pool), _p(table), capacity, page_tokens, batch, kv_heads,
                                 width, dt, n, m, _p(new_rows), _p(d_status), _stream(stream))
+
+
+def hp_gather_dequant_q(desc, quant, out, out_tokens, workspace, d_status=None, stream=None):
+    return lib().hp_gather_dequant_q(desc.ref, None if quant is None else ctypes.byref(quant),
+                                     _p(out), out_tokens, _p(workspace), _wsn(workspace),
+                                     _p(d_status), _stream(stream))
+
+
+def hp_gather_dequant_q_planned(desc, quant, out, workspace, d_status=None, stream=None):
+    return lib().hp_gather_dequant_q_planned(desc.ref,
+                                             None if quant is None else ctypes.byref(quant),
+                                             _p(out), _p(workspace), _p(d_status),
+                                             _stream(stream))
 
 
 def hp_gather_noalloc(desc, out, out_tokens, d_status=None, stream=None):
