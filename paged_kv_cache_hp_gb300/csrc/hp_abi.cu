@@ -230,6 +230,7 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
             if (per_channel) {
                 a.q_gph = (uint32_t)(d->head_dim / 8);
                 invariant_divisor(a.q_gph, &a.q_hd_m, &a.q_hd_l);
+                a.q_fixed = 256 % g == 0;  // the copy kernel's CTA width
             }
         }
         vec = v8 ? 16 : 1;

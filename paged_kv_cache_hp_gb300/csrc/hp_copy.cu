@@ -207,7 +207,10 @@ __device__ __forceinline__ uint2 ld_stream8(const uint2* p)
     return v;
 }
 
-constexpr int kDqUnroll = 16;
+#ifndef HP_DQ_UNROLL
+#define HP_DQ_UNROLL 16
+#endif
+constexpr int kDqUnroll = HP_DQ_UNROLL;  // 8-byte loads in flight per thread
 
 // 8-bit rows -> bfloat16 rows, 8 elements per thread step.  `n8` groups of 8; the row of
 // group v within the unit is v / (row_elems/8) and, for per-channel schemes, its head is
@@ -227,17 +230,49 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
         s_t = __ldg(scales);
         if (kZp) z_t = code_to_f32(__ldg(zps), sgn);
     }
+    // Per channel, when the groups of a row divide the CTA's width (q_fixed) every group a
+    // thread handles sits at the same place in its row, so its 8 scales and zero points
+    // are loaded once here.
+    float sc_f[8], zc_f[8];
+    const bool fixed = (kScheme == kQHead || kScheme == kQDim) && a.q_fixed;
+    if (fixed) {
+        const uint32_t g = threadIdx.x & (a.q_gpr - 1);
+        const uint32_t h = div_invariant(g, a.q_hd_m, a.q_hd_l);
+        if (kScheme == kQHead) {
+            const float s1 = __ldg(scales + h);
+            const float z1 = kZp ? code_to_f32(__ldg(zps + h), sgn) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sc_f[e] = s1;
+                zc_f[e] = z1;
+            }
+        } else {
+            const uint32_t d0 = (g - h * a.q_gph) * 8;
+            const float4 lo = __ldg(reinterpret_cast<const float4*>(scales + d0));
+            const float4 hi = __ldg(reinterpret_cast<const float4*>(scales + d0 + 4));
+            sc_f[0] = lo.x; sc_f[1] = lo.y; sc_f[2] = lo.z; sc_f[3] = lo.w;
+            sc_f[4] = hi.x; sc_f[5] = hi.y; sc_f[6] = hi.z; sc_f[7] = hi.w;
+            if (kZp) codes_to_f32(__ldg(reinterpret_cast<const uint2*>(zps + d0)), sgn, zc_f);
+            else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) zc_f[e] = 0.0f;
+            }
+        }
+    }
+    // per-channel groups keep 16 more values live: half the loads in flight per thread,
+    // for more resident CTAs
+    constexpr int kU = kScheme >= kQHead ? kDqUnroll / 2 : kDqUnroll;
     const uint2* s = reinterpret_cast<const uint2*>(src);
     uint4* d = reinterpret_cast<uint4*>(dst);
-    for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kDqUnroll) {
-        uint2 q[kDqUnroll];
+    for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kU) {
+        uint2 q[kU];
 #pragma unroll
-        for (int k = 0; k < kDqUnroll; ++k) {
+        for (int k = 0; k < kU; ++k) {
             const uint32_t v = v0 + k * kThreads;
             if (v < n8) q[k] = ld_stream8(s + v);
         }
 #pragma unroll
-        for (int k = 0; k < kDqUnroll; ++k) {
+        for (int k = 0; k < kU; ++k) {
             const uint32_t v = v0 + k * kThreads;
             if (v >= n8) continue;
             float sc[8], zc[8], f[8];
@@ -252,6 +287,12 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
                 for (int e = 0; e < 8; ++e) {
                     sc[e] = s1;
                     zc[e] = z1;
+                }
+            } else if (fixed) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sc[e] = sc_f[e];
+                    zc[e] = zc_f[e];
                 }
             } else {
                 const uint32_t r = div_invariant(v, a.div_m, a.div_l);
