@@ -640,7 +640,7 @@ def main():
                                   "kind": "oracle",
                                   "sample": "oracle gather (one thread) of the first %d of %d "
                                             "tokens, %.1f s" % (Ts, T, dt)}
-    if rank == 0 and not args.no_ops:
+    if rank == 0 and world == 1 and not args.no_ops:
         del step
         torch.cuda.empty_cache()
         result["ops"] = ops_measurements(dev, hp, inputs, peak)
