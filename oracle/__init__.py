@@ -115,6 +115,10 @@ def lib():
                                               P(ctypes.c_uint16)]
             L.or_gather_dequant_q.restype = i32
             L.or_gather_dequant_q.argtypes = [P(OrDesc), Q, vp, vp]
+            L.or_copy_pages.restype = i32
+            L.or_copy_pages.argtypes = [vp, u64, u64, ctypes.c_uint32, vp, vp, u64]
+            L.or_zero_tails.restype = None
+            L.or_zero_tails.argtypes = [P(OrDesc), vp]
             L.or_payload.restype = i32
             L.or_payload.argtypes = [u64, u64, u64, u64, u64, u64, P(u64)]
             _lib = L
@@ -259,6 +263,22 @@ class Desc:
         c = lib().or_gather_dequant_q(ctypes.byref(self.c), ctypes.byref(q), _ptr(out),
                                       _ptr(written))
         return out, written[:T].astype(bool), code_name(c)
+
+    # -- writer side ----------------------------------------------------------
+    def copy_pages(self, src, dst):
+        """Copies page src[i] over page dst[i] in self.pool, in place; returns the code."""
+        it = self.seq_ptr.dtype
+        a = np.ascontiguousarray(src, dtype=it)
+        b = np.ascontiguousarray(dst, dtype=it)
+        pb = self.c.page_size * self.c.num_heads * self.c.head_dim * self.es
+        return code_name(lib().or_copy_pages(_ptr(self.pool), self.c.num_pages, pb,
+                                             self.c.index_type, _ptr(a), _ptr(b), len(a)))
+
+    def zero_tails(self):
+        """Zeroes the slots no sequence reads, in self.pool; returns the per-page live counts."""
+        live = np.zeros(max(self.c.num_pages, 1), dtype=np.uint64)
+        lib().or_zero_tails(ctypes.byref(self.c), _ptr(live))
+        return live[:self.c.num_pages]
 
     def scatter_append(self, new_rows, new_ptr):
         """Writes into self.pool in place; returns the fault name."""

@@ -515,6 +515,60 @@ int or_scatter_append(const or_desc* d, const void* new_rows, const void* new_pt
     return first_fault;
 }
 
+/* ----------------------------------------------------------- writer side -- */
+/* [VA] "Copy-on-write for beam search and prefix sharing": a shared block is copied
+ * when one request needs to modify it.  For each pair i, physical page dst[i] becomes a
+ * byte copy of page src[i] (all page_size rows); pages are page_bytes long.  Page IDs
+ * are in the index type of the descriptor.  A pair naming a page >= num_pages copies
+ * nothing; the first such pair's code (PAGE_ID) is returned. */
+int or_copy_pages(void* pool, uint64_t num_pages, uint64_t page_bytes, uint32_t index_type,
+                  const void* src, const void* dst, uint64_t pairs)
+{
+    int first_fault = OR_OK;
+    for (uint64_t i = 0; i < pairs; ++i) {
+        uint64_t a = index_type == 0 ? ((const uint32_t*)src)[i] : ((const uint64_t*)src)[i];
+        uint64_t b = index_type == 0 ? ((const uint32_t*)dst)[i] : ((const uint64_t*)dst)[i];
+        if (a >= num_pages || b >= num_pages) {
+            if (first_fault == OR_OK) first_fault = OR_PAGE_ID;
+            continue;
+        }
+        memmove((unsigned char*)pool + b * page_bytes, (const unsigned char*)pool + a * page_bytes,
+                page_bytes);
+    }
+    return first_fault;
+}
+
+/* [HF] Partial trailing page: a writer should zero the slots past a sequence's valid
+ * token count when the cache crosses a trust boundary.  Slots are zeroed only where no
+ * sequence of the batch reads them: for each page the slices name, the number of leading
+ * slots that hold a valid token of some sequence referencing it is found first (a shared
+ * page keeps what its longest user needs -- [HF] Prefix Sharing), then the rest of that
+ * page is set to zero bytes.  Pages no slice names are left alone.  The descriptor must
+ * be valid (or_validate); `live` is caller scratch of num_pages entries. */
+void or_zero_tails(const or_desc* d, uint64_t* live)
+{
+    const uint64_t P = d->page_size;
+    const uint64_t row_bytes = d->num_heads * d->head_dim * or_elem_size(d->dtype);
+    unsigned char* referenced = (unsigned char*)calloc(d->num_pages ? d->num_pages : 1, 1);
+    for (uint64_t p = 0; p < d->num_pages; ++p) live[p] = 0;
+    for (uint64_t s = 0; s < d->num_seqs; ++s) {
+        const uint64_t lo = ix(d, d->seq_ptr, s), hi = ix(d, d->seq_ptr, s + 1);
+        const uint64_t len = ix(d, d->seq_lens, s);
+        for (uint64_t j = 0; j < hi - lo; ++j) {
+            const uint64_t page = ix(d, d->block_table, lo + j);
+            uint64_t used = len > j * P ? len - j * P : 0; /* tokens of s in this page */
+            if (used > P) used = P;
+            if (used > live[page]) live[page] = used;
+            referenced[page] = 1;
+        }
+    }
+    for (uint64_t p = 0; p < d->num_pages; ++p)
+        if (referenced[p])
+            memset((unsigned char*)d->page_pool + (p * P + live[p]) * row_bytes, 0,
+                   (P - live[p]) * row_bytes);
+    free(referenced);
+}
+
 /* ------------------------------------------------------- per-lane layout -- */
 /* [CH] "Locate a row without changing its logical meaning", PagedKvLayout::new:
  * zero capacity, zero page size, an overflowing rounded capacity, a table whose

@@ -84,6 +84,18 @@ class BlockAllocator:
             raise ValueError("block %d is not allocated" % block_id)
         self.ref_counts[block_id] += 1
 
+    def cow(self, block_id: int) -> int:
+        """Copy-on-write: the block a request may modify in place.  A block it holds
+        alone is returned as is; a shared one loses this reference and a fresh block is
+        allocated, which the caller fills with a copy of the old one before writing."""
+        if self.ref_counts[block_id] <= 0:
+            raise ValueError("block %d is not allocated" % block_id)
+        if self.ref_counts[block_id] == 1:
+            return block_id
+        fresh = self.allocate()
+        self.ref_counts[block_id] -= 1
+        return fresh
+
     @property
     def num_free(self) -> int:
         return len(self._heap) if self._fifo is None else len(self._fifo)
