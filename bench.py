@@ -474,6 +474,22 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     ms = med_ms(lambda: hp.hp_scatter_append_planned(d_bulk, o, np_bulk, T, ws, status), n=10)
     out["bulk_scatter_append"] = entry(b, ms)
     assert int(status.item()) == 0, hp.status_name(int(status.item()))
+    # writer side: copy-on-write copies of 20,000 pages into free pages, and zeroing the
+    # slots past every sequence's count (the pool's partial last pages)
+    rng = np.random.default_rng(9)
+    used = np.unique(w.table.astype(np.int64))
+    free = np.setdiff1d(np.arange(w.num_pages), used)
+    src = rng.choice(used, 20000, replace=False).astype(np.uint32)
+    dst = rng.choice(free, 20000, replace=False).astype(np.uint32)
+    sd, dd = idx_tensor(src, dev), idx_tensor(dst, dev)
+    page_bytes = w.page_size * w.row_bytes
+    ms = med_ms(lambda: hp.hp_copy_pages(pool, w.num_pages, page_bytes, 0, sd, dd, 20000,
+                                         status), n=10)
+    out["copy_pages_cow"] = entry(2 * 20000 * page_bytes + 2 * 20000 * 4, ms)
+    rc, nsc = hp.hp_zero_tails_scratch_bytes(d_g)
+    scratch = torch.empty(nsc, dtype=torch.uint8, device=dev)
+    out["zero_tails_step"] = step_us(lambda: hp.hp_zero_tails(d_g, ws, scratch, status))
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
     del pool, o, new
     torch.cuda.empty_cache()
 

@@ -318,6 +318,39 @@ int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, uint64_t 
                        void* workspace, uint64_t workspace_bytes, uint64_t* first_bad,
                        void* stream);
 
+/* ---------------------------------------------------------------- writer side */
+/*
+ * ASYNC.  Copy-on-write page copy ([VA] "Copy-on-write for beam search and prefix
+ * sharing": a shared block is copied when one request is about to modify it).  For every
+ * i < num_pairs, page dst_pages[i] of `page_pool` (device, num_pages pages of page_bytes
+ * bytes) becomes a byte copy of page src_pages[i].  src_pages and dst_pages are device
+ * arrays of num_pairs entries of `index_type` (HP_IDX_U32 / HP_IDX_U64).  A pair naming a
+ * page >= num_pages copies nothing and stores HP_ERR_PAGE_ID in *d_status.  Destination
+ * pages must differ from each other and from every source page (the result is otherwise
+ * unspecified).  page_pool must be 64-byte aligned.
+ */
+int hp_copy_pages(void* page_pool, uint64_t num_pages, uint64_t page_bytes, uint32_t index_type,
+                  const void* src_pages, const void* dst_pages, uint64_t num_pairs,
+                  int* d_status, void* stream);
+
+/* Bytes of scratch hp_zero_tails needs for `desc`: one 32-bit word per page. */
+int hp_zero_tails_scratch_bytes(const hp_paged_desc* desc, uint64_t* bytes);
+
+/*
+ * ASYNC.  The writer's duty of [HF] Partial trailing page before the cache crosses a trust
+ * or tenant boundary: zero the slots no sequence of the batch reads.  For every page the
+ * slices name, the slots past the largest count any referencing sequence keeps in it are
+ * set to zero bytes (a page shared by several sequences keeps what the longest of them
+ * uses, [HF] Prefix Sharing); pages no slice names are not touched.  The descriptor is
+ * always validated as hp_validate does (HP_PERMISSIVE is ignored here: zeroing through an
+ * invalid descriptor could destroy live rows); on a violation nothing is written and the
+ * rule's code goes to *d_status.  `workspace` is the plan's (hp_workspace_bytes);
+ * `scratch` (device, 4-byte aligned) holds hp_zero_tails_scratch_bytes bytes.  Writes the
+ * page pool.
+ */
+int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace_bytes,
+                  void* scratch, uint64_t scratch_bytes, int* d_status, void* stream);
+
 /* ------------------------------------------------------------ per-lane layout */
 /*
  * Host only.  The checks of [CH] PagedKvLayout::new for a layout of logical

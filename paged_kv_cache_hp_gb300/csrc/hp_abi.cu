@@ -515,6 +515,66 @@ HP_API int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, ui
     return sync_verdict(workspace, first_bad, stream);
 }
 
+HP_API int hp_copy_pages(void* page_pool, uint64_t num_pages, uint64_t page_bytes,
+                         uint32_t index_type, const void* src_pages, const void* dst_pages,
+                         uint64_t num_pairs, int* d_status, void* stream)
+{
+    if (index_type != HP_IDX_U32 && index_type != HP_IDX_U64) return HP_ERR_INDEX_TYPE;
+    if (page_bytes == 0) return HP_ERR_ZERO_DIM;
+    if (((u128)num_pages * page_bytes) >> 64) return HP_ERR_OVERFLOW;
+    if (num_pairs && (!page_pool || !src_pages || !dst_pages)) return HP_ERR_NULL;
+    if (misaligned(page_pool, 64) ||
+        misaligned(src_pages, index_type == HP_IDX_U64 ? 8 : 4) ||
+        misaligned(dst_pages, index_type == HP_IDX_U64 ? 8 : 4))
+        return HP_ERR_ALIGN;
+    int rc = reset_status(d_status, stream);
+    if (rc || num_pairs == 0) return rc;
+    hp::CopyArgs a{};
+    a.num_pages = num_pages;
+    a.src_pages = src_pages;
+    a.dst_pages = dst_pages;
+    a.lane_units = num_pairs;
+    a.src = static_cast<const char*>(page_pool);
+    a.dst = static_cast<char*>(page_pool);
+    a.row_bytes = page_bytes;
+    a.unit_bytes = page_bytes;
+    a.d_status = d_status;
+    return hp::launch_copy(hp::kCopyPages, index_type == HP_IDX_U64, a,
+                           pick_vec(page_bytes, page_pool, page_pool), stream);
+}
+
+HP_API int hp_zero_tails_scratch_bytes(const hp_paged_desc* desc, uint64_t* bytes)
+{
+    if (!desc || !bytes) return HP_ERR_NULL;
+    if (desc->num_pages > (1ull << 61)) return HP_ERR_OVERFLOW;
+    *bytes = 4 * desc->num_pages;
+    return HP_OK;
+}
+
+HP_API int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace_bytes,
+                         void* scratch, uint64_t scratch_bytes, int* d_status, void* stream)
+{
+    if (!desc) return HP_ERR_NULL;
+    hp_paged_desc d = *desc;
+    d.flags &= ~HP_PERMISSIVE;  // never zero through an unvalidated descriptor
+    int rc = check_desc(&d);
+    if (rc) return rc;
+    if (d.page_size >= (1ull << 31)) return HP_ERR_ARG;  // counts keep bit 31 free
+    if (!scratch || misaligned(scratch, 4) || scratch_bytes < 4 * d.num_pages)
+        return HP_ERR_WORKSPACE;
+    rc = check_ws(&d, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (d.num_pages &&
+        cudaMemsetAsync(scratch, 0, 4 * d.num_pages, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+        return HP_ERR_CUDA;
+    rc = plan_gather(&d, 0, workspace, workspace_bytes, d_status, stream, false);
+    if (rc) return rc;
+    hp::PlanArgs a = plan_args(&d, workspace, d_status);
+    return hp::launch_zero_tails(d.index_type == HP_IDX_U64, a, static_cast<unsigned*>(scratch),
+                                 row_bytes_of(&d), const_cast<void*>(d.page_pool), stream);
+}
+
 HP_API int hp_lane_validate(uint64_t capacity, uint64_t page_tokens, const uint64_t* table,
                             uint64_t table_len, uint64_t* detail)
 {

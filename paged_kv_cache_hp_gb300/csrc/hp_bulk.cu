@@ -265,9 +265,9 @@ int launch_t(const CopyArgs& a, cudaStream_t st)
     if (sms == 0 || !allow_dynamic_smem<bulk_kernel<MODE, IndexT, kStage, kStages>>(dev, smem))
         return HP_ERR_CUDA;
     uint64_t grid = (uint64_t)sms;
-    if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
+    if (host_counted(MODE)) grid = std::min<uint64_t>(grid, a.lane_units);
     if (grid == 0) return HP_OK;
-    if (MODE == kLaneGather || MODE == kLaneAppend) {
+    if (host_counted(MODE)) {
         kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
         return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
     }
@@ -299,6 +299,9 @@ int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, int big_stages,
         return launch_ring<kLaneGather, unsigned long long>(a, big_stages, st);
     case kLaneAppend:
         return launch_ring<kLaneAppend, unsigned long long>(a, big_stages, st);
+    case kCopyPages:
+        return index_u64 ? launch_ring<kCopyPages, unsigned long long>(a, big_stages, st)
+                         : launch_ring<kCopyPages, unsigned int>(a, big_stages, st);
     default:
         return HP_ERR_ARG;
     }

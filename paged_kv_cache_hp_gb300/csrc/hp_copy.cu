@@ -414,9 +414,9 @@ int launch_t(const CopyArgs& a, cudaStream_t st)
         sms ? resident_ctas<copy_kernel<MODE, IndexT, VEC, WARP_UNITS, Q>>(dev, kThreads, 0) : 0;
     if (sms == 0 || per_sm == 0) return HP_ERR_CUDA;
     uint64_t grid = (uint64_t)sms * (uint64_t)per_sm;
-    if (MODE == kLaneGather || MODE == kLaneAppend) grid = std::min<uint64_t>(grid, a.lane_units);
+    if (host_counted(MODE)) grid = std::min<uint64_t>(grid, a.lane_units);
     if (grid == 0) return HP_OK;
-    if (MODE == kLaneGather || MODE == kLaneAppend) {
+    if (host_counted(MODE)) {
         kern<<<(unsigned)grid, kThreads, 0, st>>>(a);
         return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
     }
@@ -481,6 +481,9 @@ int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* 
         return launch_vec<kLaneGather, unsigned long long>(a, vec, st);
     case kLaneAppend:
         return launch_vec<kLaneAppend, unsigned long long>(a, vec, st);
+    case kCopyPages:
+        return index_u64 ? launch_vec<kCopyPages, unsigned long long>(a, vec, st)
+                         : launch_vec<kCopyPages, unsigned int>(a, vec, st);
     }
     return HP_ERR_ARG;
 }

@@ -108,8 +108,26 @@ struct PlanArgs {
 // Launches the plan (and, when strict, the block-table check) on `stream`.
 int launch_plan(PlanMode mode, int index_u64, const PlanArgs& a, void* stream);
 
+// Writer side (hp_writer.cu): after a plan on `stream`, the per-page live counts and the
+// zeroing of the slots past them.
+int launch_zero_tails(int index_u64, const PlanArgs& a, unsigned* live, uint64_t row_bytes,
+                      void* pool, void* stream);
+
 // ------------------------------------------------------------------ copy step
-enum CopyMode { kGather = 0, kDequant = 1, kAppend = 2, kLaneGather = 3, kLaneAppend = 4 };
+enum CopyMode {
+    kGather = 0,
+    kDequant = 1,
+    kAppend = 2,
+    kLaneGather = 3,
+    kLaneAppend = 4,
+    kCopyPages = 5,  // whole pages src_pages[u] -> dst_pages[u] (host-known count)
+};
+
+// Modes whose unit count the host passes (no plan in front of the copy).
+__host__ __device__ constexpr bool host_counted(int mode)
+{
+    return mode == kLaneGather || mode == kLaneAppend || mode == kCopyPages;
+}
 
 struct CopyArgs {
     // block-paged descriptor data
@@ -123,8 +141,10 @@ struct CopyArgs {
     const WsHeader* hdr;
     const unsigned long long* rows_off;
     const unsigned long long* units_off;
-    // per-lane layout
+    // per-lane layout (lane_units is also the pair count of kCopyPages)
     uint64_t lanes, lane_n, lane_m, lane_units, lane_first_page, lane_pages;
+    const void* src_pages;    // kCopyPages
+    const void* dst_pages;
     // data movement
     const char* src;          // gather: pool; append: new rows
     char* dst;                // gather: out; append: pool

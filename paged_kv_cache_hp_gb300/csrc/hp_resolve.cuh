@@ -92,6 +92,16 @@ __device__ __forceinline__ Unit resolve(const CopyArgs& a, uint64_t u)
         r.rows = (unsigned)(t1 - t0);
         r.src = (n0 + (t0 - start)) * a.row_bytes;
         r.dst = (phys * P + t0 % P) * a.row_bytes;
+    } else if (MODE == kCopyPages) {
+        const unsigned long long from = static_cast<const IndexT*>(a.src_pages)[u];
+        const unsigned long long to = static_cast<const IndexT*>(a.dst_pages)[u];
+        if (from >= a.num_pages || to >= a.num_pages) {
+            report(a.d_status, HP_ERR_PAGE_ID);
+            return r;
+        }
+        r.rows = 1;  // one "row" of page_bytes
+        r.src = from * a.row_bytes;
+        r.dst = to * a.row_bytes;
     } else {
         const uint64_t A = a.lane_pages;
         const uint64_t lane = u / A, q = a.lane_first_page + u % A;

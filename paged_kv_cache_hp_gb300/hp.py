@@ -87,6 +87,9 @@ def lib():
                 "hp_lane_append": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32, u64,
                                        u64, vp, vp, vp]),
                 "hp_gather_noalloc": (i, [D, vp, u64, vp, vp]),
+                "hp_copy_pages": (i, [vp, u64, u64, ctypes.c_uint32, vp, vp, u64, vp, vp]),
+                "hp_zero_tails_scratch_bytes": (i, [D, pu64]),
+                "hp_zero_tails": (i, [D, vp, u64, vp, u64, vp, vp]),
                 "hp_gather_dequant_q": (i, [D, ctypes.POINTER(HpQuantDesc), vp, u64, vp, u64, vp,
                                             vp]),
                 "hp_gather_dequant_q_planned": (i, [D, ctypes.POINTER(HpQuantDesc), vp, vp, vp,
@@ -244,6 +247,23 @@ def hp_gather_dequant_q_planned(desc, quant, out, workspace, d_status=None, stre
                                              None if quant is None else ctypes.byref(quant),
                                              _p(out), _p(workspace), _p(d_status),
                                              _stream(stream))
+
+
+def hp_copy_pages(pool, num_pages, page_bytes, index_type, src_pages, dst_pages, num_pairs,
+                  d_status=None, stream=None):
+    return lib().hp_copy_pages(_p(pool), num_pages, page_bytes, index_type, _p(src_pages),
+                               _p(dst_pages), num_pairs, _p(d_status), _stream(stream))
+
+
+def hp_zero_tails_scratch_bytes(desc):
+    n = ctypes.c_uint64(0)
+    rc = lib().hp_zero_tails_scratch_bytes(desc.ref, ctypes.byref(n))
+    return rc, n.value
+
+
+def hp_zero_tails(desc, workspace, scratch, d_status=None, stream=None):
+    return lib().hp_zero_tails(desc.ref, _p(workspace), _wsn(workspace), _p(scratch),
+                               _wsn(scratch), _p(d_status), _stream(stream))
 
 
 def hp_gather_noalloc(desc, out, out_tokens, d_status=None, stream=None):
