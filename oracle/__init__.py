@@ -119,6 +119,15 @@ def lib():
             L.or_copy_pages.argtypes = [vp, u64, u64, ctypes.c_uint32, vp, vp, u64]
             L.or_zero_tails.restype = None
             L.or_zero_tails.argtypes = [P(OrDesc), vp]
+            L.or_from_kernel_layout.restype = None
+            L.or_from_kernel_layout.argtypes = [vp, vp, u64, u64, u64, u64, u64, u64]
+            L.or_to_kernel_layout.restype = None
+            L.or_to_kernel_layout.argtypes = [vp, vp, u64, u64, u64, u64, u64, u64]
+            L.or_padded_to_csr.restype = i32
+            L.or_padded_to_csr.argtypes = [vp, vp, u64, u64, u64, ctypes.c_uint32, vp, u64, vp,
+                                           P(u64)]
+            L.or_csr_to_padded.restype = i32
+            L.or_csr_to_padded.argtypes = [vp, vp, u64, u64, u64, ctypes.c_uint32, vp, P(u64)]
             L.or_payload.restype = i32
             L.or_payload.argtypes = [u64, u64, u64, u64, u64, u64, P(u64)]
             _lib = L
@@ -335,6 +344,52 @@ def lane_append(pool, capacity, page_tokens, table, batch_size, heads, width, n,
     c = lib().or_lane_append(_ptr(pool), capacity, page_tokens, _ptr(t), batch_size, heads,
                              width, pool.dtype.itemsize, n, m, _ptr(nr))
     return code_name(c)
+
+
+def from_kernel_layout(src, nb, bs, H, D, x):
+    """Kernel-internal [nb, H, D/x, bs, x] (numpy array of any element type) ->
+    interchange [nb, bs, H, D]."""
+    src = np.ascontiguousarray(src)
+    out = np.empty((nb, bs, H, D), dtype=src.dtype)
+    lib().or_from_kernel_layout(_ptr(src), _ptr(out), nb, bs, H, D, x, src.dtype.itemsize)
+    return out
+
+
+def to_kernel_layout(src, nb, bs, H, D, x):
+    """Interchange [nb, bs, H, D] -> kernel-internal [nb, H, D/x, bs, x]."""
+    src = np.ascontiguousarray(src)
+    out = np.empty((nb, H, D // x, bs, x), dtype=src.dtype)
+    lib().or_to_kernel_layout(_ptr(src), _ptr(out), nb, bs, H, D, x, src.dtype.itemsize)
+    return out
+
+
+def padded_to_csr(padded, lens, page_size, table_cap=None):
+    """padded [batch, max_blocks], lens [batch] (uint32 or uint64) -> (code, first,
+    table, seq_ptr)."""
+    padded = np.ascontiguousarray(padded)
+    it = 0 if padded.dtype == np.uint32 else 1
+    lens = np.ascontiguousarray(lens, dtype=padded.dtype)
+    batch, mb = padded.shape
+    cap = batch * mb if table_cap is None else table_cap
+    table = np.zeros(max(cap, 1), dtype=padded.dtype)
+    sp = np.zeros(batch + 1, dtype=padded.dtype)
+    first = ctypes.c_uint64(0)
+    c = lib().or_padded_to_csr(_ptr(padded), _ptr(lens), batch, mb, page_size, it, _ptr(table),
+                               cap, _ptr(sp), ctypes.byref(first))
+    name = code_name(c)
+    return name, first.value, (table[:int(sp[-1])] if name == "OK" else None), sp
+
+
+def csr_to_padded(table, seq_ptr, max_blocks, pad):
+    seq_ptr = np.ascontiguousarray(seq_ptr)
+    it = 0 if seq_ptr.dtype == np.uint32 else 1
+    table = np.ascontiguousarray(table, dtype=seq_ptr.dtype)
+    batch = len(seq_ptr) - 1
+    out = np.zeros((batch, max_blocks), dtype=seq_ptr.dtype)
+    first = ctypes.c_uint64(0)
+    c = lib().or_csr_to_padded(_ptr(table) if len(table) else None, _ptr(seq_ptr), batch,
+                               max_blocks, pad, it, _ptr(out), ctypes.byref(first))
+    return code_name(c), first.value, out
 
 
 PAYLOAD_FIELDS = ("reserved_pages", "active_pages", "allocated_scalar_slots",

@@ -569,6 +569,101 @@ void or_zero_tails(const or_desc* d, uint64_t* live)
     free(referenced);
 }
 
+/* ------------------------------------------------- layout conversions -- */
+/* [HF] Framework Compliance: a producer whose cache sits in a kernel-internal layout
+ * [num_blocks, num_heads, head_dim/x, block_size, x] must transpose it to the interchange
+ * layout [num_blocks, block_size, num_heads, head_dim] before emitting a descriptor.
+ * Element (b, t, h, d) of the interchange array is element (b, h, d/x, t, d mod x) of the
+ * internal one; elements are es bytes, copied as bytes.  x must divide head_dim. */
+static uint64_t internal_index(uint64_t b, uint64_t t, uint64_t h, uint64_t d, uint64_t bs,
+                               uint64_t H, uint64_t D, uint64_t x)
+{
+    return (((b * H + h) * (D / x) + d / x) * bs + t) * x + d % x;
+}
+
+void or_from_kernel_layout(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H,
+                           uint64_t D, uint64_t x, uint64_t es)
+{
+    for (uint64_t b = 0; b < nb; ++b)
+        for (uint64_t t = 0; t < bs; ++t)
+            for (uint64_t h = 0; h < H; ++h)
+                for (uint64_t d = 0; d < D; ++d)
+                    memcpy((unsigned char*)dst + (((b * bs + t) * H + h) * D + d) * es,
+                           (const unsigned char*)src + internal_index(b, t, h, d, bs, H, D, x) * es,
+                           es);
+}
+
+/* The inverse: interchange [num_blocks, block_size, num_heads, head_dim] to the
+ * kernel-internal layout. */
+void or_to_kernel_layout(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H,
+                         uint64_t D, uint64_t x, uint64_t es)
+{
+    for (uint64_t b = 0; b < nb; ++b)
+        for (uint64_t t = 0; t < bs; ++t)
+            for (uint64_t h = 0; h < H; ++h)
+                for (uint64_t d = 0; d < D; ++d)
+                    memcpy((unsigned char*)dst + internal_index(b, t, h, d, bs, H, D, x) * es,
+                           (const unsigned char*)src + (((b * bs + t) * H + h) * D + d) * es,
+                           es);
+}
+
+/* [VA] "How the attention kernel uses the block table": an attention kernel may take a
+ * padded table [batch, max_num_blocks] with per-sequence valid-token counts; the
+ * block-paged descriptor carries the same slices CSR-style ([HF] Description).  A
+ * sequence of len tokens uses its row's first ceil(len / page_size) entries.
+ * padded -> CSR: returns LEN (first bad s in *first) when a sequence needs more than
+ * max_blocks pages, OUT_SIZE when the entries exceed table_cap. */
+static uint64_t ix_t(uint32_t it, const void* buf, uint64_t i)
+{
+    return it == 0 ? ((const uint32_t*)buf)[i] : ((const uint64_t*)buf)[i];
+}
+
+static void put_t(uint32_t it, void* buf, uint64_t i, uint64_t v)
+{
+    if (it == 0) ((uint32_t*)buf)[i] = (uint32_t)v;
+    else ((uint64_t*)buf)[i] = v;
+}
+
+int or_padded_to_csr(const void* padded, const void* lens, uint64_t batch, uint64_t max_blocks,
+                     uint64_t page_size, uint32_t it, void* table_out, uint64_t table_cap,
+                     void* seq_ptr_out, uint64_t* first)
+{
+    *first = 0;
+    uint64_t total = 0;
+    for (uint64_t s = 0; s < batch; ++s) {
+        const uint64_t len = ix_t(it, lens, s);
+        const uint64_t need = len / page_size + (len % page_size != 0);
+        if (need > max_blocks) { *first = s; return OR_LEN; }
+        total += need;
+    }
+    if (total > table_cap) return OR_OUT_SIZE;
+    uint64_t k = 0;
+    put_t(it, seq_ptr_out, 0, 0);
+    for (uint64_t s = 0; s < batch; ++s) {
+        const uint64_t len = ix_t(it, lens, s);
+        const uint64_t need = len / page_size + (len % page_size != 0);
+        for (uint64_t j = 0; j < need; ++j) put_t(it, table_out, k++, ix_t(it, padded, s * max_blocks + j));
+        put_t(it, seq_ptr_out, s + 1, k);
+    }
+    return OR_OK;
+}
+
+/* CSR -> padded: row s holds slice s (block_table[seq_ptr[s] .. seq_ptr[s+1])) followed
+ * by `pad`; LEN (first s) when a slice is longer than max_blocks. */
+int or_csr_to_padded(const void* table, const void* seq_ptr, uint64_t batch, uint64_t max_blocks,
+                     uint64_t pad, uint32_t it, void* padded_out, uint64_t* first)
+{
+    *first = 0;
+    for (uint64_t s = 0; s < batch; ++s)
+        if (ix_t(it, seq_ptr, s + 1) - ix_t(it, seq_ptr, s) > max_blocks) { *first = s; return OR_LEN; }
+    for (uint64_t s = 0; s < batch; ++s) {
+        const uint64_t lo = ix_t(it, seq_ptr, s), n = ix_t(it, seq_ptr, s + 1) - lo;
+        for (uint64_t j = 0; j < max_blocks; ++j)
+            put_t(it, padded_out, s * max_blocks + j, j < n ? ix_t(it, table, lo + j) : pad);
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------- per-lane layout -- */
 /* [CH] "Locate a row without changing its logical meaning", PagedKvLayout::new:
  * zero capacity, zero page size, an overflowing rounded capacity, a table whose
