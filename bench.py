@@ -493,6 +493,16 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     del pool, o, new
     torch.cuda.empty_cache()
 
+    # kernel-internal [nb, H, D/x, bs, x] -> interchange [nb, bs, H, D], decode-gather pool
+    nb, bsz, H, D = 10000, 16, 32, 128
+    kin = torch.empty(nb * bsz * H * D * 2, dtype=torch.uint8, device=dev)
+    kout = torch.empty_like(kin)
+    ms = med_ms(lambda: hp.hp_from_kernel_layout(kin, kout, nb, bsz, H, D, 8, "f16"), n=10)
+    out["kernel_layout_to_interchange"] = entry(2 * kin.numel(), ms)
+    ms = med_ms(lambda: hp.hp_to_kernel_layout(kout, kin, nb, bsz, H, D, 8, "f16"), n=10)
+    out["interchange_to_kernel_layout"] = entry(2 * kin.numel(), ms)
+    del kin, kout
+
     # per-lane [N, B, H_kv, P, d] layout
     lw = inputs.lane_synthetic()
     g = torch.Generator(device=dev)

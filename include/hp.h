@@ -351,6 +351,52 @@ int hp_zero_tails_scratch_bytes(const hp_paged_desc* desc, uint64_t* bytes);
 int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace_bytes,
                   void* scratch, uint64_t scratch_bytes, int* d_status, void* stream);
 
+/* --------------------------------------------------------- layout conversions */
+/*
+ * ASYNC.  [HF] Framework Compliance: a producer whose cache sits in a kernel-internal
+ * layout must transpose it to the interchange layout before emitting a descriptor.
+ * hp_from_kernel_layout reads `src` as [num_blocks, num_heads, head_dim/x, block_size, x]
+ * (the older key-cache reshape; x = 1 gives [num_blocks, num_heads, head_dim, block_size])
+ * and writes `dst` as [num_blocks, block_size, num_heads, head_dim]: element (b, t, h, d)
+ * of dst is element (b, h, d/x, t, d mod x) of src.  hp_to_kernel_layout is the inverse.
+ * Elements of `dtype` are copied as bytes; src and dst are device buffers that must not
+ * overlap.  x must divide head_dim (HP_ERR_ARG); block_size*head_dim*width must not exceed
+ * 48 KiB (one (block, head) unit is staged in shared memory; HP_ERR_ARG beyond).
+ */
+int hp_from_kernel_layout(const void* src, void* dst, uint64_t num_blocks, uint64_t block_size,
+                          uint64_t num_heads, uint64_t head_dim, uint64_t x, uint32_t dtype,
+                          void* stream);
+int hp_to_kernel_layout(const void* src, void* dst, uint64_t num_blocks, uint64_t block_size,
+                        uint64_t num_heads, uint64_t head_dim, uint64_t x, uint32_t dtype,
+                        void* stream);
+
+/* Device workspace (256-byte aligned) the table conversions need for `batch` sequences. */
+int hp_table_workspace_bytes(uint64_t batch, uint64_t* bytes);
+
+/*
+ * ASYNC.  A padded block table [batch, max_blocks] with per-sequence token counts -- the
+ * form of [VA] "How the attention kernel uses the block table" -- to the CSR slices of a
+ * block-paged descriptor ([HF] Description): sequence s keeps the first
+ * ceil(lens[s] / page_size) entries of its row.  `padded`, `lens` (batch entries) and the
+ * outputs `table_out` (table_cap entries) and `seq_ptr_out` (batch+1 entries) are device
+ * arrays of `index_type`.  On the device: a sequence needing more than max_blocks pages
+ * stores HP_ERR_LEN, more than table_cap entries in all HP_ERR_OUT_SIZE; then nothing is
+ * written.
+ */
+int hp_padded_to_csr(const void* padded, const void* lens, uint64_t batch, uint64_t max_blocks,
+                     uint64_t page_size, uint32_t index_type, void* table_out,
+                     uint64_t table_cap, void* seq_ptr_out, void* workspace,
+                     uint64_t workspace_bytes, int* d_status, void* stream);
+
+/*
+ * ASYNC.  The inverse: row s of `padded_out` ([batch, max_blocks]) holds the slice
+ * table[seq_ptr[s] .. seq_ptr[s+1]) followed by `pad`.  A slice that is reversed, ends
+ * past table_len or is longer than max_blocks stores HP_ERR_LEN (nothing written).
+ */
+int hp_csr_to_padded(const void* table, uint64_t table_len, const void* seq_ptr, uint64_t batch,
+                     uint64_t max_blocks, uint64_t pad, uint32_t index_type, void* padded_out,
+                     void* workspace, uint64_t workspace_bytes, int* d_status, void* stream);
+
 /* ------------------------------------------------------------ per-lane layout */
 /*
  * Host only.  The checks of [CH] PagedKvLayout::new for a layout of logical

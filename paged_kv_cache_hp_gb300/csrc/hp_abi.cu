@@ -149,16 +149,6 @@ int sync_verdict(const void* ws, u64* first_bad, void* stream)
     return hp::key_status(key);
 }
 
-// (m, l) with n / g = div_invariant(n, m, l) for 32-bit n (Granlund and Montgomery's
-// round-up method; g <= 2^31).
-void invariant_divisor(u64 g, uint32_t* m, uint32_t* l)
-{
-    uint32_t ll = 0;
-    while ((1ull << ll) < g) ++ll;  // ceil(log2 g)
-    *l = ll;
-    *m = (uint32_t)(((((u128)1) << 32) * ((((u128)1) << ll) - g)) / g + 1);
-}
-
 // [HF] Per-scheme composition, for hp_gather_dequant_q, in the order hp.h lists.
 int check_quant(const hp_paged_desc* d, const hp_quant_desc* q)
 {
@@ -225,11 +215,11 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
                         (u128)d->page_size * g < ((u128)1 << 32) &&
                         (!per_channel || d->head_dim % 8 == 0);
         if (v8) {
-            invariant_divisor(g, &a.div_m, &a.div_l);
+            hp::invariant_divisor(g, &a.div_m, &a.div_l);
             a.q_gpr = (uint32_t)g;
             if (per_channel) {
                 a.q_gph = (uint32_t)(d->head_dim / 8);
-                invariant_divisor(a.q_gph, &a.q_hd_m, &a.q_hd_l);
+                hp::invariant_divisor(a.q_gph, &a.q_hd_m, &a.q_hd_l);
                 a.q_fixed = 256 % g == 0;  // the copy kernel's CTA width
             }
         }
@@ -573,6 +563,104 @@ HP_API int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t wo
     hp::PlanArgs a = plan_args(&d, workspace, d_status);
     return hp::launch_zero_tails(d.index_type == HP_IDX_U64, a, static_cast<unsigned*>(scratch),
                                  row_bytes_of(&d), const_cast<void*>(d.page_pool), stream);
+}
+
+namespace {
+
+int transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H, uint64_t D,
+              uint64_t x, uint32_t dtype, bool to_interchange, void* stream)
+{
+    const u64 es = elem_bytes(dtype);
+    if (!es) return HP_ERR_DTYPE;
+    if (!bs || !H || !D || !x) return HP_ERR_ZERO_DIM;
+    if (D % x) return HP_ERR_ARG;
+    if ((u128)bs * D * es > 48 * 1024) return HP_ERR_ARG;
+    const u128 total = (u128)nb * bs * H * D * es;
+    if (total >> 64) return HP_ERR_OVERFLOW;
+    if (nb == 0) return HP_OK;
+    if (!src || !dst) return HP_ERR_NULL;
+    return hp::launch_transpose(src, dst, nb, bs, H, D, x, es, to_interchange, stream);
+}
+
+u64 table_ws_bytes(u64 batch) { return hp::kWsHeaderBytes + hp::round_up_256(8 * (batch + 1)); }
+
+}  // namespace
+
+HP_API int hp_from_kernel_layout(const void* src, void* dst, uint64_t num_blocks,
+                                 uint64_t block_size, uint64_t num_heads, uint64_t head_dim,
+                                 uint64_t x, uint32_t dtype, void* stream)
+{
+    return transpose(src, dst, num_blocks, block_size, num_heads, head_dim, x, dtype, true, stream);
+}
+
+HP_API int hp_to_kernel_layout(const void* src, void* dst, uint64_t num_blocks,
+                               uint64_t block_size, uint64_t num_heads, uint64_t head_dim,
+                               uint64_t x, uint32_t dtype, void* stream)
+{
+    return transpose(src, dst, num_blocks, block_size, num_heads, head_dim, x, dtype, false,
+                     stream);
+}
+
+HP_API int hp_table_workspace_bytes(uint64_t batch, uint64_t* bytes)
+{
+    if (!bytes) return HP_ERR_NULL;
+    if (batch >= (1ull << 58)) return HP_ERR_OVERFLOW;
+    *bytes = table_ws_bytes(batch);
+    return HP_OK;
+}
+
+HP_API int hp_padded_to_csr(const void* padded, const void* lens, uint64_t batch,
+                            uint64_t max_blocks, uint64_t page_size, uint32_t index_type,
+                            void* table_out, uint64_t table_cap, void* seq_ptr_out,
+                            void* workspace, uint64_t workspace_bytes, int* d_status,
+                            void* stream)
+{
+    if (index_type != HP_IDX_U32 && index_type != HP_IDX_U64) return HP_ERR_INDEX_TYPE;
+    if (!page_size) return HP_ERR_ZERO_PAGE_SIZE;
+    if (batch >= (1ull << 58) || ((u128)batch * max_blocks) >> 64) return HP_ERR_OVERFLOW;
+    if (!seq_ptr_out || (batch && (!lens || (max_blocks && !padded))) || (table_cap && !table_out))
+        return HP_ERR_NULL;
+    if (!workspace || misaligned(workspace, 256) || workspace_bytes < table_ws_bytes(batch))
+        return HP_ERR_WORKSPACE;
+    hp::TableArgs t{};
+    t.to_csr = true;
+    t.in = padded;
+    t.lens = lens;
+    t.out = table_out;
+    t.out2 = seq_ptr_out;
+    t.batch = batch;
+    t.max_blocks = max_blocks;
+    t.page_size = page_size;
+    t.cap = table_cap;
+    t.workspace = workspace;
+    t.d_status = d_status;
+    return hp::launch_tables(index_type == HP_IDX_U64, t, stream);
+}
+
+HP_API int hp_csr_to_padded(const void* table, uint64_t table_len, const void* seq_ptr,
+                            uint64_t batch, uint64_t max_blocks, uint64_t pad,
+                            uint32_t index_type, void* padded_out, void* workspace,
+                            uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    if (index_type != HP_IDX_U32 && index_type != HP_IDX_U64) return HP_ERR_INDEX_TYPE;
+    if (index_type == HP_IDX_U32 && pad > 0xFFFFFFFFull) return HP_ERR_ARG;
+    if (batch >= (1ull << 58) || ((u128)batch * max_blocks) >> 64) return HP_ERR_OVERFLOW;
+    if (!seq_ptr || (table_len && !table) || (batch && max_blocks && !padded_out))
+        return HP_ERR_NULL;
+    if (!workspace || misaligned(workspace, 256) || workspace_bytes < table_ws_bytes(batch))
+        return HP_ERR_WORKSPACE;
+    hp::TableArgs t{};
+    t.to_csr = false;
+    t.in = table;
+    t.seq_ptr = seq_ptr;
+    t.out = padded_out;
+    t.batch = batch;
+    t.max_blocks = max_blocks;
+    t.table_len = table_len;
+    t.pad = pad;
+    t.workspace = workspace;
+    t.d_status = d_status;
+    return hp::launch_tables(index_type == HP_IDX_U64, t, stream);
 }
 
 HP_API int hp_lane_validate(uint64_t capacity, uint64_t page_tokens, const uint64_t* table,

@@ -132,17 +132,6 @@ __device__ __forceinline__ unsigned dq_bf16(float q, float s)
     return r;
 }
 
-// Quotient n / d for an invariant divisor d <= 2^31 from a multiply-high and shifts:
-// m = floor(2^32 (2^l - d) / d) + 1 with l = ceil(log2 d), computed on the host
-// (Granlund and Montgomery, "Division by invariant integers using multiplication",
-// PLDI 1994, round-up method).
-__device__ __forceinline__ uint32_t div_invariant(uint32_t n, uint32_t m, uint32_t l)
-{
-    if (l == 0) return n;
-    const uint32_t t1 = __umulhi(m, n);
-    return (t1 + ((n - t1) >> 1)) >> (l - 1);
-}
-
 // Quantization schemes of the dequantising gather; the copy kernel's Q template argument
 // is scheme * 2 + (zero points present).
 enum QScheme { kQSlot = 0, kQTensor = 1, kQHead = 2, kQDim = 3 };

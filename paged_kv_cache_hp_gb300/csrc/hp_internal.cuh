@@ -108,6 +108,24 @@ struct PlanArgs {
 // Launches the plan (and, when strict, the block-table check) on `stream`.
 int launch_plan(PlanMode mode, int index_u64, const PlanArgs& a, void* stream);
 
+// Block-table forms (hp_plan.cu): padded [batch, max_blocks] + counts <-> CSR slices.
+struct TableArgs {
+    bool to_csr;
+    const void* in;        // padded (to_csr) or CSR table
+    const void* lens;      // to_csr: token counts
+    const void* seq_ptr;   // from CSR: offsets
+    void* out;             // CSR table (to_csr) or padded
+    void* out2;            // to_csr: seq_ptr out
+    uint64_t batch, max_blocks, page_size, cap, table_len, pad;
+    void* workspace;       // header + batch+1 prefix entries
+    int* d_status;
+};
+int launch_tables(int index_u64, const TableArgs& t, void* stream);
+
+// Layout transpose (hp_layout.cu) between [nb, H, D/x, bs, x] and [nb, bs, H, D].
+int launch_transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H,
+                     uint64_t D, uint64_t x, uint64_t es, bool to_interchange, void* stream);
+
 // Writer side (hp_writer.cu): after a plan on `stream`, the per-page live counts and the
 // zeroing of the slots past them.
 int launch_zero_tails(int index_u64, const PlanArgs& a, unsigned* live, uint64_t row_bytes,
@@ -215,6 +233,26 @@ inline bool allow_dynamic_smem(int dev, int bytes)
         return false;
     done[dev].store(1, std::memory_order_release);
     return true;
+}
+
+// Quotient n / d for an invariant divisor d <= 2^31 from a multiply-high and shifts:
+// m = floor(2^32 (2^l - d) / d) + 1 with l = ceil(log2 d), computed on the host
+// (Granlund and Montgomery, "Division by invariant integers using multiplication",
+// PLDI 1994, round-up method).
+__device__ __forceinline__ uint32_t div_invariant(uint32_t n, uint32_t m, uint32_t l)
+{
+    if (l == 0) return n;
+    const uint32_t t1 = __umulhi(m, n);
+    return (t1 + ((n - t1) >> 1)) >> (l - 1);
+}
+
+// Host side of div_invariant: (m, l) for the divisor g (1 <= g <= 2^31).
+inline void invariant_divisor(uint64_t g, uint32_t* m, uint32_t* l)
+{
+    uint32_t ll = 0;
+    while ((1ull << ll) < g) ++ll;  // ceil(log2 g)
+    *l = ll;
+    *m = (uint32_t)(((((unsigned __int128)1) << 32) * ((((unsigned __int128)1) << ll) - g)) / g + 1);
 }
 
 // ------------------------------------------------------- dependent launches

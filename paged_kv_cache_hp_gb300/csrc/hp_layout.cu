@@ -1,0 +1,157 @@
+// hp_layout.cu -- layout conversions at the boundary of the block-paged format.
+//
+// "Block-Paged Layout -- Hurray Format Specification", Framework Compliance: the portable
+// layout is [num_blocks, block_size, num_kv_heads, head_dim]; a producer that stores its
+// cache in a kernel-internal layout such as [num_blocks, num_kv_heads, head_dim/x,
+// block_size, x] must transpose before emitting a descriptor.  (x = 1 is the
+// [num_blocks, num_kv_heads, head_dim, block_size] value-cache form.)
+//
+// Unit of work: one (block, head).  In the internal layout a unit is one contiguous run
+// of block_size*head_dim elements ([head_dim/x, block_size, x]); in the interchange layout
+// it is block_size rows of head_dim elements, one per slot, num_kv_heads*head_dim apart.
+// A CTA stages whole units (up to 32 KiB of them at a time) in shared memory, so both the
+// global reads and the global writes are contiguous vector accesses; only the
+// shared-memory side is permuted.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "hp_internal.cuh"
+
+namespace hp {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int VEC> struct VecT;
+template <> struct VecT<16> { using T = uint4; };
+template <> struct VecT<8> { using T = uint2; };
+template <> struct VecT<4> { using T = unsigned int; };
+template <> struct VecT<2> { using T = unsigned short; };
+template <> struct VecT<1> { using T = unsigned char; };
+
+struct TransposeArgs {
+    const char* src;
+    char* dst;
+    uint64_t units;          // num_blocks * num_heads
+    uint32_t bs, H;          // block_size, num_heads
+    uint32_t cb;             // bytes of one x-chunk (x * element bytes)
+    uint32_t rowb;           // bytes of one head row (head_dim * element bytes)
+    uint32_t vpr;            // VEC-vectors per head row
+    uint32_t vpr_m, vpr_l;   // divide by vpr
+    uint32_t cb_m, cb_l;     // divide by cb
+    uint32_t nv, nv_m, nv_l; // VEC-vectors per unit, divide by nv
+    uint32_t per_tile;       // units staged together (their bytes fit the tile)
+};
+
+// Offset in a staged unit ([D/x, bs, x] order) of byte `byte` of slot t's row.
+__device__ __forceinline__ uint32_t tile_offset(const TransposeArgs& a, uint32_t t, uint32_t byte)
+{
+    const uint32_t dx = div_invariant(byte, a.cb_m, a.cb_l);  // which x-chunk
+    return (dx * a.bs + t) * a.cb + (byte - dx * a.cb);
+}
+
+// Up to per_tile consecutive units are staged at once (up to 32 KiB), so each thread has
+// several vector loads in flight before the CTA synchronises.
+template <int VEC, bool TO_INTERCHANGE>
+__global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs a)
+{
+    using T = typename VecT<VEC>::T;
+    extern __shared__ __align__(16) unsigned char tile[];
+    const uint32_t U = a.bs * a.rowb;  // bytes of a unit
+    const uint64_t row_stride = (uint64_t)a.H * a.rowb;
+    for (uint64_t u0 = (uint64_t)blockIdx.x * a.per_tile; u0 < a.units;
+         u0 += (uint64_t)gridDim.x * a.per_tile) {
+        const uint32_t k_units = (uint32_t)(a.units - u0 < a.per_tile ? a.units - u0 : a.per_tile);
+        const uint32_t n = k_units * a.nv;
+        if (TO_INTERCHANGE) {
+            // internal units u0.. are contiguous: one linear load
+            const T* in = reinterpret_cast<const T*>(a.src + u0 * U);
+            for (uint32_t i = threadIdx.x; i < n; i += kThreads)
+                reinterpret_cast<T*>(tile)[i] = __ldg(in + i);
+            __syncthreads();
+            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+                const uint32_t k = div_invariant(i, a.nv_m, a.nv_l), iv = i - k * a.nv;
+                const uint64_t u = u0 + k, b = u / a.H, h = u - b * a.H;
+                const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
+                const uint32_t byte = (iv - t * a.vpr) * VEC;
+                *reinterpret_cast<T*>(a.dst + (b * a.bs * a.H + h) * a.rowb + t * row_stride + byte) =
+                    *reinterpret_cast<const T*>(tile + k * U + tile_offset(a, t, byte));
+            }
+        } else {
+            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+                const uint32_t k = div_invariant(i, a.nv_m, a.nv_l), iv = i - k * a.nv;
+                const uint64_t u = u0 + k, b = u / a.H, h = u - b * a.H;
+                const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
+                const uint32_t byte = (iv - t * a.vpr) * VEC;
+                *reinterpret_cast<T*>(tile + k * U + tile_offset(a, t, byte)) = __ldg(
+                    reinterpret_cast<const T*>(a.src + (b * a.bs * a.H + h) * a.rowb + t * row_stride + byte));
+            }
+            __syncthreads();
+            T* out = reinterpret_cast<T*>(a.dst + u0 * U);
+            for (uint32_t i = threadIdx.x; i < n; i += kThreads)
+                out[i] = reinterpret_cast<const T*>(tile)[i];
+        }
+        __syncthreads();  // the tile is reused by the next units
+    }
+}
+
+template <int VEC, bool TO>
+int launch_t(const TransposeArgs& a, uint32_t smem, cudaStream_t st)
+{
+    auto kern = transpose_kernel<VEC, TO>;
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms == 0) return HP_ERR_CUDA;
+    const int per_sm = resident_ctas<transpose_kernel<VEC, TO>>(dev, kThreads, smem);
+    if (per_sm == 0) return HP_ERR_CUDA;
+    const uint64_t tiles = (a.units + a.per_tile - 1) / a.per_tile;
+    const uint64_t grid = std::min<uint64_t>(tiles, (uint64_t)sms * per_sm);
+    if (grid == 0) return HP_OK;
+    kern<<<(unsigned)grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H,
+                     uint64_t D, uint64_t x, uint64_t es, bool to_interchange, void* stream)
+{
+    TransposeArgs a{};
+    a.src = static_cast<const char*>(src);
+    a.dst = static_cast<char*>(dst);
+    a.units = nb * H;
+    a.bs = (uint32_t)bs;
+    a.H = (uint32_t)H;
+    a.cb = (uint32_t)(x * es);
+    a.rowb = (uint32_t)(D * es);
+    // widest vector dividing the chunk, the row and both bases
+    const uintptr_t m = a.cb | a.rowb | reinterpret_cast<uintptr_t>(src) |
+                        reinterpret_cast<uintptr_t>(dst);
+    int vec = 1;
+    for (int v = 16; v > 1; v >>= 1)
+        if (m % v == 0) {
+            vec = v;
+            break;
+        }
+    a.vpr = a.rowb / vec;
+    invariant_divisor(a.vpr, &a.vpr_m, &a.vpr_l);
+    invariant_divisor(a.cb, &a.cb_m, &a.cb_l);
+    const uint32_t U = a.bs * a.rowb;
+    a.nv = U / vec;
+    invariant_divisor(a.nv, &a.nv_m, &a.nv_l);
+    a.per_tile = U >= 32768 ? 1 : 32768 / U;
+    const uint32_t smem = a.per_tile * U;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define HP_TR(v)                                                                        \
+    case v:                                                                             \
+        return to_interchange ? launch_t<v, true>(a, smem, st) : launch_t<v, false>(a, smem, st);
+    switch (vec) {
+        HP_TR(16) HP_TR(8) HP_TR(4) HP_TR(2)
+    default:
+        return to_interchange ? launch_t<1, true>(a, smem, st) : launch_t<1, false>(a, smem, st);
+    }
+#undef HP_TR
+}
+
+}  // namespace hp

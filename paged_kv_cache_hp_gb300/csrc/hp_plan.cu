@@ -217,6 +217,146 @@ __global__ void __launch_bounds__(256) table_kernel(const IndexT* __restrict__ t
     }
 }
 
+// ---------------------------------------------------------- block-table forms
+// A padded table [batch, max_blocks] with token counts (the form an attention kernel
+// takes, "Visualize PagedAttention block layout", How the attention kernel uses the block
+// table) versus the CSR slices of the block-paged descriptor.  Sequence s uses the first
+// ceil(len_s / page_size) entries of its row.
+
+template <typename IndexT>
+__global__ void __launch_bounds__(kPlanThreads) padded_scan_kernel(
+    const IndexT* lens, uint64_t batch, uint64_t max_blocks, uint64_t P, uint64_t cap,
+    WsHeader* hdr, unsigned long long* prefix, int* d_status)
+{
+    pdl_trigger();
+    __shared__ unsigned long long s_key, s_carry;
+    if (threadIdx.x == 0) {
+        s_key = kVerdictOk;
+        s_carry = 0;
+    }
+    __syncthreads();
+    for (uint64_t base = 0; base < batch; base += kPlanThreads) {
+        const uint64_t s = base + threadIdx.x;
+        unsigned long long need = 0;
+        if (s < batch) {
+            const unsigned long long len = lens[s];
+            need = len / P + (len % P != 0);
+            if (need > max_blocks) atomicMin(&s_key, verdict_key(kRankLen, s));
+        }
+        unsigned long long ex, ex2, tot, tot2;
+        block_scan2(need, 0, ex, ex2, tot, tot2);
+        const unsigned long long c = s_carry;
+        if (s < batch) prefix[s] = sat_add(c, ex);
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry = sat_add(c, tot);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        unsigned long long key = s_key;
+        const unsigned long long total = s_carry;
+        if (total > cap) key = min(key, verdict_key(kRankOutSize, 0));
+        prefix[batch] = total;
+        hdr->total_units = total;
+        hdr->verdict = key;
+        if (d_status) *d_status = key_status(key);
+    }
+}
+
+template <typename IndexT>
+__global__ void __launch_bounds__(256) padded_fill_kernel(
+    const IndexT* padded, uint64_t batch, uint64_t max_blocks, const WsHeader* hdr,
+    const unsigned long long* prefix, IndexT* table_out, IndexT* seq_ptr_out)
+{
+    pdl_wait();
+    if (hdr->verdict != kVerdictOk) return;
+    if (blockIdx.x == 0 && threadIdx.x == 0) seq_ptr_out[batch] = (IndexT)prefix[batch];
+    const unsigned lane = threadIdx.x & 31;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
+    for (uint64_t s = (uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); s < batch;
+         s += warps) {
+        const unsigned long long at = prefix[s], need = prefix[s + 1] - at;
+        if (lane == 0) seq_ptr_out[s] = (IndexT)at;
+        for (uint64_t j = lane; j < need; j += 32) table_out[at + j] = padded[s * max_blocks + j];
+    }
+}
+
+template <typename IndexT>
+__global__ void __launch_bounds__(kPlanThreads) csr_check_kernel(
+    const IndexT* seq_ptr, uint64_t batch, uint64_t max_blocks, uint64_t table_len,
+    WsHeader* hdr, int* d_status)
+{
+    pdl_trigger();
+    __shared__ unsigned long long s_key;
+    if (threadIdx.x == 0) s_key = kVerdictOk;
+    __syncthreads();
+    for (uint64_t s = threadIdx.x; s < batch; s += kPlanThreads) {
+        const unsigned long long lo = seq_ptr[s], hi = seq_ptr[s + 1];
+        if (hi < lo || hi > table_len || hi - lo > max_blocks)
+            atomicMin(&s_key, verdict_key(kRankLen, s));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        hdr->verdict = s_key;
+        if (d_status) *d_status = key_status(s_key);
+    }
+}
+
+template <typename IndexT>
+__global__ void __launch_bounds__(256) csr_fill_kernel(
+    const IndexT* table, const IndexT* seq_ptr, uint64_t batch, uint64_t max_blocks,
+    unsigned long long pad, const WsHeader* hdr, IndexT* padded_out)
+{
+    pdl_wait();
+    if (hdr->verdict != kVerdictOk) return;
+    const uint64_t n = batch * max_blocks, stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint64_t s = i / max_blocks, j = i - s * max_blocks;
+        const unsigned long long lo = seq_ptr[s], cnt = seq_ptr[s + 1] - lo;
+        padded_out[i] = j < cnt ? table[lo + j] : (IndexT)pad;
+    }
+}
+
+template <typename IndexT>
+int launch_tables_t(const TableArgs& t, cudaStream_t st)
+{
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms == 0) return HP_ERR_CUDA;
+    const uint64_t cap = (uint64_t)sms * 8;
+    WsHeader* hdr = static_cast<WsHeader*>(t.workspace);
+    unsigned long long* prefix =
+        reinterpret_cast<unsigned long long*>(static_cast<char*>(t.workspace) + kWsHeaderBytes);
+    if (t.to_csr) {
+        padded_scan_kernel<IndexT><<<1, kPlanThreads, 0, st>>>(
+            static_cast<const IndexT*>(t.lens), t.batch, t.max_blocks, t.page_size, t.cap, hdr,
+            prefix, t.d_status);
+        if (cudaGetLastError() != cudaSuccess) return HP_ERR_CUDA;
+        uint64_t g = (t.batch + 7) / 8;
+        g = g == 0 ? 1 : (g < cap ? g : cap);
+        return launch_dependent(padded_fill_kernel<IndexT>, (unsigned)g, 256, 0, st,
+                                static_cast<const IndexT*>(t.in), t.batch, t.max_blocks,
+                                (const WsHeader*)hdr, (const unsigned long long*)prefix,
+                                static_cast<IndexT*>(t.out), static_cast<IndexT*>(t.out2)) ==
+                       cudaSuccess
+                   ? HP_OK
+                   : HP_ERR_CUDA;
+    }
+    csr_check_kernel<IndexT><<<1, kPlanThreads, 0, st>>>(
+        static_cast<const IndexT*>(t.seq_ptr), t.batch, t.max_blocks, t.table_len, hdr,
+        t.d_status);
+    if (cudaGetLastError() != cudaSuccess) return HP_ERR_CUDA;
+    const uint64_t n = t.batch * t.max_blocks;
+    if (n == 0) return HP_OK;
+    uint64_t g = (n + 255) / 256;
+    g = g < cap ? g : cap;
+    return launch_dependent(csr_fill_kernel<IndexT>, (unsigned)g, 256, 0, st,
+                            static_cast<const IndexT*>(t.in), static_cast<const IndexT*>(t.seq_ptr),
+                            t.batch, t.max_blocks, (unsigned long long)t.pad, (const WsHeader*)hdr,
+                            static_cast<IndexT*>(t.out)) == cudaSuccess
+               ? HP_OK
+               : HP_ERR_CUDA;
+}
+
 template <typename IndexT>
 int launch_plan_t(PlanMode mode, const PlanArgs& a, cudaStream_t st)
 {
@@ -241,6 +381,13 @@ int launch_plan_t(PlanMode mode, const PlanArgs& a, cudaStream_t st)
 }
 
 }  // namespace
+
+int launch_tables(int index_u64, const TableArgs& t, void* stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return index_u64 ? launch_tables_t<unsigned long long>(t, st)
+                     : launch_tables_t<unsigned int>(t, st);
+}
 
 int launch_plan(PlanMode mode, int index_u64, const PlanArgs& a, void* stream)
 {

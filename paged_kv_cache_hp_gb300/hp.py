@@ -88,6 +88,15 @@ def lib():
                                        u64, vp, vp, vp]),
                 "hp_gather_noalloc": (i, [D, vp, u64, vp, vp]),
                 "hp_copy_pages": (i, [vp, u64, u64, ctypes.c_uint32, vp, vp, u64, vp, vp]),
+                "hp_from_kernel_layout": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32,
+                                              vp]),
+                "hp_to_kernel_layout": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32,
+                                            vp]),
+                "hp_table_workspace_bytes": (i, [u64, pu64]),
+                "hp_padded_to_csr": (i, [vp, vp, u64, u64, u64, ctypes.c_uint32, vp, u64, vp, vp,
+                                         u64, vp, vp]),
+                "hp_csr_to_padded": (i, [vp, u64, vp, u64, u64, u64, ctypes.c_uint32, vp, vp, u64,
+                                         vp, vp]),
                 "hp_zero_tails_scratch_bytes": (i, [D, pu64]),
                 "hp_zero_tails": (i, [D, vp, u64, vp, u64, vp, vp]),
                 "hp_gather_dequant_q": (i, [D, ctypes.POINTER(HpQuantDesc), vp, u64, vp, u64, vp,
@@ -264,6 +273,40 @@ def hp_zero_tails_scratch_bytes(desc):
 def hp_zero_tails(desc, workspace, scratch, d_status=None, stream=None):
     return lib().hp_zero_tails(desc.ref, _p(workspace), _wsn(workspace), _p(scratch),
                                _wsn(scratch), _p(d_status), _stream(stream))
+
+
+def hp_from_kernel_layout(src, dst, num_blocks, block_size, num_heads, head_dim, x, dtype,
+                          stream=None):
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    return lib().hp_from_kernel_layout(_p(src), _p(dst), num_blocks, block_size, num_heads,
+                                       head_dim, x, dt, _stream(stream))
+
+
+def hp_to_kernel_layout(src, dst, num_blocks, block_size, num_heads, head_dim, x, dtype,
+                        stream=None):
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    return lib().hp_to_kernel_layout(_p(src), _p(dst), num_blocks, block_size, num_heads,
+                                     head_dim, x, dt, _stream(stream))
+
+
+def hp_table_workspace_bytes(batch):
+    n = ctypes.c_uint64(0)
+    rc = lib().hp_table_workspace_bytes(batch, ctypes.byref(n))
+    return rc, n.value
+
+
+def hp_padded_to_csr(padded, lens, batch, max_blocks, page_size, index_type, table_out,
+                     table_cap, seq_ptr_out, workspace, d_status=None, stream=None):
+    return lib().hp_padded_to_csr(_p(padded), _p(lens), batch, max_blocks, page_size, index_type,
+                                  _p(table_out), table_cap, _p(seq_ptr_out), _p(workspace),
+                                  _wsn(workspace), _p(d_status), _stream(stream))
+
+
+def hp_csr_to_padded(table, table_len, seq_ptr, batch, max_blocks, pad, index_type, padded_out,
+                     workspace, d_status=None, stream=None):
+    return lib().hp_csr_to_padded(_p(table), table_len, _p(seq_ptr), batch, max_blocks, pad,
+                                  index_type, _p(padded_out), _p(workspace), _wsn(workspace),
+                                  _p(d_status), _stream(stream))
 
 
 def hp_gather_noalloc(desc, out, out_tokens, d_status=None, stream=None):
