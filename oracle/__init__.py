@@ -128,6 +128,12 @@ def lib():
                                            P(u64)]
             L.or_csr_to_padded.restype = i32
             L.or_csr_to_padded.argtypes = [vp, vp, u64, u64, u64, ctypes.c_uint32, vp, P(u64)]
+            L.or_f16_to_double.restype = ctypes.c_double
+            L.or_f16_to_double.argtypes = [ctypes.c_uint16]
+            L.or_bf16_to_double.restype = ctypes.c_double
+            L.or_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.or_attention_decode.restype = None
+            L.or_attention_decode.argtypes = [P(OrDesc), vp, vp, u64, ctypes.c_double, vp]
             L.or_payload.restype = i32
             L.or_payload.argtypes = [u64, u64, u64, u64, u64, u64, P(u64)]
             _lib = L
@@ -288,6 +294,16 @@ class Desc:
         live = np.zeros(max(self.c.num_pages, 1), dtype=np.uint64)
         lib().or_zero_tails(ctypes.byref(self.c), _ptr(live))
         return live[:self.c.num_pages]
+
+    def attention_decode(self, v_pool, q, num_q_heads, scale):
+        """Decode attention over this descriptor's K pool and v_pool (same geometry);
+        q [num_seqs, Hq, D] of the pool's element type.  Returns float64 [S, Hq, D]."""
+        vp_ = np.ascontiguousarray(v_pool)
+        q_ = np.ascontiguousarray(q)
+        out = np.zeros((self.c.num_seqs, num_q_heads, self.c.head_dim), np.float64)
+        lib().or_attention_decode(ctypes.byref(self.c), _ptr(vp_), _ptr(q_), num_q_heads,
+                                  float(scale), _ptr(out))
+        return out
 
     def scatter_append(self, new_rows, new_ptr):
         """Writes into self.pool in place; returns the fault name."""

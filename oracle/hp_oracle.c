@@ -569,6 +569,88 @@ void or_zero_tails(const or_desc* d, uint64_t* live)
     free(referenced);
 }
 
+/* ---------------------------------------------------- decode attention -- */
+/* binary16 and bfloat16 values as doubles, from the IEEE 754 definitions (binary16: 1
+ * sign, 5 exponent bits biased by 15, 10 fraction bits; bfloat16: the upper half of a
+ * binary32). */
+double or_f16_to_double(uint16_t h)
+{
+    const int sign = h >> 15, e = (h >> 10) & 0x1F, f = h & 0x3FF;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp(1.0 + f / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+double or_bf16_to_double(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+static double elem_value(uint32_t dtype, const void* base, uint64_t i)
+{
+    switch (dtype) {
+    case OR_F16: return or_f16_to_double(((const uint16_t*)base)[i]);
+    case OR_BF16: return or_bf16_to_double(((const uint16_t*)base)[i]);
+    case OR_F32: return ((const float*)base)[i];
+    default: return ((const double*)base)[i];
+    }
+}
+
+/* Decode attention over a block-paged K/V cache ([VA] "How the attention kernel uses the
+ * block table"; [HF] Element Lookup for every key and value): for sequence s and query
+ * head qh, kv head g = qh / (Hq / H_kv) (consecutive query heads share a K/V head, as in
+ * grouped-query attention); score_t = scale * sum_d q[s,qh,d] * K(s,t,g,d) for t < len_s;
+ * weights = softmax(scores) (the maximum subtracted before exp); out[s,qh,d] =
+ * sum_t weight_t * V(s,t,g,d).  K comes through the descriptor's pool, V through v_pool
+ * with the same table, offsets and counts; q is [num_seqs, Hq, D] of the pool's element
+ * type; everything is computed in double.  A sequence with no tokens gets zeros. */
+void or_attention_decode(const or_desc* d, const void* v_pool, const void* q, uint64_t Hq,
+                         double scale, double* out)
+{
+    const uint64_t H = d->num_heads, D = d->head_dim, G = Hq / H;
+    or_desc vd = *d;
+    vd.page_pool = (void*)v_pool;
+    for (uint64_t s = 0; s < d->num_seqs; ++s) {
+        const uint64_t len = ix(d, d->seq_lens, s);
+        double* scores = (double*)malloc((len ? len : 1) * sizeof(double));
+        for (uint64_t qh = 0; qh < Hq; ++qh) {
+            const uint64_t g = qh / G;
+            double* o = out + (s * Hq + qh) * D;
+            for (uint64_t dd = 0; dd < D; ++dd) o[dd] = 0.0;
+            if (len == 0) continue;
+            double mx = -INFINITY;
+            for (uint64_t t = 0; t < len; ++t) {
+                double acc = 0.0;
+                for (uint64_t dd = 0; dd < D; ++dd) {
+                    uint64_t flat;
+                    lookup_flat(d, s, t, g, dd, &flat, 0, 0);
+                    acc += elem_value(d->dtype, q, (s * Hq + qh) * D + dd) *
+                           elem_value(d->dtype, d->page_pool, flat);
+                }
+                scores[t] = scale * acc;
+                if (scores[t] > mx) mx = scores[t];
+            }
+            double sum = 0.0;
+            for (uint64_t t = 0; t < len; ++t) {
+                scores[t] = exp(scores[t] - mx);
+                sum += scores[t];
+            }
+            for (uint64_t t = 0; t < len; ++t)
+                for (uint64_t dd = 0; dd < D; ++dd) {
+                    uint64_t flat;
+                    lookup_flat(&vd, s, t, g, dd, &flat, 0, 0);
+                    o[dd] += scores[t] / sum * elem_value(d->dtype, v_pool, flat);
+                }
+        }
+        free(scores);
+    }
+}
+
 /* ------------------------------------------------- layout conversions -- */
 /* [HF] Framework Compliance: a producer whose cache sits in a kernel-internal layout
  * [num_blocks, num_heads, head_dim/x, block_size, x] must transpose it to the interchange
