@@ -490,7 +490,27 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     scratch = torch.empty(nsc, dtype=torch.uint8, device=dev)
     out["zero_tails_step"] = step_us(lambda: hp.hp_zero_tails(d_g, ws, scratch, status))
     assert int(status.item()) == 0, hp.status_name(int(status.item()))
-    del pool, o, new
+    # decode attention over the grown batch: 32 query heads on the 8 K/V heads, reading
+    # every key and value row once through the block table
+    del o
+    torch.cuda.empty_cache()
+    wv = inputs.Workload(**{**w.__dict__, "pool_seed": w.pool_seed + 77})
+    vpool = inputs.device_pool(wv, dev)
+    Hq = 32
+    gq = torch.Generator(device=dev)
+    gq.manual_seed(11)
+    qd = torch.randn((w.num_seqs, Hq, w.head_dim), generator=gq, device=dev).to(torch.bfloat16)
+    ao = torch.empty((w.num_seqs, Hq, w.head_dim), dtype=torch.float32, device=dev)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(d_g, Hq)
+    aws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+    ms = med_ms(lambda: hp.hp_attention_decode(d_g, vpool, qd, Hq, 1 / np.sqrt(w.head_dim), ao,
+                                               aws, status), n=10)
+    kv_bytes = 2 * T * w.row_bytes
+    out["decode_attention"] = entry(kv_bytes + qd.numel() * 2 + ao.numel() * 4, ms,
+                                    note="K and V rows read once; 32 query heads, GQA 4")
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
+    del vpool, aws
+    del pool, new
     torch.cuda.empty_cache()
 
     # kernel-internal [nb, H, D/x, bs, x] -> interchange [nb, bs, H, D], decode-gather pool

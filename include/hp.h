@@ -351,6 +351,33 @@ int hp_zero_tails_scratch_bytes(const hp_paged_desc* desc, uint64_t* bytes);
 int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace_bytes,
                   void* scratch, uint64_t scratch_bytes, int* d_status, void* stream);
 
+/* ---------------------------------------------------------- decode attention */
+/*
+ * Bytes of device workspace hp_attention_decode needs: the plan's (hp_workspace_bytes)
+ * plus fp32 partials for every chunk of HP_ATTN_CHUNK_PAGES pages and query head.
+ */
+#define HP_ATTN_CHUNK_PAGES 32
+int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t num_q_heads,
+                                        uint64_t* bytes);
+
+/*
+ * ASYNC.  Decode attention over the block-paged cache -- the consumer of the block table
+ * in [VA] "How the attention kernel uses the block table".  For every sequence s and query
+ * head qh (of num_q_heads; K/V head g = qh / (num_q_heads / num_heads), grouped-query
+ * sharing): score_t = scale * sum_d q[s, qh, d] * K(s, t, g, d) for t < seq_lens[s],
+ * weights = softmax over t, out[s, qh, d] = sum_t weight_t * V(s, t, g, d), where K comes
+ * from k_desc's pool and V from `v_pool` (same geometry, table, offsets and counts), both
+ * read through the Element Lookup ([HF]).  q (device, [num_seqs, num_q_heads, head_dim])
+ * has the pool's element type (HP_F16 or HP_BF16); out (device, fp32, same shape) gets 0
+ * for a sequence with no tokens.  Arithmetic is fp32.  Supported: head_dim 64, 128 or
+ * 256, num_q_heads / num_heads in {1, 2, 4, 8} (HP_ERR_ARG otherwise).  The descriptor is
+ * validated as hp_plan does (unless HP_PERMISSIVE is set, in which case the caller
+ * vouches for it; an attention reader cannot skip rows).
+ */
+int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const void* q,
+                        uint32_t num_q_heads, float scale, float* out, void* workspace,
+                        uint64_t workspace_bytes, int* d_status, void* stream);
+
 /* --------------------------------------------------------- layout conversions */
 /*
  * ASYNC.  [HF] Framework Compliance: a producer whose cache sits in a kernel-internal

@@ -567,6 +567,81 @@ HP_API int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t wo
 
 namespace {
 
+int attention_ws(const hp_paged_desc* d, uint32_t hq, u64* bytes)
+{
+    u64 plan = 0;
+    int rc = ws_bytes(d, &plan);
+    if (rc) return rc;
+    const u128 chunks = (u128)(d->table_len / HP_ATTN_CHUNK_PAGES) + d->num_seqs + 1;
+    const u128 part = chunks * hq * (d->head_dim + 2) * 4;
+    if ((part + plan) >> 64) return HP_ERR_OVERFLOW;
+    *bytes = plan + (u64)part;
+    return HP_OK;
+}
+
+}  // namespace
+
+HP_API int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t num_q_heads,
+                                               uint64_t* bytes)
+{
+    if (!k_desc || !bytes) return HP_ERR_NULL;
+    return attention_ws(k_desc, num_q_heads, bytes);
+}
+
+HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const void* q,
+                               uint32_t num_q_heads, float scale, float* out, void* workspace,
+                               uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    int rc = check_desc(k_desc);
+    if (rc) return rc;
+    const hp_paged_desc* d = k_desc;
+    if (d->dtype != HP_F16 && d->dtype != HP_BF16) return HP_ERR_DTYPE;
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return HP_ERR_ARG;
+    if (num_q_heads == 0 || num_q_heads % d->num_heads) return HP_ERR_ARG;
+    const u64 G = num_q_heads / d->num_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return HP_ERR_ARG;
+    if (d->num_seqs && (!q || !out)) return HP_ERR_NULL;
+    if (d->num_pages && !v_pool) return HP_ERR_NULL;
+    if (misaligned(v_pool, 64) || misaligned(q, 16) || misaligned(out, 16)) return HP_ERR_ALIGN;
+    u64 need = 0;
+    rc = attention_ws(d, num_q_heads, &need);
+    if (rc) return rc;
+    if (!workspace || misaligned(workspace, 256) || workspace_bytes < need) return HP_ERR_WORKSPACE;
+    u64 plan_bytes = 0;
+    ws_bytes(d, &plan_bytes);
+    hp::PlanArgs pa = plan_args(d, workspace, d_status);
+    pa.chunk_pages = HP_ATTN_CHUNK_PAGES;
+    rc = hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
+    if (rc || d->num_seqs == 0) return rc;
+    hp::AttnArgs a{};
+    a.k_pool = d->page_pool;
+    a.v_pool = v_pool;
+    a.q = q;
+    a.table = d->block_table;
+    a.seq_ptr = d->seq_ptr;
+    a.lens = d->seq_lens;
+    a.num_seqs = d->num_seqs;
+    a.page_size = d->page_size;
+    a.num_pages = d->num_pages;
+    a.table_len = d->table_len;
+    a.Hkv = (uint32_t)d->num_heads;
+    a.Hq = num_q_heads;
+    a.D = (uint32_t)d->head_dim;
+    a.G = (uint32_t)G;
+    a.hgroups = (uint32_t)((d->num_heads + 7) / 8);
+    a.chunk_pages = HP_ATTN_CHUNK_PAGES;
+    a.scale = scale;
+    a.hdr = pa.ws.hdr;
+    a.units_off = pa.ws.units_off;
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes);
+    a.out = out;
+    a.elem_bf16 = d->dtype == HP_BF16;
+    a.d_status = d_status;
+    return hp::launch_attention(d->index_type == HP_IDX_U64, a, stream);
+}
+
+namespace {
+
 int transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H, uint64_t D,
               uint64_t x, uint32_t dtype, bool to_interchange, void* stream)
 {

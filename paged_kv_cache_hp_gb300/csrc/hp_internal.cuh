@@ -89,7 +89,7 @@ inline WsView ws_view(void* ws, uint64_t num_seqs)
 }
 
 // ------------------------------------------------------------------ plan step
-enum PlanMode { kPlanGather = 0, kPlanAppend = 1 };
+enum PlanMode { kPlanGather = 0, kPlanAppend = 1, kPlanAttention = 2 };
 
 struct PlanArgs {
     const void* seq_ptr;
@@ -99,6 +99,7 @@ struct PlanArgs {
     uint64_t num_seqs, page_size, table_len, num_pages;
     uint64_t out_tokens;      // gather: expected total rows
     uint64_t total_new;       // append: expected new_ptr[S]
+    uint64_t chunk_pages;     // attention: pages per work chunk
     int strict;               // check the storage invariants
     int check_out;            // gather: compare the total with out_tokens
     int* d_status;
@@ -107,6 +108,28 @@ struct PlanArgs {
 
 // Launches the plan (and, when strict, the block-table check) on `stream`.
 int launch_plan(PlanMode mode, int index_u64, const PlanArgs& a, void* stream);
+
+// Decode attention (hp_attention.cu), after a kPlanAttention plan on the same stream.
+struct AttnArgs {
+    const void* k_pool;
+    const void* v_pool;
+    const void* q;            // [num_seqs, Hq, D]
+    const void* table;
+    const void* seq_ptr;
+    const void* lens;
+    uint64_t num_seqs, page_size, num_pages, table_len;
+    uint32_t Hkv, Hq, D, G;   // G = Hq / Hkv query heads per K/V head
+    uint32_t hgroups;         // groups of up to 8 K/V heads (one CTA each per chunk)
+    uint64_t chunk_pages;
+    float scale;
+    const WsHeader* hdr;
+    const unsigned long long* units_off;  // chunks per sequence, prefix
+    float* partials;          // [chunks, Hq, D + 2]: m, l, acc
+    float* out;               // [num_seqs, Hq, D] fp32
+    int elem_bf16;            // element type: bf16 (1) or f16 (0)
+    int* d_status;
+};
+int launch_attention(int index_u64, const AttnArgs& a, void* stream);
 
 // Block-table forms (hp_plan.cu): padded [batch, max_blocks] + counts <-> CSR slices.
 struct TableArgs {

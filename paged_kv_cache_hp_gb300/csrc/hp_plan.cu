@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a)
         unsigned long long rows = 0, units = 0;
         if (s < S) {
             const unsigned long long lo = sp[s], hi = sp[s + 1], len = lens[s];
-            if (MODE == kPlanGather) {
+            if (MODE == kPlanGather || MODE == kPlanAttention) {
                 rows = len;
                 units = len / P + (len % P != 0);
                 if (a.strict) {
@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a)
                     else if (units > hi - lo)
                         atomicMin(&s_key, verdict_key(kRankLen, s));
                 }
+                if (MODE == kPlanAttention)  // pages -> chunks of chunk_pages pages
+                    units = units / a.chunk_pages + (units % a.chunk_pages != 0);
             } else {
                 const unsigned long long n0 = np[s], n1 = np[s + 1];
                 const bool ok_new = n0 <= n1 && n1 <= a.total_new;
@@ -362,8 +364,10 @@ int launch_plan_t(PlanMode mode, const PlanArgs& a, cudaStream_t st)
 {
     if (mode == kPlanGather)
         plan_kernel<IndexT, kPlanGather><<<1, kPlanThreads, 0, st>>>(a);
-    else
+    else if (mode == kPlanAppend)
         plan_kernel<IndexT, kPlanAppend><<<1, kPlanThreads, 0, st>>>(a);
+    else
+        plan_kernel<IndexT, kPlanAttention><<<1, kPlanThreads, 0, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return HP_ERR_CUDA;
     if (a.strict && a.table_len > 0) {
         int dev = 0;

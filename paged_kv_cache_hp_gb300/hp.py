@@ -88,6 +88,9 @@ def lib():
                                        u64, vp, vp, vp]),
                 "hp_gather_noalloc": (i, [D, vp, u64, vp, vp]),
                 "hp_copy_pages": (i, [vp, u64, u64, ctypes.c_uint32, vp, vp, u64, vp, vp]),
+                "hp_attention_decode_workspace_bytes": (i, [D, ctypes.c_uint32, pu64]),
+                "hp_attention_decode": (i, [D, vp, vp, ctypes.c_uint32, ctypes.c_float, vp, vp,
+                                            u64, vp, vp]),
                 "hp_from_kernel_layout": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32,
                                               vp]),
                 "hp_to_kernel_layout": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32,
@@ -273,6 +276,19 @@ def hp_zero_tails_scratch_bytes(desc):
 def hp_zero_tails(desc, workspace, scratch, d_status=None, stream=None):
     return lib().hp_zero_tails(desc.ref, _p(workspace), _wsn(workspace), _p(scratch),
                                _wsn(scratch), _p(d_status), _stream(stream))
+
+
+def hp_attention_decode_workspace_bytes(desc, num_q_heads):
+    n = ctypes.c_uint64(0)
+    rc = lib().hp_attention_decode_workspace_bytes(desc.ref, num_q_heads, ctypes.byref(n))
+    return rc, n.value
+
+
+def hp_attention_decode(desc, v_pool, q, num_q_heads, scale, out, workspace, d_status=None,
+                        stream=None):
+    return lib().hp_attention_decode(desc.ref, _p(v_pool), _p(q), num_q_heads, float(scale),
+                                     _p(out), _p(workspace), _wsn(workspace), _p(d_status),
+                                     _stream(stream))
 
 
 def hp_from_kernel_layout(src, dst, num_blocks, block_size, num_heads, head_dim, x, dtype,

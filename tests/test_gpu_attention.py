@@ -1,0 +1,135 @@
+"""GPU parity of hp_attention_decode (decode attention through the block table) against the
+oracle's float64 attention.
+
+Tolerance, derived from the fp32 path: each output is a convex combination of value rows,
+so |out| <= max|V|; the kernel's errors come from fp32 dot products of head_dim terms,
+expf, and fp32 accumulation over at most a few thousand weighted rows per chunk plus the
+chunk merge -- a relative error well under 1e-3 of max|V| (about n * 2^-24 for n terms in
+the worst case).  The bar is |gpu - oracle| <= 1e-3 * max|V| + 1e-6 per element."""
+import numpy as np
+import pytest
+
+from helpers import Batch, index_tensor, sub_batch
+from paged_kv_cache_hp_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(hp, oracle, w, Hq, seed, scale=None):
+    import torch
+    D = w.head_dim
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    b = Batch(w)
+    wv = inputs.Workload(**{**w.__dict__, "pool_seed": w.pool_seed + 77})
+    vpool = inputs.device_pool(wv, "cuda")
+    rng = np.random.default_rng(seed)
+    qf = rng.standard_normal((w.num_seqs, Hq, D)).astype(np.float32)
+    if w.dtype == "bf16":
+        qt = torch.from_numpy(qf).to(torch.bfloat16)
+    else:
+        qt = torch.from_numpy(qf.astype(np.float16))
+    q = qt.to("cuda")
+    rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, Hq)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    out = torch.full((w.num_seqs, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    rc = hp.hp_attention_decode(b.desc, vpool, q, Hq, scale, out, ws, b.status)
+    torch.cuda.synchronize()
+    assert hp.status_name(rc) == "HP_OK" and b.status_value() == 0
+    return b, vpool, qt, out.cpu().numpy(), scale
+
+
+def _check(got, want, vmax):
+    tol = 1e-3 * vmax + 1e-6
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got)) and err.max() <= tol, (err.max(), tol)
+
+
+@pytest.mark.parametrize("dtype,Hkv,G,D,P", [
+    ("bf16", 8, 4, 128, 16), ("f16", 8, 4, 128, 16), ("bf16", 2, 1, 64, 8),
+    ("bf16", 4, 2, 256, 5), ("f16", 3, 8, 128, 3), ("bf16", 12, 1, 128, 32),
+])
+def test_attention_matches_oracle(hp, oracle, dtype, Hkv, G, D, P):
+    # lengths up to ~1300 tokens: several chunks of 32 pages for small pages
+    w = inputs.decode_gather(seed=Hkv * 10 + G + D + P, num_pages=4000, page_size=P,
+                             num_heads=Hkv, head_dim=D, num_seqs=5, len_lo=0, len_hi=1300,
+                             dtype=dtype, index_dtype=np.uint32 if P % 2 == 0 else np.uint64)
+    Hq = Hkv * G
+    b, vpool, qt, got, scale = _run(hp, oracle, w, Hq, seed=P)
+    kh = b.host_pool()
+    vh = vpool.cpu().numpy()
+    od = b.oracle_desc(pool_host=kh)
+    qh = qt.view(torch_int16()).numpy().view(np.uint16)
+    want = od.attention_decode(vh, qh, Hq, scale)
+    _check(got, want, _vmax_read(od, vh, dtype))
+    for s in range(w.num_seqs):
+        if int(w.lens[s]) == 0:
+            assert (got[s] == 0).all()
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
+def _vmax_read(od, vh, dtype):
+    """Largest |V| among the value rows the batch reads (the oracle's gather of V)."""
+    import torch
+    keep = od.pool
+    od.pool = vh
+    od.c.page_pool = vh.ctypes.data
+    rows = od.gather()[0]
+    od.pool = keep
+    od.c.page_pool = keep.ctypes.data
+    if rows.size == 0:
+        return 0.0
+    t = torch.from_numpy(rows.reshape(-1).view(np.int16).copy())
+    f = t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).float().numpy()
+    return float(np.abs(f).max())
+
+
+def test_attention_single_token_and_empty(hp, oracle):
+    """A one-token sequence returns its value row (the weight is 1); an empty one zeros."""
+    import torch
+    w = inputs.decode_gather(seed=5, num_pages=50, page_size=16, num_heads=2, head_dim=128,
+                             num_seqs=3, len_lo=1, len_hi=40, dtype="bf16")
+    lens = w.lens.copy()
+    lens[0], lens[2] = 1, 0
+    w = inputs.Workload(**{**w.__dict__, "lens": lens})
+    b, vpool, qt, got, scale = _run(hp, oracle, w, 4, seed=1)
+    page = int(w.table[0])
+    vrow = torch.from_numpy(vpool.cpu().numpy()[page, 0].view(np.int16).copy()).view(
+        torch.bfloat16).float().numpy().reshape(2, 128)
+    for qh in range(4):
+        np.testing.assert_allclose(got[0, qh], vrow[qh // 2], rtol=0, atol=1e-6)
+    assert (got[2] == 0).all()
+
+
+def test_attention_full_size_sampled(hp, oracle):
+    """The decode step's grown batch (256 sequences up to 32k tokens, 8 K/V heads, 32 query
+    heads, bf16): a few whole sequences against the oracle."""
+    import torch
+    w = inputs.config("decode_append", "full")
+    b, vpool, qt, got, scale = _run(hp, oracle, w, 32, seed=3)
+    seqs = [0, 77, 255]
+    table, seq_ptr, lens = sub_batch(w, seqs)
+    kh = b.pool.cpu().numpy()
+    vh = vpool.cpu().numpy()
+    sub = oracle.Desc(kh, table, seq_ptr, lens, num_pages=w.num_pages, page_size=16,
+                      num_heads=8, head_dim=128, dtype="bf16", index_type=0)
+    qh = qt.view(torch.int16).numpy().view(np.uint16)[seqs]
+    want = sub.attention_decode(vh, qh, 32, scale)
+    _check(got[seqs], want, _vmax_read(sub, vh, "bf16"))
+
+
+def test_attention_rejections(hp, oracle):
+    import torch
+    w = inputs.config("decode_gather", "small")   # 32 heads of 128, fp16
+    b = Batch(w)
+    rc, n = hp.hp_attention_decode_workspace_bytes(b.desc, 32)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    q = torch.zeros((w.num_seqs, 48, 128), dtype=torch.float16, device="cuda")
+    out = torch.zeros((w.num_seqs, 48, 128), dtype=torch.float32, device="cuda")
+    assert hp.status_name(hp.hp_attention_decode(b.desc, b.pool, q, 48, 1.0, out, ws)) == \
+        "HP_ERR_ARG"   # 48 query heads over 32 K/V heads
+    assert hp.status_name(hp.hp_attention_decode(b.desc, b.pool, q, 32, 1.0, out, ws[:100])) == \
+        "HP_ERR_WORKSPACE"
