@@ -332,6 +332,71 @@ def time_oracle(w, host_pool, oracle_mod, budget_s, max_tokens=None):
 
 
 # ----------------------------------------------------------------------------- ops
+def median_ms(fn, stream, n=20, warm=3):
+    """Median of n CUDA-event timings of fn() on `stream`, after `warm` untimed calls."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def rate_entry(bytes_, ms, peak, **kw):
+    gbps = bytes_ / (ms * 1e-3) / 1e9
+    return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
+
+
+def attention_only(scale, dev, hp, inputs, peak, reps):
+    """Decode attention alone on the decode-append batch at `scale` ("full": 256 sequences
+    of 1K-32K tokens; "mid": 32 of them, about 2.5 GB on the device, the profiler's case)."""
+    import torch
+    w = inputs.config("decode_append", scale)
+    pool = inputs.device_pool(w, dev)
+    d_k = hp.PagedDesc(pool, idx_tensor(w.table, dev), idx_tensor(w.seq_ptr, dev),
+                       idx_tensor(w.lens, dev), num_pages=w.num_pages, page_size=w.page_size,
+                       num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+    stream = torch.cuda.current_stream()
+    res = attention_measurement(dev, hp, inputs, w, d_k, peak,
+                                lambda b, ms, **kw: rate_entry(b, ms, peak, **kw),
+                                lambda fn, n: median_ms(fn, stream, n), reps=reps)
+    res.update(op="decode_attention", workload=w.name, num_seqs=w.num_seqs,
+               total_tokens=w.total_tokens, num_heads=w.num_heads, head_dim=w.head_dim)
+    return res
+
+
+def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, reps=10):
+    """hp_attention_decode over batch w (K pool and descriptor d_k; a V pool of the same
+    geometry is drawn here): Hq query heads, bytes = K and V rows once + q + out."""
+    import torch
+    wv = inputs.Workload(**{**w.__dict__, "pool_seed": w.pool_seed + 77})
+    vpool = inputs.device_pool(wv, dev)
+    gq = torch.Generator(device=dev)
+    gq.manual_seed(11)
+    qd = torch.randn((w.num_seqs, Hq, w.head_dim), generator=gq, device=dev).to(torch.bfloat16)
+    ao = torch.empty((w.num_seqs, Hq, w.head_dim), dtype=torch.float32, device=dev)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(d_k, Hq)
+    assert rc == 0
+    aws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms = med_ms(lambda: hp.hp_attention_decode(d_k, vpool, qd, Hq, 1 / np.sqrt(w.head_dim), ao,
+                                               aws, status), n=reps)
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
+    kv_bytes = 2 * w.total_tokens * w.row_bytes
+    res = entry(kv_bytes + qd.numel() * 2 + ao.numel() * 4, ms,
+                note="K and V rows read once; %d query heads, GQA %d" % (Hq, Hq // w.num_heads))
+    del vpool, aws
+    torch.cuda.empty_cache()
+    return res
+
+
 def ops_measurements(dev, hp, inputs, peak, reps=20):
     """The other rows of the path at their own configurations (bytes as in
     gather_bytes; medians over reps, inputs larger than L2 except where noted)."""
@@ -340,18 +405,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     stream = torch.cuda.current_stream()
 
     def med_ms(fn, n=reps, warm=3):
-        for _ in range(warm):
-            fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(n):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+        return median_ms(fn, stream, n, warm)
 
     def step_us(fn, n=300):
         """Steps issued back to back, as a decode loop issues them: (issue-bound) time
@@ -391,8 +445,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
         return {"us_per_step_back_to_back": round(loop, 2), "us_per_step_graph": graph}
 
     def entry(bytes_, ms, **kw):
-        gbps = bytes_ / (ms * 1e-3) / 1e9
-        return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
+        return rate_entry(bytes_, ms, peak, **kw)
 
     # tiny prefix-sharing gather: latency
     w = inputs.tiny_prefix_gather()
@@ -494,22 +547,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     # every key and value row once through the block table
     del o
     torch.cuda.empty_cache()
-    wv = inputs.Workload(**{**w.__dict__, "pool_seed": w.pool_seed + 77})
-    vpool = inputs.device_pool(wv, dev)
-    Hq = 32
-    gq = torch.Generator(device=dev)
-    gq.manual_seed(11)
-    qd = torch.randn((w.num_seqs, Hq, w.head_dim), generator=gq, device=dev).to(torch.bfloat16)
-    ao = torch.empty((w.num_seqs, Hq, w.head_dim), dtype=torch.float32, device=dev)
-    rc, nws = hp.hp_attention_decode_workspace_bytes(d_g, Hq)
-    aws = torch.zeros(nws, dtype=torch.uint8, device=dev)
-    ms = med_ms(lambda: hp.hp_attention_decode(d_g, vpool, qd, Hq, 1 / np.sqrt(w.head_dim), ao,
-                                               aws, status), n=10)
-    kv_bytes = 2 * T * w.row_bytes
-    out["decode_attention"] = entry(kv_bytes + qd.numel() * 2 + ao.numel() * 4, ms,
-                                    note="K and V rows read once; 32 query heads, GQA 4")
-    assert int(status.item()) == 0, hp.status_name(int(status.item()))
-    del vpool, aws
+    out["decode_attention"] = attention_measurement(dev, hp, inputs, w, d_g, peak, entry, med_ms)
     del pool, new
     torch.cuda.empty_cache()
 
@@ -555,8 +593,19 @@ def main():
                     choices=["decode_gather", "decode_append", "prefix_sharing", "quantized_pool",
                              "quantized_pool_mid"],
                     help="batch the timed steps gather (default: the decode-sized gather)")
+    ap.add_argument("--attention", choices=["full", "mid"],
+                    help="time only hp_attention_decode on the decode-append batch at this "
+                         "scale (warm-up calls, then --steps timed calls) and print its line")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.attention:
+        import torch
+        from paged_kv_cache_hp_gb300 import build, hp, inputs
+        build.build()
+        hp.lib()
+        print(json.dumps(attention_only(args.attention, "cuda", hp, inputs, peak_hbm()[0],
+                                        args.steps)))
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

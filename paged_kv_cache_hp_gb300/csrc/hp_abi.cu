@@ -600,6 +600,7 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     if (num_q_heads == 0 || num_q_heads % d->num_heads) return HP_ERR_ARG;
     const u64 G = num_q_heads / d->num_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return HP_ERR_ARG;
+    if (d->page_size > (1u << 26)) return HP_ERR_ARG;  // token offsets in a chunk fit 32 bits
     if (d->num_seqs && (!q || !out)) return HP_ERR_NULL;
     if (d->num_pages && !v_pool) return HP_ERR_NULL;
     if (misaligned(v_pool, 64) || misaligned(q, 16) || misaligned(out, 16)) return HP_ERR_ALIGN;
@@ -628,7 +629,7 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     a.Hq = num_q_heads;
     a.D = (uint32_t)d->head_dim;
     a.G = (uint32_t)G;
-    a.hgroups = (uint32_t)((d->num_heads + 7) / 8);
+    hp::invariant_divisor(d->page_size, &a.p_m, &a.p_l);
     a.chunk_pages = HP_ATTN_CHUNK_PAGES;
     a.scale = scale;
     a.hdr = pa.ws.hdr;

@@ -9,15 +9,17 @@
 //
 // Decode attention reads every key and value once for about 2G flops per byte, so it is
 // bound by HBM, not by arithmetic: it runs on the CUDA cores.
-//   attn_kernel     one CTA per (sequence, chunk of chunk_pages pages, group of <= 8 K/V
-//                   heads); warp w takes K/V head 8*group + w, so a CTA reads each token's
-//                   rows of those heads as one contiguous run.  Lane l owns dims
-//                   [l*E, l*E+E) (E = D/32).  Tokens go 32/G at a time: the 32 (token,
-//                   head) partial dot products are summed across the warp with a
-//                   transposed butterfly (31 shuffles, lane l ends with pair l), then an
-//                   online softmax per head updates the running max, sum and the lane's
-//                   E dims of each head's weighted value sum.  Each chunk leaves
-//                   (max, sum, acc[D]) per query head in the workspace.
+//   attn_kernel     every warp runs its own (chunk of chunk_pages pages, K/V head) items.
+//                   It streams the chunk's rows of that head into a ring of kStages
+//                   shared-memory stages with cp.async (a step's K rows, then its V rows;
+//                   the page of each token comes from the chunk's page IDs, held one per
+//                   lane), so the loads of the next steps are in flight while it computes.
+//                   Lane l owns dims [l*E, l*E+E) (E = D/32).  A step is TS tokens: their
+//                   (token, query head) partial dot products are summed across the warp with
+//                   a transposed butterfly (one shuffle per product), then an online softmax
+//                   per query head updates the running max, sum and the lane's E dims of the
+//                   weighted value sum.  Each item leaves (max, sum, acc[D]) per query head
+//                   in the workspace.
 //   combine_kernel  one warp per (sequence, query head) merges its chunks' partials.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -31,136 +33,224 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;  // per-warp ring of shared-memory stages
 
 template <int E> struct Pack;
 template <> struct Pack<2> { using T = unsigned int; };
 template <> struct Pack<4> { using T = uint2; };
 template <> struct Pack<8> { using T = uint4; };
 
+// Geometry of one step for G query heads per K/V head and E = D/32 dims per lane.
+template <int G, int E> struct Step {
+    // TS tokens per step: their TS*G (token, head) dot products fill NP <= 32 slots and a
+    // stage (the step's K rows, then its V rows) is at most 4 KiB.
+    static constexpr int TS = (32 / G) < (32 / E) ? (32 / G) : (32 / E);
+    static constexpr int NP = TS * G;        // partial dot products per step
+    static constexpr int R = 32 / NP;        // lanes holding the same reduced partial
+    static constexpr int ROW = 64 * E;       // bytes of one head's K or V row
+    static constexpr int PIECES = ROW / 16;  // 16-byte pieces of a row
+    static constexpr int LT = 32 / TS;       // lanes copying one token's rows
+    static constexpr int NPC = PIECES / LT;  // pieces of each row a lane copies
+    static constexpr int STAGE = 2 * TS * ROW;
+    static constexpr int WBUF = 32 * 8;      // the step's weights, each stored twice
+    static constexpr int WARP_SMEM = kStages * STAGE + WBUF;
+};
+
+template <int G, int E>
+constexpr int smem_bytes() { return kWarps * Step<G, E>::WARP_SMEM; }
+
+// Two fp32 values in one 64-bit register pair, for the packed f32x2 arithmetic.
+using f2 = unsigned long long;
+__device__ __forceinline__ f2 pack2(float lo, float hi)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(f2 v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b)
+{
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float exp2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// A 32-bit word of two 16-bit elements as an f2 (element 0 low).
 template <bool BF16>
-__device__ __forceinline__ float to_f32(unsigned short v)
+__device__ __forceinline__ f2 widen2(unsigned w)
 {
-    if (BF16) return __uint_as_float((unsigned)v << 16);
-    return __half2float(__ushort_as_half(v));
+    if (BF16) return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    return pack2(f.x, f.y);
 }
 
 template <bool BF16, int E>
-__device__ __forceinline__ void unpack(const typename Pack<E>::T& raw, float f[E])
+__device__ __forceinline__ void widen_row(const typename Pack<E>::T& raw, f2 v[E / 2])
 {
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(&raw);
+    const unsigned* w = reinterpret_cast<const unsigned*>(&raw);
 #pragma unroll
-    for (int k = 0; k < E; ++k) f[k] = to_f32<BF16>(h[k]);
+    for (int k = 0; k < E / 2; ++k) v[k] = widen2<BF16>(w[k]);
 }
 
-// E consecutive 16-bit elements at p (E*2 bytes, aligned) as floats.
-template <bool BF16, int E>
-__device__ __forceinline__ void load_row(const unsigned short* p, float f[E])
+// 16 bytes global -> shared, L2 only; src_bytes 0 stores zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes)
 {
-    typename Pack<E>::T raw = __ldg(reinterpret_cast<const typename Pack<E>::T*>(p));
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(&raw);
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Request one step's rows: tokens x0 .. x0+TS-1 of the chunk (offsets from its first
+// token), K rows then V rows of head g.  Lane l copies token l / LT: pieces
+// l % LT + LT*m of both rows, so the LT lanes of a token read LT*16 contiguous bytes per
+// instruction.  Tokens at or past n_tok become zero rows.
+template <typename IndexT, int G, int E>
+__device__ __forceinline__ void issue_step(const AttnArgs& a, unsigned char* stage, uint32_t x0,
+                                           uint32_t n_tok, IndexT my_page, uint32_t g,
+                                           unsigned lane)
+{
+    using S = Step<G, E>;
+    const char* K = static_cast<const char*>(a.k_pool);
+    const char* V = static_cast<const char*>(a.v_pool);
+    const unsigned i = lane / S::LT, jp = lane % S::LT;
+    const uint32_t x = x0 + i;
+    const uint32_t pi = div_invariant(x, a.p_m, a.p_l);  // the chunk's page holding x
+    const IndexT page = __shfl_sync(0xffffffffu, my_page, (int)(pi & 31));
+    const bool live = x < n_tok;
+    const uint64_t slot_row = (uint64_t)page * a.page_size + (x - pi * (uint32_t)a.page_size);
+    const uint64_t off = (slot_row * a.Hkv + g) * S::ROW + jp * 16;
+    const char* ks = live ? K + off : K;
+    const char* vs = live ? V + off : K;
+    const uint32_t n = live ? 16u : 0u;
+    unsigned char* kd = stage + i * S::ROW + jp * 16;
 #pragma unroll
-    for (int k = 0; k < E; ++k) f[k] = to_f32<BF16>(h[k]);
+    for (int m = 0; m < S::NPC; ++m) {
+        cp_async16(kd + m * S::LT * 16, ks + m * S::LT * 16, n);
+        cp_async16(kd + S::TS * S::ROW + m * S::LT * 16, vs + m * S::LT * 16, n);
+    }
 }
 
 template <typename IndexT, bool BF16, int G, int E>
 __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
 {
-    // TS tokens per step: their TS*G (token, head) dot products fill NP <= 32 slots, and the
-    // step's raw K and V rows take TS*E registers (at most 64).
-    constexpr int TS = (32 / G) < (64 / E) ? (32 / G) : (64 / E);
-    constexpr int NP = TS * G;  // partial dot products per step
-    constexpr int R = 32 / NP;  // lanes holding the same reduced partial
-    pdl_wait();                 // the plan before this launch is complete
+    using S = Step<G, E>;
+    constexpr int TS = S::TS, NP = S::NP, R = S::R;
+    using RowT = typename Pack<E>::T;
+    extern __shared__ __align__(16) unsigned char smem[];
+    pdl_wait();  // the plan before this launch is complete
     if (a.hdr->verdict != kVerdictOk) return;
     const unsigned warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint64_t items = a.hdr->total_units * a.hgroups;
+    unsigned char* ring = smem + warp * S::WARP_SMEM;
+    f2* wbuf = reinterpret_cast<f2*>(ring + kStages * S::STAGE);
+    const uint64_t items = a.hdr->total_units * a.Hkv;  // (chunk, K/V head) pairs
     const IndexT* table = static_cast<const IndexT*>(a.table);
     const IndexT* sp = static_cast<const IndexT*>(a.seq_ptr);
     const IndexT* lens = static_cast<const IndexT*>(a.lens);
-    const unsigned short* K = static_cast<const unsigned short*>(a.k_pool);
-    const unsigned short* V = static_cast<const unsigned short*>(a.v_pool);
     const unsigned short* Q = static_cast<const unsigned short*>(a.q);
     const uint64_t P = a.page_size, D = a.D;
-    // the reduced partial lane l holds: token j / G, head j % G of the step
-    const unsigned j = lane / R, my_tok = j / G, my_head = j % G;
+    // After the reduction lane l holds slot lx = l / R: token lx / G, head lx % G of the
+    // step.  Before it, lane l keeps slot k ^ lx at array position k, so every level of
+    // the transposed butterfly keeps the low half and sends the high half: position k
+    // reads K row (k / G) ^ lt with query head (k % G) ^ lh.
+    const unsigned lx = lane / R, my_tok = lx / G, my_head = lx % G;
+    const unsigned lt = my_tok, lh = my_head;
+    uint32_t roff[TS];  // byte offset in a stage of the K row position i reads
+#pragma unroll
+    for (int i = 0; i < TS; ++i) roff[i] = (i ^ lt) * S::ROW + lane * (2 * E);
+    const float qscale = a.scale * 1.4426950408889634f;  // scores in log2 units
 
-    for (uint64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const uint64_t u = it / a.hgroups;
-        const uint32_t g = (uint32_t)(it - u * a.hgroups) * kWarps + warp;
-        if (g >= a.Hkv) continue;  // whole warp; no block-wide barrier below
+    // every warp runs its own items: no barrier across the CTA
+    for (uint64_t it = (uint64_t)blockIdx.x * kWarps + warp; it < items;
+         it += (uint64_t)gridDim.x * kWarps) {
+        const uint64_t u = it / a.Hkv;
+        const uint32_t g = (uint32_t)(it - u * a.Hkv);
         const uint64_t s = find_seq(a.units_off, a.num_seqs, u);
         const uint64_t c = u - a.units_off[s];
-        const uint64_t len = lens[s];
         const uint64_t t_begin = c * a.chunk_pages * P;
-        const uint64_t t_end = umin(len, t_begin + a.chunk_pages * P);
-        const uint64_t tab0 = sp[s];
+        const uint32_t n_tok = (uint32_t)(umin(lens[s], t_begin + a.chunk_pages * P) - t_begin);
+        const uint64_t n_pg = (n_tok + P - 1) / P;
+        // the chunk's page IDs, one per lane (a chunk has at most 32 pages)
+        const IndexT my_page = lane < n_pg ? table[(uint64_t)sp[s] + c * a.chunk_pages + lane] : IndexT(0);
+        const uint32_t steps = (n_tok + TS - 1) / TS;
+#pragma unroll
+        for (int k = 0; k < kStages - 1; ++k) {
+            if ((uint32_t)k < steps)
+                issue_step<IndexT, G, E>(a, ring + k * S::STAGE, k * TS, n_tok, my_page, g, lane);
+            cp_async_commit();
+        }
 
-        float qv[G][E];
+        f2 qp[G][E / 2];  // position h holds query head h ^ lh, scaled
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            load_row<BF16, E>(Q + ((s * a.Hq + (uint64_t)g * G + h) * D + lane * E), qv[h]);
+            const RowT raw = __ldg(reinterpret_cast<const RowT*>(
+                Q + ((s * a.Hq + (uint64_t)g * G + (h ^ lh)) * D + lane * E)));
+            widen_row<BF16, E>(raw, qp[h]);
 #pragma unroll
-            for (int k = 0; k < E; ++k) qv[h][k] *= a.scale;
+            for (int e = 0; e < E / 2; ++e) qp[h][e] = mul2(qp[h][e], pack2(qscale, qscale));
         }
-        float m[G], l[G], acc[G][E];
+        float m[G], l[G];
+        f2 acc[G][E / 2];  // the lane's dims of each head's weighted value sum
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             m[h] = -INFINITY;
             l[h] = 0.0f;
 #pragma unroll
-            for (int k = 0; k < E; ++k) acc[h][k] = 0.0f;
+            for (int e = 0; e < E / 2; ++e) acc[h][e] = 0ull;
         }
 
-        // the chunk's page IDs, one per lane (a chunk has at most 32 pages)
-        const uint64_t n_pg = (t_end - t_begin + P - 1) / P;
-        const unsigned long long my_page =
-            lane < n_pg ? (unsigned long long)table[tab0 + c * a.chunk_pages + lane] : 0ull;
+        for (uint32_t k = 0; k < steps; ++k) {
+            const uint32_t kn = k + kStages - 1;
+            if (kn < steps)
+                issue_step<IndexT, G, E>(a, ring + (kn % kStages) * S::STAGE, kn * TS, n_tok,
+                                         my_page, g, lane);
+            cp_async_commit();
+            cp_async_wait<kStages - 1>();  // this lane's pieces of step k have landed
+            __syncwarp();                  // and every other lane's
+            const unsigned char* st = ring + (k % kStages) * S::STAGE;
 
-        for (uint64_t t0 = t_begin; t0 < t_end; t0 += TS) {
-            // every K and V row of the step is requested before any arithmetic
-            typename Pack<E>::T kraw[TS], vraw[TS];
+            float part[NP];
 #pragma unroll
             for (int i = 0; i < TS; ++i) {
-                const uint64_t t = t0 + i;
-                if (t < t_end) {  // uniform across the warp
-                    const unsigned long long page =
-                        __shfl_sync(0xffffffffu, my_page, (int)((t - t_begin) / P));
-                    const uint64_t row = ((page * P + t % P) * a.Hkv + g) * D + lane * E;
-                    kraw[i] = __ldg(reinterpret_cast<const typename Pack<E>::T*>(K + row));
-                    vraw[i] = __ldg(reinterpret_cast<const typename Pack<E>::T*>(V + row));
-                } else {
-                    kraw[i] = typename Pack<E>::T{};
-                    vraw[i] = typename Pack<E>::T{};
-                }
-            }
-            float part[NP];  // (token i, head h) at i*G + h
-#pragma unroll
-            for (int i = 0; i < TS; ++i) {
-                float kf[E];
-                unpack<BF16, E>(kraw[i], kf);
+                f2 kv[E / 2];
+                widen_row<BF16, E>(*reinterpret_cast<const RowT*>(st + roff[i]), kv);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    float d = 0.0f;
+                    f2 d = mul2(qp[h][0], kv[0]);
 #pragma unroll
-                    for (int k = 0; k < E; ++k) d = fmaf(qv[h][k], kf[k], d);
-                    part[i * G + h] = d;
+                    for (int e = 1; e < E / 2; ++e) d = fma2(qp[h][e], kv[e], d);
+                    float d0, d1;
+                    unpack2(d, d0, d1);
+                    part[i * G + h] = d0 + d1;
                 }
             }
-            // transposed butterfly over the top log2(NP) lane bits: lane l keeps slot l / R
-            // summed over those bits; a plain butterfly over the low bits finishes the sum.
 #pragma unroll
             for (int o = 16, n = NP; n > 1; o >>= 1, n >>= 1) {
-                const bool upper = lane & o;
 #pragma unroll
-                for (int k = 0; k < n / 2; ++k) {
-                    const float send = upper ? part[k] : part[k + n / 2];
-                    const float keep = upper ? part[k + n / 2] : part[k];
-                    part[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
+                for (int e = 0; e < n / 2; ++e)
+                    part[e] += __shfl_xor_sync(0xffffffffu, part[e + n / 2], o);
             }
 #pragma unroll
             for (int o = R / 2; o >= 1; o >>= 1) part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
-            const float sc = (t0 + my_tok < t_end) ? part[0] : -INFINITY;
+            const float sc = (k * TS + my_tok < n_tok) ? part[0] : -INFINITY;
             // per-head step maximum: lanes of one head differ only in the token bits (>= R*G)
             float bm = sc;
 #pragma unroll
@@ -169,10 +259,11 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 mnew[h] = fmaxf(m[h], __shfl_sync(0xffffffffu, bm, h * R));
-                corr[h] = expf(m[h] - mnew[h]);  // 0 on the first step (m = -inf)
+                corr[h] = exp2_approx(m[h] - mnew[h]);  // 0 on the first step (m = -inf)
                 if ((int)my_head == h) my_m = mnew[h];
             }
-            const float p = expf(sc - my_m);  // 0 for tokens past the chunk
+            const float p = exp2_approx(sc - my_m);  // 0 for tokens past the chunk
+            if (lane % R == 0) wbuf[lx] = pack2(p, p);
             float ps = p;
 #pragma unroll
             for (int o = R * G; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
@@ -180,20 +271,24 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
             for (int h = 0; h < G; ++h) {
                 l[h] = l[h] * corr[h] + __shfl_sync(0xffffffffu, ps, h * R);
                 m[h] = mnew[h];
+                const f2 c2 = pack2(corr[h], corr[h]);
 #pragma unroll
-                for (int k = 0; k < E; ++k) acc[h][k] *= corr[h];
+                for (int e = 0; e < E / 2; ++e) acc[h][e] = mul2(acc[h][e], c2);
             }
+            __syncwarp();  // the weights are in wbuf
 #pragma unroll
             for (int i = 0; i < TS; ++i) {
-                float vf[E];
-                unpack<BF16, E>(vraw[i], vf);  // zero rows past the chunk: weight 0
+                f2 vv[E / 2];  // rows past the chunk are zeros with weight 0
+                widen_row<BF16, E>(
+                    *reinterpret_cast<const RowT*>(st + (TS + i) * S::ROW + lane * (2 * E)), vv);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float w = __shfl_sync(0xffffffffu, p, (i * G + h) * R);
+                    const f2 w = wbuf[i * G + h];
 #pragma unroll
-                    for (int k = 0; k < E; ++k) acc[h][k] = fmaf(w, vf[k], acc[h][k]);
+                    for (int e = 0; e < E / 2; ++e) acc[h][e] = fma2(w, vv[e], acc[h][e]);
                 }
             }
+            __syncwarp();  // the stage and wbuf are rewritten by later steps
         }
         float* out = a.partials + (u * a.Hq + (uint64_t)g * G) * (D + 2);
 #pragma unroll
@@ -204,7 +299,12 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
                 o[1] = l[h];
             }
 #pragma unroll
-            for (int k = 0; k < E; ++k) o[2 + lane * E + k] = acc[h][k];
+            for (int e = 0; e < E / 2; ++e) {
+                float v0, v1;
+                unpack2(acc[h][e], v0, v1);
+                o[2 + lane * E + 2 * e] = v0;
+                o[3 + lane * E + 2 * e] = v1;
+            }
         }
     }
 }
@@ -227,13 +327,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a)
         float L = 0.0f;
         for (uint64_t c = c0; c < c1; ++c) {
             const float* pc = a.partials + (c * a.Hq + qh) * (D + 2);
-            L += pc[1] * expf(pc[0] - M);
+            L += pc[1] * exp2f(pc[0] - M);
         }
         for (uint64_t d = lane; d < D; d += 32) {
             float acc = 0.0f;
             for (uint64_t c = c0; c < c1; ++c) {
                 const float* pc = a.partials + (c * a.Hq + qh) * (D + 2);
-                acc = fmaf(pc[2 + d], expf(pc[0] - M), acc);
+                acc = fmaf(pc[2 + d], exp2f(pc[0] - M), acc);
             }
             out[d] = c1 > c0 ? acc / L : 0.0f;
         }
@@ -243,13 +343,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a)
 template <typename IndexT, bool BF16, int G, int E>
 int launch_g(const AttnArgs& a, cudaStream_t st)
 {
+    constexpr int smem = smem_bytes<G, E>();
     int dev = 0;
     const int sms = current_sms(&dev);
     if (sms == 0) return HP_ERR_CUDA;
-    const int per_sm = resident_ctas<attn_kernel<IndexT, BF16, G, E>>(dev, kThreads, 0);
+    if (!allow_dynamic_smem<attn_kernel<IndexT, BF16, G, E>>(dev, smem)) return HP_ERR_CUDA;
+    const int per_sm = resident_ctas<attn_kernel<IndexT, BF16, G, E>>(dev, kThreads, smem);
     if (per_sm == 0) return HP_ERR_CUDA;
-    if (launch_dependent(attn_kernel<IndexT, BF16, G, E>, (unsigned)(sms * per_sm), kThreads, 0,
-                         st, a) != cudaSuccess)
+    if (launch_dependent(attn_kernel<IndexT, BF16, G, E>, (unsigned)(sms * per_sm), kThreads,
+                         smem, st, a) != cudaSuccess)
         return HP_ERR_CUDA;
     uint64_t g2 = (a.num_seqs * a.Hq + 7) / 8;
     const uint64_t cap = (uint64_t)sms * 8;

@@ -119,7 +119,7 @@ struct AttnArgs {
     const void* lens;
     uint64_t num_seqs, page_size, num_pages, table_len;
     uint32_t Hkv, Hq, D, G;   // G = Hq / Hkv query heads per K/V head
-    uint32_t hgroups;         // groups of up to 8 K/V heads (one CTA each per chunk)
+    uint32_t p_m, p_l;        // div_invariant constants of page_size
     uint64_t chunk_pages;
     float scale;
     const WsHeader* hdr;

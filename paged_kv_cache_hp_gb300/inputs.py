@@ -301,6 +301,8 @@ def config(name: str, scale: str = "full") -> Workload:
         return decode_gather(num_pages=600, num_seqs=7, len_lo=1, len_hi=700,
                              name="decode_gather_small") if small else decode_gather()
     if name == "decode_append":
+        if scale == "mid":  # 32 sequences, about 2.5 GB of K and V pools
+            return decode_append(num_pages=40000, num_seqs=32, name="decode_append_mid")
         return decode_append(num_pages=2000, num_seqs=9, len_lo=1, len_hi=2000,
                              name="decode_append_small") if small else decode_append()
     if name == "prefix_sharing":
