@@ -250,48 +250,73 @@ def time_copy_kernel(step, launches, stream):
 
 
 def e2e_gather(w, dev, hp, inputs, steps):
-    """The same step through host buffers: every step copies the pool and index
-    buffers from pinned host memory, gathers through the C ABI, and reads the gathered
-    tensor back to pinned host memory."""
+    """The same step through host buffers: every step uploads the pool and index buffers
+    from pinned host memory, gathers through the C ABI and downloads the gathered tensor
+    to pinned host memory.  Steps are pipelined over two device buffer sets and three
+    streams (upload, gather, download), so step k+1's upload overlaps step k's download;
+    a buffer set is reused only after the gather that read it and the download that read
+    its output have finished."""
     import torch
-    stream = torch.cuda.current_stream()
     pool_dev = inputs.device_pool(w, dev)
     h_pool = torch.empty(pool_dev.shape, dtype=torch.uint8, pin_memory=True)
     h_pool.copy_(pool_dev)
     del pool_dev
     host_idx = [torch.from_numpy(np.ascontiguousarray(a).view(np.int32).copy()).pin_memory()
                 for a in (w.table, w.seq_ptr, w.lens)]
-    d_pool = torch.empty(h_pool.shape, dtype=torch.uint8, device=dev)
-    d_idx = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_idx]
     T = w.total_tokens
-    h_out = torch.empty(T * w.row_bytes, dtype=torch.uint8, pin_memory=True)
-    d_out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)
-    desc = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[2], num_pages=w.num_pages,
-                        page_size=w.page_size, num_heads=w.num_heads, head_dim=w.head_dim,
-                        dtype=w.dtype, index_type=0)
-    ws = hp.workspace_for(desc, dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sets = []
+    for _ in range(2):
+        d_pool = torch.empty(h_pool.shape, dtype=torch.uint8, device=dev)
+        d_idx = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_idx]
+        desc = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[2], num_pages=w.num_pages,
+                            page_size=w.page_size, num_heads=w.num_heads,
+                            head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+        sets.append(dict(pool=d_pool, idx=d_idx, desc=desc, ws=hp.workspace_for(desc, dev),
+                         status=torch.zeros(1, dtype=torch.int32, device=dev),
+                         out=torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev),
+                         h_out=torch.empty(T * w.row_bytes, dtype=torch.uint8,
+                                           pin_memory=True),
+                         gathered=None, downloaded=None))
+    up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def one():
-        d_pool.copy_(h_pool, non_blocking=True)
-        for d, h in zip(d_idx, host_idx):
-            d.copy_(h, non_blocking=True)
-        rc = hp.hp_gather(desc, d_out, T, ws, status)
+    def one(k):
+        b = sets[k % 2]
+        with torch.cuda.stream(up):
+            if b["gathered"] is not None:
+                up.wait_event(b["gathered"])  # the last gather through this set is done
+            b["pool"].copy_(h_pool, non_blocking=True)
+            for d, h in zip(b["idx"], host_idx):
+                d.copy_(h, non_blocking=True)
+            uploaded = torch.cuda.Event()
+            uploaded.record(up)
+        comp.wait_event(uploaded)
+        if b["downloaded"] is not None:
+            comp.wait_event(b["downloaded"])  # its output buffer has been read back
+        rc = hp.hp_gather(b["desc"], b["out"], T, b["ws"], b["status"], stream=comp)
         assert rc == 0
-        h_out.copy_(d_out, non_blocking=True)
+        b["gathered"] = torch.cuda.Event()
+        b["gathered"].record(comp)
+        down.wait_event(b["gathered"])
+        with torch.cuda.stream(down):
+            b["h_out"].copy_(b["out"], non_blocking=True)
+            b["downloaded"] = torch.cuda.Event()
+            b["downloaded"].record(down)
 
-    one()
+    for k in range(2):
+        one(k)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
+    e0.record(up)
+    for k in range(steps):
+        one(k)
+    main = torch.cuda.current_stream()
+    main.wait_stream(down)
+    e1.record(main)
     torch.cuda.synchronize()
-    assert int(status.item()) == 0
+    assert all(int(b["status"].item()) == 0 for b in sets)
     ms = e0.elapsed_time(e1) / steps
     h2d = h_pool.numel() + sum(h.numel() * h.element_size() for h in host_idx)
-    return ms, h2d, h_out.numel()
+    return ms, h2d, T * w.row_bytes
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -331,15 +356,46 @@ def time_oracle(w, host_pool, oracle_mod, budget_s, max_tokens=None):
     return b / dt / 1e9, dt, T, lens
 
 
+def time_oracle_threads(w, host_pool, oracle_mod, nthreads):
+    """The oracle gather, as it stands, over the whole batch on nthreads host threads:
+    the sequences are cut into nthreads contiguous groups, each gathered by one call
+    through its own sub-descriptor (ctypes releases the GIL during the call)."""
+    from concurrent.futures import ThreadPoolExecutor
+    lens = w.lens.astype(np.int64)
+    cuts = np.linspace(0, w.num_seqs, nthreads + 1).astype(int)
+    descs = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if b <= a:
+            continue
+        sp = (w.seq_ptr[a:b + 1].astype(np.int64) - int(w.seq_ptr[a])).astype(w.index_dtype)
+        table = w.table[int(w.seq_ptr[a]):int(w.seq_ptr[b])]
+        descs.append(oracle_mod.Desc(host_pool, table, sp, lens[a:b].astype(w.index_dtype),
+                                     num_pages=w.num_pages, page_size=w.page_size,
+                                     num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype,
+                                     index_type=0 if w.index_dtype == np.uint32 else 1))
+    outs = [np.zeros((d.total_tokens(), w.row_bytes), dtype=np.uint8) for d in descs]
+    with ThreadPoolExecutor(len(descs)) as ex:
+        list(ex.map(lambda i: descs[i].gather(outs[i]), range(len(descs))))  # page in
+        t0 = time.perf_counter()
+        faults = list(ex.map(lambda i: descs[i].gather(outs[i])[2], range(len(descs))))
+        dt = time.perf_counter() - t0
+    assert all(f == "OK" for f in faults), faults
+    b, _ = gather_bytes(w)
+    return b / dt / 1e9, dt, len(descs)
+
+
 # ----------------------------------------------------------------------------- ops
-def median_ms(fn, stream, n=20, warm=3):
-    """Median of n CUDA-event timings of fn() on `stream`, after `warm` untimed calls."""
+def median_ms(fn, stream, n=20, warm=3, between=None):
+    """Median of n CUDA-event timings of fn() on `stream`, after `warm` untimed calls;
+    `between` (untimed) runs before each timed call, e.g. an L2 scrub."""
     import torch
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     ts = []
     for _ in range(n):
+        if between is not None:
+            between()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -356,7 +412,8 @@ def rate_entry(bytes_, ms, peak, **kw):
 
 def attention_only(scale, dev, hp, inputs, peak, reps):
     """Decode attention alone on the decode-append batch at `scale` ("full": 256 sequences
-    of 1K-32K tokens; "mid": 32 of them, about 2.5 GB on the device, the profiler's case)."""
+    of 1K-32K tokens; "mid": 32 of them, about 2.5 GB on the device, the profiler's case;
+    "short": 2048 sequences of 16-1024 tokens)."""
     import torch
     w = inputs.config("decode_append", scale)
     pool = inputs.device_pool(w, dev)
@@ -404,8 +461,14 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     out = {}
     stream = torch.cuda.current_stream()
 
-    def med_ms(fn, n=reps, warm=3):
-        return median_ms(fn, stream, n, warm)
+    def med_ms(fn, n=reps, warm=3, between=None):
+        return median_ms(fn, stream, n, warm, between)
+
+    # L2-cold timings write a 256 MB buffer (twice the 129 MB L2) before each timed call
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def cold():
+        scrub.fill_(1)
 
     def step_us(fn, n=300):
         """Steps issued back to back, as a decode loop issues them: (issue-bound) time
@@ -452,6 +515,8 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     st = GatherStep(w, dev, hp, inputs)
     # stream=None: the binding uses torch's current stream, the capture stream inside a graph
     out["tiny_prefix_gather"] = step_us(lambda: (st.plan(None), st.copy(None)))
+    out["tiny_prefix_gather"]["us_per_step_l2_cold"] = round(
+        1e3 * med_ms(lambda: (st.plan(stream), st.copy(stream)), between=cold), 2)
     st.check_status()
     del st
 
@@ -463,6 +528,9 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     ms = med_ms(lambda: st.copy(stream))
     out["prefix_sharing_gather"] = entry(b, ms, note="logical bytes; the 128 shared pages are "
                                          "read from L2 after their first use")
+    ms = med_ms(lambda: st.copy(stream), between=cold)
+    out["prefix_sharing_gather_l2_cold"] = entry(
+        b, ms, note="logical bytes, L2 scrubbed (256 MB write) before each call")
     st.check_status()
     del st
 
@@ -593,7 +661,7 @@ def main():
                     choices=["decode_gather", "decode_append", "prefix_sharing", "quantized_pool",
                              "quantized_pool_mid"],
                     help="batch the timed steps gather (default: the decode-sized gather)")
-    ap.add_argument("--attention", choices=["full", "mid"],
+    ap.add_argument("--attention", choices=["full", "mid", "short"],
                     help="time only hp_attention_decode on the decode-append batch at this "
                          "scale (warm-up calls, then --steps timed calls) and print its line")
     args = ap.parse_args()
@@ -722,19 +790,27 @@ def main():
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_e2e and args.workload == "decode_gather":
-        ms, h2d, d2h = e2e_gather(w, dev, hp, inputs, steps=5)
+        ms, h2d, d2h = e2e_gather(w, dev, hp, inputs, steps=8)
         result["e2e"] = {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "ms_per_step": round(ms, 3)}
+                         "ms_per_step": round(ms, 3),
+                         "note": "pinned host buffers; uploads, gathers and downloads "
+                                 "pipelined over two buffer sets"}
     if rank == 0 and world == 1 and not args.no_cpu and w.scales_seed is None:
         import oracle
         oracle.build()
         host_pool = step.pool.cpu().numpy()
         gbps, dt, Ts, lens = time_oracle(w, host_pool, oracle, budget_s=12.0)
-        result["cpu_baseline"] = {"value": round(gbps, 3), "unit": UNIT, "cores": 1,
-                                  "kind": "oracle",
-                                  "sample": "oracle gather (one thread) of the first %d of %d "
-                                            "tokens, %.1f s" % (Ts, T, dt)}
+        nthr = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                   else (os.cpu_count() or 1))
+        gbps_mt, dt_mt, used = time_oracle_threads(w, host_pool, oracle, nthr)
+        result["cpu_baseline"] = {
+            "value": round(gbps_mt, 3), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": "oracle gather of the whole batch (%d tokens) on %d threads, one "
+                      "contiguous group of sequences each, %.2f s" % (T, used, dt_mt),
+            "single_thread": {"value": round(gbps, 3), "cores": 1,
+                              "sample": "oracle gather (one thread) of the first %d of %d "
+                                        "tokens, %.1f s" % (Ts, T, dt)}}
     if rank == 0 and world == 1 and not args.no_ops:
         del step
         torch.cuda.empty_cache()

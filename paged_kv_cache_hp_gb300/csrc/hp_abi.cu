@@ -567,13 +567,32 @@ HP_API int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t wo
 
 namespace {
 
+// Pages per attention work chunk: the largest power of two in [HP_ATTN_MIN_CHUNK_PAGES,
+// HP_ATTN_CHUNK_PAGES] that still cuts the batch into at least kAttnItems (chunk, K/V head)
+// items, so a small batch still spreads over every warp slot of the GPU (152 SMs x 16
+// warps, about 3 items each); table_len stands in for the pages the sequences use.
+#ifndef HP_ATTN_TARGET_ITEMS
+#define HP_ATTN_TARGET_ITEMS 8192
+#endif
+constexpr u64 kAttnItems = HP_ATTN_TARGET_ITEMS;
+u64 attn_chunk_pages(const hp_paged_desc* d)
+{
+    u64 cp = HP_ATTN_CHUNK_PAGES;
+    while (cp > HP_ATTN_MIN_CHUNK_PAGES && (u128)(d->table_len / cp) * d->num_heads < kAttnItems)
+        cp >>= 1;
+    return cp;
+}
+
+// Chunks a batch can have: a sequence of need_s <= slice_s pages has
+// ceil(need_s / cp) <= slice_s / cp + 1 of them.
+u64 attn_max_chunks(const hp_paged_desc* d) { return d->table_len / attn_chunk_pages(d) + d->num_seqs + 1; }
+
 int attention_ws(const hp_paged_desc* d, uint32_t hq, u64* bytes)
 {
     u64 plan = 0;
     int rc = ws_bytes(d, &plan);
     if (rc) return rc;
-    const u128 chunks = (u128)(d->table_len / HP_ATTN_CHUNK_PAGES) + d->num_seqs + 1;
-    const u128 part = chunks * hq * (d->head_dim + 2) * 4;
+    const u128 part = (u128)attn_max_chunks(d) * hq * (d->head_dim + 2) * 4;
     if ((part + plan) >> 64) return HP_ERR_OVERFLOW;
     *bytes = plan + (u64)part;
     return HP_OK;
@@ -611,7 +630,7 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     u64 plan_bytes = 0;
     ws_bytes(d, &plan_bytes);
     hp::PlanArgs pa = plan_args(d, workspace, d_status);
-    pa.chunk_pages = HP_ATTN_CHUNK_PAGES;
+    pa.chunk_pages = attn_chunk_pages(d);
     rc = hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
     if (rc || d->num_seqs == 0) return rc;
     hp::AttnArgs a{};
@@ -630,11 +649,12 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     a.D = (uint32_t)d->head_dim;
     a.G = (uint32_t)G;
     hp::invariant_divisor(d->page_size, &a.p_m, &a.p_l);
-    a.chunk_pages = HP_ATTN_CHUNK_PAGES;
+    a.chunk_pages = pa.chunk_pages;
     a.scale = scale;
     a.hdr = pa.ws.hdr;
     a.units_off = pa.ws.units_off;
-    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes);
+    a.part_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes);
+    a.part_ml = a.part_acc + attn_max_chunks(d) * num_q_heads * d->head_dim;
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
     a.d_status = d_status;

@@ -9,18 +9,21 @@
 //
 // Decode attention reads every key and value once for about 2G flops per byte, so it is
 // bound by HBM, not by arithmetic: it runs on the CUDA cores.
-//   attn_kernel     every warp runs its own (chunk of chunk_pages pages, K/V head) items.
-//                   It streams the chunk's rows of that head into a ring of kStages
-//                   shared-memory stages with cp.async (a step's K rows, then its V rows;
-//                   the page of each token comes from the chunk's page IDs, held one per
-//                   lane), so the loads of the next steps are in flight while it computes.
-//                   Lane l owns dims [l*E, l*E+E) (E = D/32).  A step is TS tokens: their
-//                   (token, query head) partial dot products are summed across the warp with
-//                   a transposed butterfly (one shuffle per product), then an online softmax
-//                   per query head updates the running max, sum and the lane's E dims of the
-//                   weighted value sum.  Each item leaves (max, sum, acc[D]) per query head
-//                   in the workspace.
+//   attn_kernel     works on (chunk of chunk_pages pages, K/V head) items: a CTA owns a
+//                   contiguous range of them and its eight warps take every eighth, so
+//                   they read the heads of one chunk together.  A warp streams its item's
+//                   rows into a ring of kStages shared-memory stages with cp.async (a
+//                   step's K rows, then its V rows; the page of each token comes from the
+//                   chunk's page IDs, held one per lane), so the loads of the next steps
+//                   are in flight while it computes.  Lane l owns dims [l*E, l*E+E)
+//                   (E = D/32).  A step is TS tokens: their (token, query head) partial
+//                   dot products are summed across the warp with a transposed butterfly
+//                   (one shuffle per product), then an online softmax per query head
+//                   updates the running max, sum and the lane's E dims of the weighted
+//                   value sum.  Each item leaves (max, sum, acc[D]) per query head in the
+//                   workspace.
 //   combine_kernel  one warp per (sequence, query head) merges its chunks' partials.
+// Partials: acc [chunks, Hq, D] and (max, sum) [chunks, Hq] in the workspace after the plan.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,6 +42,12 @@ template <int E> struct Pack;
 template <> struct Pack<2> { using T = unsigned int; };
 template <> struct Pack<4> { using T = uint2; };
 template <> struct Pack<8> { using T = uint4; };
+
+template <int EV> struct FVec;
+template <> struct FVec<2> { using T = float2; };
+template <> struct FVec<4> { using T = float4; };
+struct __align__(16) Float8 { float4 lo, hi; };
+template <> struct FVec<8> { using T = Float8; };
 
 // Geometry of one step for G query heads per K/V head and E = D/32 dims per lane.
 template <int G, int E> struct Step {
@@ -149,8 +158,10 @@ __device__ __forceinline__ void issue_step(const AttnArgs& a, unsigned char* sta
     }
 }
 
+// G = 8 query heads at D >= 128 keep 64 to 128 fp32 query and accumulator values per
+// lane: those variants run one CTA per SM with the registers they need instead of spilling.
 template <typename IndexT, bool BF16, int G, int E>
-__global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_kernel(const AttnArgs a)
 {
     using S = Step<G, E>;
     constexpr int TS = S::TS, NP = S::NP, R = S::R;
@@ -161,12 +172,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
     const unsigned warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* ring = smem + warp * S::WARP_SMEM;
     f2* wbuf = reinterpret_cast<f2*>(ring + kStages * S::STAGE);
-    const uint64_t items = a.hdr->total_units * a.Hkv;  // (chunk, K/V head) pairs
-    const IndexT* table = static_cast<const IndexT*>(a.table);
-    const IndexT* sp = static_cast<const IndexT*>(a.seq_ptr);
-    const IndexT* lens = static_cast<const IndexT*>(a.lens);
     const unsigned short* Q = static_cast<const unsigned short*>(a.q);
-    const uint64_t P = a.page_size, D = a.D;
+    const uint64_t D = a.D;
     // After the reduction lane l holds slot lx = l / R: token lx / G, head lx % G of the
     // step.  Before it, lane l keeps slot k ^ lx at array position k, so every level of
     // the transposed butterfly keeps the low half and sends the high half: position k
@@ -178,18 +185,33 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
     for (int i = 0; i < TS; ++i) roff[i] = (i ^ lt) * S::ROW + lane * (2 * E);
     const float qscale = a.scale * 1.4426950408889634f;  // scores in log2 units
 
-    // every warp runs its own items: no barrier across the CTA
-    for (uint64_t it = (uint64_t)blockIdx.x * kWarps + warp; it < items;
-         it += (uint64_t)gridDim.x * kWarps) {
+    // CTA b owns the contiguous range [it_lo, it_hi) of the (chunk, K/V head) items, head-
+    // major within a chunk; warp w takes items it_lo + w, it_lo + w + kWarps, ...  So the
+    // eight warps read the eight heads of one chunk together (whole 8-head runs of every
+    // token row), and a warp's next item is usually the next chunk: its sequence is found
+    // by walking forward from the last one (a binary search only for the first item).
+    const uint64_t items = a.hdr->total_units * a.Hkv;
+    const uint64_t it_lo = (uint64_t)((unsigned __int128)items * blockIdx.x / gridDim.x) + warp;
+    const uint64_t it_hi = (uint64_t)((unsigned __int128)items * (blockIdx.x + 1) / gridDim.x);
+    const IndexT* table = static_cast<const IndexT*>(a.table);
+    const IndexT* spp = static_cast<const IndexT*>(a.seq_ptr);
+    const IndexT* lensp = static_cast<const IndexT*>(a.lens);
+    const uint64_t P = a.page_size;
+    f2 qp[G][E / 2];   // position h holds query head h ^ lh, scaled
+    float m[G], l[G];
+    f2 acc[G][E / 2];  // the lane's dims of each head's weighted value sum
+    uint64_t s = it_lo < it_hi ? find_seq(a.units_off, a.num_seqs, it_lo / a.Hkv) : 0;
+    for (uint64_t it = it_lo; it < it_hi; it += kWarps) {
         const uint64_t u = it / a.Hkv;
         const uint32_t g = (uint32_t)(it - u * a.Hkv);
-        const uint64_t s = find_seq(a.units_off, a.num_seqs, u);
+        while (a.units_off[s + 1] <= u) ++s;  // skips sequences without chunks
         const uint64_t c = u - a.units_off[s];
         const uint64_t t_begin = c * a.chunk_pages * P;
-        const uint32_t n_tok = (uint32_t)(umin(lens[s], t_begin + a.chunk_pages * P) - t_begin);
+        const uint32_t n_tok = (uint32_t)(umin(lensp[s], t_begin + a.chunk_pages * P) - t_begin);
         const uint64_t n_pg = (n_tok + P - 1) / P;
         // the chunk's page IDs, one per lane (a chunk has at most 32 pages)
-        const IndexT my_page = lane < n_pg ? table[(uint64_t)sp[s] + c * a.chunk_pages + lane] : IndexT(0);
+        const IndexT my_page =
+            lane < n_pg ? table[(uint64_t)spp[s] + c * a.chunk_pages + lane] : IndexT(0);
         const uint32_t steps = (n_tok + TS - 1) / TS;
 #pragma unroll
         for (int k = 0; k < kStages - 1; ++k) {
@@ -197,24 +219,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
                 issue_step<IndexT, G, E>(a, ring + k * S::STAGE, k * TS, n_tok, my_page, g, lane);
             cp_async_commit();
         }
-
-        f2 qp[G][E / 2];  // position h holds query head h ^ lh, scaled
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+        for (int hh = 0; hh < G; ++hh) {
             const RowT raw = __ldg(reinterpret_cast<const RowT*>(
-                Q + ((s * a.Hq + (uint64_t)g * G + (h ^ lh)) * D + lane * E)));
-            widen_row<BF16, E>(raw, qp[h]);
+                Q + ((s * a.Hq + (uint64_t)g * G + (hh ^ lh)) * D + lane * E)));
+            widen_row<BF16, E>(raw, qp[hh]);
 #pragma unroll
-            for (int e = 0; e < E / 2; ++e) qp[h][e] = mul2(qp[h][e], pack2(qscale, qscale));
-        }
-        float m[G], l[G];
-        f2 acc[G][E / 2];  // the lane's dims of each head's weighted value sum
+            for (int e = 0; e < E / 2; ++e) qp[hh][e] = mul2(qp[hh][e], pack2(qscale, qscale));
+            m[hh] = -INFINITY;
+            l[hh] = 0.0f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < E / 2; ++e) acc[h][e] = 0ull;
+            for (int e = 0; e < E / 2; ++e) acc[hh][e] = 0ull;
         }
 
         for (uint32_t k = 0; k < steps; ++k) {
@@ -233,15 +248,16 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
                 f2 kv[E / 2];
                 widen_row<BF16, E>(*reinterpret_cast<const RowT*>(st + roff[i]), kv);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    f2 d = mul2(qp[h][0], kv[0]);
+                for (int hh = 0; hh < G; ++hh) {
+                    f2 d = mul2(qp[hh][0], kv[0]);
 #pragma unroll
-                    for (int e = 1; e < E / 2; ++e) d = fma2(qp[h][e], kv[e], d);
+                    for (int e = 1; e < E / 2; ++e) d = fma2(qp[hh][e], kv[e], d);
                     float d0, d1;
                     unpack2(d, d0, d1);
-                    part[i * G + h] = d0 + d1;
+                    part[i * G + hh] = d0 + d1;
                 }
             }
+            // transposed butterfly: every level keeps the low half and sends the high half
 #pragma unroll
             for (int o = 16, n = NP; n > 1; o >>= 1, n >>= 1) {
 #pragma unroll
@@ -257,10 +273,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
             for (int o = R * G; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
             float mnew[G], corr[G], my_m = 0.0f;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                mnew[h] = fmaxf(m[h], __shfl_sync(0xffffffffu, bm, h * R));
-                corr[h] = exp2_approx(m[h] - mnew[h]);  // 0 on the first step (m = -inf)
-                if ((int)my_head == h) my_m = mnew[h];
+            for (int hh = 0; hh < G; ++hh) {
+                mnew[hh] = fmaxf(m[hh], __shfl_sync(0xffffffffu, bm, hh * R));
+                corr[hh] = exp2_approx(m[hh] - mnew[hh]);  // 0 on the first step (m = -inf)
+                if ((int)my_head == hh) my_m = mnew[hh];
             }
             const float p = exp2_approx(sc - my_m);  // 0 for tokens past the chunk
             if (lane % R == 0) wbuf[lx] = pack2(p, p);
@@ -268,12 +284,12 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
 #pragma unroll
             for (int o = R * G; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                l[h] = l[h] * corr[h] + __shfl_sync(0xffffffffu, ps, h * R);
-                m[h] = mnew[h];
-                const f2 c2 = pack2(corr[h], corr[h]);
+            for (int hh = 0; hh < G; ++hh) {
+                l[hh] = l[hh] * corr[hh] + __shfl_sync(0xffffffffu, ps, hh * R);
+                m[hh] = mnew[hh];
+                const f2 c2 = pack2(corr[hh], corr[hh]);
 #pragma unroll
-                for (int e = 0; e < E / 2; ++e) acc[h][e] = mul2(acc[h][e], c2);
+                for (int e = 0; e < E / 2; ++e) acc[hh][e] = mul2(acc[hh][e], c2);
             }
             __syncwarp();  // the weights are in wbuf
 #pragma unroll
@@ -282,61 +298,90 @@ __global__ void __launch_bounds__(kThreads, 2) attn_kernel(const AttnArgs a)
                 widen_row<BF16, E>(
                     *reinterpret_cast<const RowT*>(st + (TS + i) * S::ROW + lane * (2 * E)), vv);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const f2 w = wbuf[i * G + h];
+                for (int hh = 0; hh < G; ++hh) {
+                    const f2 w = wbuf[i * G + hh];
 #pragma unroll
-                    for (int e = 0; e < E / 2; ++e) acc[h][e] = fma2(w, vv[e], acc[h][e]);
+                    for (int e = 0; e < E / 2; ++e) acc[hh][e] = fma2(w, vv[e], acc[hh][e]);
                 }
             }
             __syncwarp();  // the stage and wbuf are rewritten by later steps
         }
-        float* out = a.partials + (u * a.Hq + (uint64_t)g * G) * (D + 2);
+        // the item's partial result
+        const uint64_t row0 = u * a.Hq + (uint64_t)g * G;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float* o = out + h * (D + 2);
-            if (lane == 0) {
-                o[0] = m[h];
-                o[1] = l[h];
-            }
+        for (int hh = 0; hh < G; ++hh) {
+            if (lane == 0)
+                reinterpret_cast<float2*>(a.part_ml)[row0 + hh] = make_float2(m[hh], l[hh]);
+            f2* o = reinterpret_cast<f2*>(a.part_acc + (row0 + hh) * D + lane * E);
 #pragma unroll
-            for (int e = 0; e < E / 2; ++e) {
-                float v0, v1;
-                unpack2(acc[h][e], v0, v1);
-                o[2 + lane * E + 2 * e] = v0;
-                o[3 + lane * E + 2 * e] = v1;
-            }
+            for (int e = 0; e < E / 2; ++e) o[e] = acc[hh][e];
         }
     }
 }
 
-// One warp per (sequence, query head): merge the chunks' (max, sum, acc) partials.
+// One warp per (sequence, query head) merges its chunks' partials: the maximum and the
+// rescaled sum over the chunks with the lanes striding the chunks, then the weighted
+// accumulators with each lane owning EV = D/32 dims (vector loads, four chunks in flight).
+template <int EV>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a)
 {
+    using VT = typename FVec<EV>::T;  // EV floats
     pdl_wait();
     if (a.hdr->verdict != kVerdictOk) return;
     const unsigned lane = threadIdx.x & 31;
     const uint64_t pairs = a.num_seqs * a.Hq, D = a.D;
     const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
     for (uint64_t w = (uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < pairs;
          w += warps) {
         const uint64_t s = w / a.Hq, qh = w - s * a.Hq;
         const uint64_t c0 = a.units_off[s], c1 = a.units_off[s + 1];
-        float* out = a.out + w * D;
-        float M = -INFINITY;
-        for (uint64_t c = c0; c < c1; ++c) M = fmaxf(M, a.partials[(c * a.Hq + qh) * (D + 2)]);
-        float L = 0.0f;
-        for (uint64_t c = c0; c < c1; ++c) {
-            const float* pc = a.partials + (c * a.Hq + qh) * (D + 2);
-            L += pc[1] * exp2f(pc[0] - M);
-        }
-        for (uint64_t d = lane; d < D; d += 32) {
-            float acc = 0.0f;
-            for (uint64_t c = c0; c < c1; ++c) {
-                const float* pc = a.partials + (c * a.Hq + qh) * (D + 2);
-                acc = fmaf(pc[2 + d], exp2f(pc[0] - M), acc);
+        float acc[EV];
+#pragma unroll
+        for (int e = 0; e < EV; ++e) acc[e] = 0.0f;
+        if (c1 > c0) {
+            float M = -INFINITY;
+            for (uint64_t c = c0 + lane; c < c1; c += 32) M = fmaxf(M, ml[c * a.Hq + qh].x);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float L = 0.0f;
+            for (uint64_t c = c0 + lane; c < c1; c += 32) {
+                const float2 v = ml[c * a.Hq + qh];
+                L += v.y * exp2f(v.x - M);
             }
-            out[d] = c1 > c0 ? acc / L : 0.0f;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            const float inv = 1.0f / L;
+            uint64_t c = c0;
+            for (; c + 4 <= c1; c += 4) {
+                VT v[4];
+                float wt[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint64_t row = (c + j) * a.Hq + qh;
+                    v[j] = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
+                    wt[j] = ml[row].x;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x = exp2f(wt[j] - M);
+                    const float* f = reinterpret_cast<const float*>(&v[j]);
+#pragma unroll
+                    for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f[e], acc[e]);
+                }
+            }
+            for (; c < c1; ++c) {
+                const uint64_t row = c * a.Hq + qh;
+                const VT v = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
+                const float x = exp2f(ml[row].x - M);
+                const float* f = reinterpret_cast<const float*>(&v);
+#pragma unroll
+                for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < EV; ++e) acc[e] *= inv;
         }
+        *reinterpret_cast<VT*>(a.out + w * D + lane * EV) = *reinterpret_cast<const VT*>(acc);
     }
 }
 
@@ -356,7 +401,8 @@ int launch_g(const AttnArgs& a, cudaStream_t st)
     uint64_t g2 = (a.num_seqs * a.Hq + 7) / 8;
     const uint64_t cap = (uint64_t)sms * 8;
     g2 = g2 == 0 ? 1 : (g2 < cap ? g2 : cap);
-    return launch_dependent(combine_kernel, (unsigned)g2, 256, 0, st, a) == cudaSuccess
+    auto comb = E == 2 ? combine_kernel<2> : (E == 4 ? combine_kernel<4> : combine_kernel<8>);
+    return launch_dependent(comb, (unsigned)g2, 256, 0, st, a) == cudaSuccess
                ? HP_OK
                : HP_ERR_CUDA;
 }

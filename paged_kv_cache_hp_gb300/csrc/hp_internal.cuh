@@ -124,7 +124,8 @@ struct AttnArgs {
     float scale;
     const WsHeader* hdr;
     const unsigned long long* units_off;  // chunks per sequence, prefix
-    float* partials;          // [chunks, Hq, D + 2]: m, l, acc
+    float* part_acc;          // [max chunks, Hq, D]: each chunk's weighted value sums
+    float* part_ml;           // [max chunks, Hq, 2]: its score maximum and weight sum
     float* out;               // [num_seqs, Hq, D] fp32
     int elem_bf16;            // element type: bf16 (1) or f16 (0)
     int* d_status;

@@ -11,7 +11,11 @@
 // it is block_size rows of head_dim elements, one per slot, num_kv_heads*head_dim apart.
 // A CTA stages whole units (up to 32 KiB of them at a time) in shared memory, so both the
 // global reads and the global writes are contiguous vector accesses; only the
-// shared-memory side is permuted.
+// shared-memory side is permuted.  When an x-chunk is one 16-byte vector and block_size
+// is a multiple of 8, chunk (dx, t) of a unit sits at position dx*bs + (t ^ (dx & 7)):
+// eight lanes reading one slot's row (dx = 0..7, same t) and eight lanes reading
+// consecutive slots of one chunk row (same dx) then both touch eight different 16-byte
+// bank groups, where the plain order puts the first eight on one.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -42,20 +46,32 @@ struct TransposeArgs {
     uint32_t cb_m, cb_l;     // divide by cb
     uint32_t nv, nv_m, nv_l; // VEC-vectors per unit, divide by nv
     uint32_t per_tile;       // units staged together (their bytes fit the tile)
+    uint32_t bs_m, bs_l;     // divide by bs (swizzled layout)
 };
 
 // Offset in a staged unit ([D/x, bs, x] order) of byte `byte` of slot t's row.
+template <bool SWZ>
 __device__ __forceinline__ uint32_t tile_offset(const TransposeArgs& a, uint32_t t, uint32_t byte)
 {
     const uint32_t dx = div_invariant(byte, a.cb_m, a.cb_l);  // which x-chunk
+    if (SWZ) return (dx * a.bs + (t ^ (dx & 7))) * 16;       // cb == 16: byte is dx * 16
     return (dx * a.bs + t) * a.cb + (byte - dx * a.cb);
+}
+
+// Offset in a staged unit of its linear 16-byte chunk p (= dx * bs + t).
+template <bool SWZ>
+__device__ __forceinline__ uint32_t linear_offset(const TransposeArgs& a, uint32_t p)
+{
+    if (!SWZ) return p * 16;
+    return (p ^ (div_invariant(p, a.bs_m, a.bs_l) & 7)) * 16;
 }
 
 // Up to per_tile consecutive units are staged at once (up to 32 KiB), so each thread has
 // several vector loads in flight before the CTA synchronises.
-template <int VEC, bool TO_INTERCHANGE>
+template <int VEC, bool TO_INTERCHANGE, bool SWZ>
 __global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs a)
 {
+    static_assert(!SWZ || VEC == 16, "the swizzled layout moves 16-byte chunks");
     using T = typename VecT<VEC>::T;
     extern __shared__ __align__(16) unsigned char tile[];
     const uint32_t U = a.bs * a.rowb;  // bytes of a unit
@@ -67,8 +83,14 @@ __global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs
         if (TO_INTERCHANGE) {
             // internal units u0.. are contiguous: one linear load
             const T* in = reinterpret_cast<const T*>(a.src + u0 * U);
-            for (uint32_t i = threadIdx.x; i < n; i += kThreads)
-                reinterpret_cast<T*>(tile)[i] = __ldg(in + i);
+            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+                if (SWZ) {
+                    const uint32_t k = div_invariant(i, a.nv_m, a.nv_l);
+                    *reinterpret_cast<T*>(tile + k * U + linear_offset<true>(a, i - k * a.nv)) = __ldg(in + i);
+                } else {
+                    reinterpret_cast<T*>(tile)[i] = __ldg(in + i);
+                }
+            }
             __syncthreads();
             for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
                 const uint32_t k = div_invariant(i, a.nv_m, a.nv_l), iv = i - k * a.nv;
@@ -76,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs
                 const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
                 const uint32_t byte = (iv - t * a.vpr) * VEC;
                 *reinterpret_cast<T*>(a.dst + (b * a.bs * a.H + h) * a.rowb + t * row_stride + byte) =
-                    *reinterpret_cast<const T*>(tile + k * U + tile_offset(a, t, byte));
+                    *reinterpret_cast<const T*>(tile + k * U + tile_offset<SWZ>(a, t, byte));
             }
         } else {
             for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
@@ -84,26 +106,32 @@ __global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs
                 const uint64_t u = u0 + k, b = u / a.H, h = u - b * a.H;
                 const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
                 const uint32_t byte = (iv - t * a.vpr) * VEC;
-                *reinterpret_cast<T*>(tile + k * U + tile_offset(a, t, byte)) = __ldg(
+                *reinterpret_cast<T*>(tile + k * U + tile_offset<SWZ>(a, t, byte)) = __ldg(
                     reinterpret_cast<const T*>(a.src + (b * a.bs * a.H + h) * a.rowb + t * row_stride + byte));
             }
             __syncthreads();
             T* out = reinterpret_cast<T*>(a.dst + u0 * U);
-            for (uint32_t i = threadIdx.x; i < n; i += kThreads)
-                out[i] = reinterpret_cast<const T*>(tile)[i];
+            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
+                if (SWZ) {
+                    const uint32_t k = div_invariant(i, a.nv_m, a.nv_l);
+                    out[i] = *reinterpret_cast<const T*>(tile + k * U + linear_offset<true>(a, i - k * a.nv));
+                } else {
+                    out[i] = reinterpret_cast<const T*>(tile)[i];
+                }
+            }
         }
         __syncthreads();  // the tile is reused by the next units
     }
 }
 
-template <int VEC, bool TO>
+template <int VEC, bool TO, bool SWZ = false>
 int launch_t(const TransposeArgs& a, uint32_t smem, cudaStream_t st)
 {
-    auto kern = transpose_kernel<VEC, TO>;
+    auto kern = transpose_kernel<VEC, TO, SWZ>;
     int dev = 0;
     const int sms = current_sms(&dev);
     if (sms == 0) return HP_ERR_CUDA;
-    const int per_sm = resident_ctas<transpose_kernel<VEC, TO>>(dev, kThreads, smem);
+    const int per_sm = resident_ctas<transpose_kernel<VEC, TO, SWZ>>(dev, kThreads, smem);
     if (per_sm == 0) return HP_ERR_CUDA;
     const uint64_t tiles = (a.units + a.per_tile - 1) / a.per_tile;
     const uint64_t grid = std::min<uint64_t>(tiles, (uint64_t)sms * per_sm);
@@ -143,6 +171,11 @@ int launch_transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint6
     a.per_tile = U >= 32768 ? 1 : 32768 / U;
     const uint32_t smem = a.per_tile * U;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (vec == 16 && a.cb == 16 && bs % 8 == 0) {
+        invariant_divisor(a.bs, &a.bs_m, &a.bs_l);
+        return to_interchange ? launch_t<16, true, true>(a, smem, st)
+                              : launch_t<16, false, true>(a, smem, st);
+    }
 #define HP_TR(v)                                                                        \
     case v:                                                                             \
         return to_interchange ? launch_t<v, true>(a, smem, st) : launch_t<v, false>(a, smem, st);

@@ -303,6 +303,9 @@ def config(name: str, scale: str = "full") -> Workload:
     if name == "decode_append":
         if scale == "mid":  # 32 sequences, about 2.5 GB of K and V pools
             return decode_append(num_pages=40000, num_seqs=32, name="decode_append_mid")
+        if scale == "short":  # 2048 short sequences (16 to 1024 tokens), about 4.4 GB read
+            return decode_append(num_pages=80000, num_seqs=2048, len_lo=16, len_hi=1024,
+                                 name="decode_append_short")
         return decode_append(num_pages=2000, num_seqs=9, len_lo=1, len_hi=2000,
                              name="decode_append_small") if small else decode_append()
     if name == "prefix_sharing":

@@ -156,3 +156,25 @@ def test_lane_host_checks(hpc):
                                             None)) == "HP_ERR_LENGTH"
     assert hpc.status_name(L.hp_lane_gather(pool, table, 1 << 62, 1, 1 << 10, 2, 2, 5, 1, out,
                                             None, None)) == "HP_ERR_LANE_OVERFLOW"
+
+
+@pytest.mark.parametrize("table_len,num_heads,cp", [
+    (273_000, 8, 32), (31_300, 8, 16), (20_000, 8, 16), (8_200, 8, 8), (8_000, 8, 4),
+    (100, 2, 4), (0, 8, 4), (1_000_000, 1, 32), (40_000, 1, 4),
+])
+def test_attention_workspace_follows_the_chunk_rule(hpc, table_len, num_heads, cp):
+    """hp_attention_decode_workspace_bytes = the plan's workspace + fp32 (max, sum, acc[D])
+    for table_len / cp + num_seqs + 1 chunks and every query head, cp the documented chunk
+    size: the largest power of two in [4, 32] with (table_len / cp) * num_heads >= 8192."""
+    W, f = fake_desc(hpc, num_seqs=37, table_len=table_len, num_heads=num_heads, head_dim=128,
+                     num_pages=max(table_len, 1), block_table=0x20000 if table_len else 0)
+    rule = 32
+    while rule > 4 and (table_len // rule) * num_heads < 8192:
+        rule //= 2
+    assert rule == cp
+    plan = ctypes.c_uint64(0)
+    assert hpc.lib().hp_workspace_bytes(W.ref, ctypes.byref(plan)) == 0
+    Hq = 4 * num_heads
+    rc, n = hpc.hp_attention_decode_workspace_bytes(W, Hq)
+    assert rc == 0
+    assert n == plan.value + (table_len // cp + 37 + 1) * Hq * (128 + 2) * 4

@@ -17,6 +17,9 @@ NPDT = {"f16": np.float16, "bf16": np.uint16, "f32": np.float32, "i8": np.int8, 
     (11, 7, 2, 8, 4, "f32"),
     (5, 3, 2, 6, 2, "f64"),
     (64, 32, 2, 256, 8, "f16"),
+    (13, 8, 3, 32, 4, "f32"),     # 16-byte chunks, block_size 8: swizzled staging
+    (7, 24, 2, 64, 8, "bf16"),    # block_size a multiple of 8 but not a power of two
+    (6, 12, 2, 64, 8, "f16"),     # 16-byte chunks, block_size not a multiple of 8: plain
 ])
 def test_transpose_matches_oracle(hp, oracle, nb, bs, H, D, x, dtype):
     import torch
