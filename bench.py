@@ -429,6 +429,20 @@ def attention_only(scale, dev, hp, inputs, peak, reps):
     return res
 
 
+def transpose_only(dev, hp, peak, reps, nb=10000, bsz=16, H=32, D=128, x=8):
+    """Both cache layout conversions on a [nb, bs, H, D] fp16 cache (1.31 GB each way)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    kin = torch.empty(nb * bsz * H * D * 2, dtype=torch.uint8, device=dev)
+    kout = torch.empty_like(kin)
+    res = {"op": "cache_layout_conversions", "shape": [nb, bsz, H, D], "x": x, "dtype": "f16"}
+    ms = median_ms(lambda: hp.hp_from_kernel_layout(kin, kout, nb, bsz, H, D, x, "f16"), stream, reps)
+    res["kernel_layout_to_interchange"] = rate_entry(2 * kin.numel(), ms, peak)
+    ms = median_ms(lambda: hp.hp_to_kernel_layout(kout, kin, nb, bsz, H, D, x, "f16"), stream, reps)
+    res["interchange_to_kernel_layout"] = rate_entry(2 * kin.numel(), ms, peak)
+    return res
+
+
 def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, reps=10):
     """hp_attention_decode over batch w (K pool and descriptor d_k; a V pool of the same
     geometry is drawn here): Hq query heads, bytes = K and V rows once + q + out."""
@@ -664,8 +678,19 @@ def main():
     ap.add_argument("--attention", choices=["full", "mid", "short"],
                     help="time only hp_attention_decode on the decode-append batch at this "
                          "scale (warm-up calls, then --steps timed calls) and print its line")
+    ap.add_argument("--transpose", action="store_true",
+                    help="time only the two cache layout conversions (kernel-internal "
+                         "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
+                         "and print their line")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.transpose:
+        import torch
+        from paged_kv_cache_hp_gb300 import build, hp
+        build.build()
+        hp.lib()
+        print(json.dumps(transpose_only("cuda", hp, peak_hbm()[0], args.steps)))
+        return
     if args.attention:
         import torch
         from paged_kv_cache_hp_gb300 import build, hp, inputs

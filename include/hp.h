@@ -392,7 +392,8 @@ int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const v
  * of dst is element (b, h, d/x, t, d mod x) of src.  hp_to_kernel_layout is the inverse.
  * Elements of `dtype` are copied as bytes; src and dst are device buffers that must not
  * overlap.  x must divide head_dim (HP_ERR_ARG); block_size*head_dim*width must not exceed
- * 48 KiB (one (block, head) unit is staged in shared memory; HP_ERR_ARG beyond).
+ * 48 KiB (one (block, head) unit is staged in shared memory; HP_ERR_ARG beyond), and
+ * num_heads must be below 2^31 (HP_ERR_ARG).
  */
 int hp_from_kernel_layout(const void* src, void* dst, uint64_t num_blocks, uint64_t block_size,
                           uint64_t num_heads, uint64_t head_dim, uint64_t x, uint32_t dtype,

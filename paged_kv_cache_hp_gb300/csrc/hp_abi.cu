@@ -671,6 +671,7 @@ int transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint64_t H, 
     if (!bs || !H || !D || !x) return HP_ERR_ZERO_DIM;
     if (D % x) return HP_ERR_ARG;
     if ((u128)bs * D * es > 48 * 1024) return HP_ERR_ARG;
+    if (H >= (1ull << 31)) return HP_ERR_ARG;  // heads are counted in 32 bits on the device
     const u128 total = (u128)nb * bs * H * D * es;
     if (total >> 64) return HP_ERR_OVERFLOW;
     if (nb == 0) return HP_OK;

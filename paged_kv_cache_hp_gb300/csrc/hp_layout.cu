@@ -47,6 +47,7 @@ struct TransposeArgs {
     uint32_t nv, nv_m, nv_l; // VEC-vectors per unit, divide by nv
     uint32_t per_tile;       // units staged together (their bytes fit the tile)
     uint32_t bs_m, bs_l;     // divide by bs (swizzled layout)
+    uint32_t H_m, H_l;       // divide by H
 };
 
 // Offset in a staged unit ([D/x, bs, x] order) of byte `byte` of slot t's row.
@@ -66,8 +67,29 @@ __device__ __forceinline__ uint32_t linear_offset(const TransposeArgs& a, uint32
     return (p ^ (div_invariant(p, a.bs_m, a.bs_l) & 7)) * 16;
 }
 
-// Up to per_tile consecutive units are staged at once (up to 32 KiB), so each thread has
-// several vector loads in flight before the CTA synchronises.
+// Up to per_tile consecutive units (u = block * H + head) are staged at once (up to
+// 32 KiB); each thread moves its vectors in batches of kBatch, every load of a batch
+// issued before the first use.  The interchange-side address of staged vector i: unit
+// k = i / nv, slot t and byte offset within the slot's row from the rest; the unit's
+// block and head come from the tile's first unit by a 32-bit step (no 64-bit division
+// per vector).
+constexpr int kBatch = 8;
+
+template <int VEC>
+__device__ __forceinline__ uint64_t interchange_offset(const TransposeArgs& a, uint64_t b0,
+                                                       uint32_t h0, uint32_t i, uint32_t& k,
+                                                       uint32_t& t, uint32_t& byte)
+{
+    k = div_invariant(i, a.nv_m, a.nv_l);
+    const uint32_t iv = i - k * a.nv;
+    t = div_invariant(iv, a.vpr_m, a.vpr_l);
+    byte = (iv - t * a.vpr) * VEC;
+    uint32_t h = h0 + k;
+    const uint32_t db = div_invariant(h, a.H_m, a.H_l);
+    h -= db * a.H;
+    return (((b0 + db) * a.bs + t) * a.H + h) * a.rowb + byte;
+}
+
 template <int VEC, bool TO_INTERCHANGE, bool SWZ>
 __global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs a)
 {
@@ -75,48 +97,64 @@ __global__ void __launch_bounds__(kThreads) transpose_kernel(const TransposeArgs
     using T = typename VecT<VEC>::T;
     extern __shared__ __align__(16) unsigned char tile[];
     const uint32_t U = a.bs * a.rowb;  // bytes of a unit
-    const uint64_t row_stride = (uint64_t)a.H * a.rowb;
     for (uint64_t u0 = (uint64_t)blockIdx.x * a.per_tile; u0 < a.units;
          u0 += (uint64_t)gridDim.x * a.per_tile) {
         const uint32_t k_units = (uint32_t)(a.units - u0 < a.per_tile ? a.units - u0 : a.per_tile);
         const uint32_t n = k_units * a.nv;
-        if (TO_INTERCHANGE) {
-            // internal units u0.. are contiguous: one linear load
-            const T* in = reinterpret_cast<const T*>(a.src + u0 * U);
-            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-                if (SWZ) {
-                    const uint32_t k = div_invariant(i, a.nv_m, a.nv_l);
-                    *reinterpret_cast<T*>(tile + k * U + linear_offset<true>(a, i - k * a.nv)) = __ldg(in + i);
-                } else {
-                    reinterpret_cast<T*>(tile)[i] = __ldg(in + i);
+        const uint64_t b0 = u0 / a.H;
+        const uint32_t h0 = (uint32_t)(u0 - b0 * a.H);
+        // phase 1: global -> tile
+        for (uint32_t base = 0; base < n; base += kThreads * kBatch) {
+            T r[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const uint32_t i = base + threadIdx.x + j * kThreads;
+                if (i < n) {
+                    if (TO_INTERCHANGE) {  // internal units u0.. are contiguous
+                        r[j] = __ldg(reinterpret_cast<const T*>(a.src + u0 * U) + i);
+                    } else {
+                        uint32_t k, t, byte;
+                        r[j] = __ldg(reinterpret_cast<const T*>(
+                            a.src + interchange_offset<VEC>(a, b0, h0, i, k, t, byte)));
+                    }
                 }
             }
-            __syncthreads();
-            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-                const uint32_t k = div_invariant(i, a.nv_m, a.nv_l), iv = i - k * a.nv;
-                const uint64_t u = u0 + k, b = u / a.H, h = u - b * a.H;
-                const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
-                const uint32_t byte = (iv - t * a.vpr) * VEC;
-                *reinterpret_cast<T*>(a.dst + (b * a.bs * a.H + h) * a.rowb + t * row_stride + byte) =
-                    *reinterpret_cast<const T*>(tile + k * U + tile_offset<SWZ>(a, t, byte));
-            }
-        } else {
-            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-                const uint32_t k = div_invariant(i, a.nv_m, a.nv_l), iv = i - k * a.nv;
-                const uint64_t u = u0 + k, b = u / a.H, h = u - b * a.H;
-                const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
-                const uint32_t byte = (iv - t * a.vpr) * VEC;
-                *reinterpret_cast<T*>(tile + k * U + tile_offset<SWZ>(a, t, byte)) = __ldg(
-                    reinterpret_cast<const T*>(a.src + (b * a.bs * a.H + h) * a.rowb + t * row_stride + byte));
-            }
-            __syncthreads();
-            T* out = reinterpret_cast<T*>(a.dst + u0 * U);
-            for (uint32_t i = threadIdx.x; i < n; i += kThreads) {
-                if (SWZ) {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const uint32_t i = base + threadIdx.x + j * kThreads;
+                if (i < n) {
                     const uint32_t k = div_invariant(i, a.nv_m, a.nv_l);
-                    out[i] = *reinterpret_cast<const T*>(tile + k * U + linear_offset<true>(a, i - k * a.nv));
-                } else {
-                    out[i] = reinterpret_cast<const T*>(tile)[i];
+                    uint32_t off;
+                    if (TO_INTERCHANGE) {
+                        off = SWZ ? linear_offset<true>(a, i - k * a.nv) : (i - k * a.nv) * VEC;
+                    } else {
+                        const uint32_t iv = i - k * a.nv;
+                        const uint32_t t = div_invariant(iv, a.vpr_m, a.vpr_l);
+                        off = tile_offset<SWZ>(a, t, (iv - t * a.vpr) * VEC);
+                    }
+                    *reinterpret_cast<T*>(tile + k * U + off) = r[j];
+                }
+            }
+        }
+        __syncthreads();
+        // phase 2: tile -> global
+        for (uint32_t base = 0; base < n; base += kThreads * kBatch) {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const uint32_t i = base + threadIdx.x + j * kThreads;
+                if (i < n) {
+                    const uint32_t k = div_invariant(i, a.nv_m, a.nv_l);
+                    if (TO_INTERCHANGE) {
+                        uint32_t kk, t, byte;
+                        const uint64_t g = interchange_offset<VEC>(a, b0, h0, i, kk, t, byte);
+                        *reinterpret_cast<T*>(a.dst + g) =
+                            *reinterpret_cast<const T*>(tile + k * U + tile_offset<SWZ>(a, t, byte));
+                    } else {
+                        const uint32_t off =
+                            SWZ ? linear_offset<true>(a, i - k * a.nv) : (i - k * a.nv) * VEC;
+                        reinterpret_cast<T*>(a.dst + u0 * U)[i] =
+                            *reinterpret_cast<const T*>(tile + k * U + off);
+                    }
                 }
             }
         }
@@ -169,6 +207,7 @@ int launch_transpose(const void* src, void* dst, uint64_t nb, uint64_t bs, uint6
     a.nv = U / vec;
     invariant_divisor(a.nv, &a.nv_m, &a.nv_l);
     a.per_tile = U >= 32768 ? 1 : 32768 / U;
+    invariant_divisor(a.H, &a.H_m, &a.H_l);
     const uint32_t smem = a.per_tile * U;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (vec == 16 && a.cb == 16 && bs % 8 == 0) {
