@@ -200,6 +200,17 @@ __device__ __forceinline__ uint2 ld_stream8(const uint2* p)
 #define HP_DQ_UNROLL 16
 #endif
 constexpr int kDqUnroll = HP_DQ_UNROLL;  // 8-byte loads in flight per thread
+#ifndef HP_DQ_DIM_HOIST
+#define HP_DQ_DIM_HOIST 0
+#endif
+#ifndef HP_DQ_DIM_DIV
+#define HP_DQ_DIM_DIV 2
+#endif
+// Per-head_dim scales and zero points held in registers cost 16 live values per thread
+// (101 registers, 2 CTAs per SM); read per group from L1 instead the kernel keeps 4 CTAs
+// per SM and its loads in flight (0.76 -> 0.83 of the copy bandwidth on a 2.5 GB pool).
+constexpr bool kDqDimHoist = HP_DQ_DIM_HOIST;
+constexpr int kDqDimDiv = HP_DQ_DIM_DIV;       // per-head_dim: kDqUnroll / this in flight
 
 // 8-bit rows -> bfloat16 rows, 8 elements per thread step.  `n8` groups of 8; the row of
 // group v within the unit is v / (row_elems/8) and, for per-channel schemes, its head is
@@ -219,11 +230,11 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
         s_t = __ldg(scales);
         if (kZp) z_t = code_to_f32(__ldg(zps), sgn);
     }
-    // Per channel, when the groups of a row divide the CTA's width (q_fixed) every group a
-    // thread handles sits at the same place in its row, so its 8 scales and zero points
-    // are loaded once here.
+    // Per head, when the groups of a row divide the CTA's width (q_fixed) every group a
+    // thread handles sits at the same place in its row, so its scale and zero point are
+    // loaded once here.
     float sc_f[8], zc_f[8];
-    const bool fixed = (kScheme == kQHead || kScheme == kQDim) && a.q_fixed;
+    const bool fixed = (kScheme == kQHead || (kScheme == kQDim && kDqDimHoist)) && a.q_fixed;
     if (fixed) {
         const uint32_t g = threadIdx.x & (a.q_gpr - 1);
         const uint32_t h = div_invariant(g, a.q_hd_m, a.q_hd_l);
@@ -250,7 +261,8 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
     }
     // per-channel groups keep 16 more values live: half the loads in flight per thread,
     // for more resident CTAs
-    constexpr int kU = kScheme >= kQHead ? kDqUnroll / 2 : kDqUnroll;
+    constexpr int kU = kScheme == kQHead ? kDqUnroll / 2
+                       : kScheme == kQDim ? kDqUnroll / kDqDimDiv : kDqUnroll;
     const uint2* s = reinterpret_cast<const uint2*>(src);
     uint4* d = reinterpret_cast<uint4*>(dst);
     for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kU) {
