@@ -356,7 +356,7 @@ int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace
  * Bytes of device workspace hp_attention_decode needs: the plan's (hp_workspace_bytes)
  * plus fp32 partials for every work chunk and query head.  A chunk is cp consecutive pages
  * of one sequence, cp the largest power of two in [HP_ATTN_MIN_CHUNK_PAGES,
- * HP_ATTN_CHUNK_PAGES] with (table_len / cp) * num_heads >= 8192 (else the minimum), so
+ * HP_ATTN_CHUNK_PAGES] with (table_len / cp) * num_heads >= 4096 (else the minimum), so
  * the size depends only on the descriptor's table_len, num_heads, num_seqs and head_dim.
  */
 #define HP_ATTN_CHUNK_PAGES 32

@@ -159,17 +159,17 @@ def test_lane_host_checks(hpc):
 
 
 @pytest.mark.parametrize("table_len,num_heads,cp", [
-    (273_000, 8, 32), (31_300, 8, 16), (20_000, 8, 16), (8_200, 8, 8), (8_000, 8, 4),
-    (100, 2, 4), (0, 8, 4), (1_000_000, 1, 32), (40_000, 1, 4),
+    (273_000, 8, 32), (31_300, 8, 32), (20_000, 8, 32), (8_200, 8, 16), (4_100, 8, 8),
+    (4_000, 8, 4), (100, 2, 4), (0, 8, 4), (1_000_000, 1, 32), (40_000, 1, 8),
 ])
 def test_attention_workspace_follows_the_chunk_rule(hpc, table_len, num_heads, cp):
     """hp_attention_decode_workspace_bytes = the plan's workspace + fp32 (max, sum, acc[D])
     for table_len / cp + num_seqs + 1 chunks and every query head, cp the documented chunk
-    size: the largest power of two in [4, 32] with (table_len / cp) * num_heads >= 8192."""
+    size: the largest power of two in [4, 32] with (table_len / cp) * num_heads >= 4096."""
     W, f = fake_desc(hpc, num_seqs=37, table_len=table_len, num_heads=num_heads, head_dim=128,
                      num_pages=max(table_len, 1), block_table=0x20000 if table_len else 0)
     rule = 32
-    while rule > 4 and (table_len // rule) * num_heads < 8192:
+    while rule > 4 and (table_len // rule) * num_heads < 4096:
         rule //= 2
     assert rule == cp
     plan = ctypes.c_uint64(0)
