@@ -604,6 +604,13 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     out["decode_append_step"] = dict(
         step_us(lambda: hp.hp_scatter_append(d_app, new, new_ptr, w.total_new, ws, status)),
         rows=w.total_new, bytes=2 * w.total_new * w.row_bytes)
+    # the same step with HP_PERMISSIVE (the caller vouches for the descriptor): one kernel,
+    # one warp per sequence, no plan and no block-table check
+    d_app_p = hp.PagedDesc(pool, table, sp, before, flags=1, **kw)
+    out["decode_append_step_permissive"] = dict(
+        step_us(lambda: hp.hp_scatter_append(d_app_p, new, new_ptr, w.total_new, ws, status)),
+        rows=w.total_new, bytes=2 * w.total_new * w.row_bytes)
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
     d_g = hp.PagedDesc(pool, table, sp, after, **kw)
     T = w.total_tokens
     o = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)

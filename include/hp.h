@@ -297,7 +297,11 @@ int hp_gather_dequant_q_planned(const hp_paged_desc* desc, const hp_quant_desc* 
  * new_ptr[num_seqs] = total_new, then seq_lens[s] + rows of s <= the slice's
  * slots.  Rows whose targets alias (two sequences naming one page and slot)
  * land in an unspecified order.  `new_rows` must be 16-byte aligned for the
- * vector path.
+ * vector path.  With HP_PERMISSIVE the caller vouches for the descriptor: nothing is
+ * validated up front, a row whose logical page lies outside its slice or the table is
+ * skipped with HP_ERR_LEN in *d_status, one naming a page outside the pool with
+ * HP_ERR_PAGE_ID.  An append of fewer than num_seqs*page_size rows (a decode step)
+ * runs as one kernel with one warp per sequence (after the plan when validated).
  */
 int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, const void* new_ptr,
                       uint64_t total_new, void* workspace, uint64_t workspace_bytes,

@@ -278,8 +278,15 @@ int append_planned(const hp_paged_desc* d, const void* new_rows, const void* new
     if (!new_ptr) return HP_ERR_NULL;
     hp::CopyArgs a = copy_args(d, ws, d_status);
     a.new_ptr = new_ptr;
-    // a unit is at most one page of rows, and on average total_new / num_seqs rows: a
-    // decode step's single rows take the low-latency register path
+    if ((u128)total_new < (u128)d->num_seqs * d->page_size) {
+        // decode-sized: one warp per sequence after the plan's verdict, no unit search
+        a.src = static_cast<const char*>(new_rows);
+        a.dst = static_cast<char*>(const_cast<void*>(d->page_pool));
+        if (!a.src) a.src = reinterpret_cast<const char*>(d->page_pool);  // never read
+        return hp::launch_append_rows(d->index_type == HP_IDX_U64, a,
+                                      pick_vec(a.row_bytes, a.src, d->page_pool), stream);
+    }
+    // a unit is at most one page of rows, and on average total_new / num_seqs rows
     const u64 avg_rows = total_new / d->num_seqs + (total_new % d->num_seqs != 0);
     if (avg_rows < d->page_size) a.unit_bytes = avg_rows * a.row_bytes;
     a.src = static_cast<const char*>(new_rows);
@@ -487,6 +494,25 @@ HP_API int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, co
     int rc = check_desc(desc);
     if (rc) return rc;
     if (total_new && !new_rows) return HP_ERR_NULL;
+    if ((desc->flags & HP_PERMISSIVE) && desc->num_seqs &&
+        (u128)total_new < (u128)desc->num_seqs * desc->page_size) {
+        // decode-sized and vouched for: one warp per sequence, no plan, no table check
+        rc = check_ws(desc, workspace, workspace_bytes);
+        if (rc) return rc;
+        if (!new_ptr) return HP_ERR_NULL;
+        if (misaligned(new_ptr, desc->index_type == HP_IDX_U64 ? 8 : 4)) return HP_ERR_ALIGN;
+        if ((u128)total_new * row_bytes_of(desc) >> 64) return HP_ERR_OVERFLOW;
+        rc = reset_status(d_status, stream);
+        if (rc) return rc;
+        hp::CopyArgs a = copy_args(desc, workspace, d_status);
+        a.hdr = nullptr;  // no plan to wait for
+        a.new_ptr = new_ptr;
+        a.src = static_cast<const char*>(new_rows);
+        a.dst = static_cast<char*>(const_cast<void*>(desc->page_pool));
+        if (!a.src) a.src = reinterpret_cast<const char*>(desc->page_pool);  // never read
+        return hp::launch_append_rows(desc->index_type == HP_IDX_U64, a,
+                                      pick_vec(a.row_bytes, a.src, desc->page_pool), stream);
+    }
     rc = plan_append(desc, new_ptr, total_new, workspace, workspace_bytes, d_status, stream);
     if (rc) return rc;
     return append_planned(desc, new_rows, new_ptr, total_new, workspace, d_status, stream);

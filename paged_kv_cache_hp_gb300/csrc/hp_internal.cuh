@@ -208,6 +208,9 @@ struct CopyArgs {
 
 int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* stream);
 
+// The permissive decode-step append (hp_writer.cu): one warp per sequence, no plan.
+int launch_append_rows(int index_u64, const CopyArgs& a, int vec, void* stream);
+
 // The TMA bulk engine (hp_bulk.cu): pure copies whose rows and bases are 16-byte aligned.
 // big_stages selects 32 KiB ring stages (else 8 KiB).
 int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, int big_stages, void* stream);

@@ -11,9 +11,22 @@
 //   zero_kernel  one warp per entry: the first entry naming a page claims it (bit 31 of
 //                its count) and zeroes the page's slots from that count to the end.
 // Pages no slice names are never touched.
+//
+// The decode-step append ("Block-Paged Layout -- Hurray Format Specification", Element
+// Lookup used as a store: row i of sequence s goes to token len_s + i), for appends of
+// less than a page per sequence on average:
+//   append_rows_kernel  one warp per sequence, no unit search (after the plan's verdict
+//                when the descriptor is validated, with no plan at all when it is
+//                permissive): its new rows are
+//                rows new_ptr[s] .. new_ptr[s+1] of the input and token len_s + i lives in
+//                slot (len_s + i) mod P of page block_table[seq_ptr[s] + (len_s + i) / P].
+//                The row loads go out together with the block-table lookup.  A row whose
+//                logical page lies outside the slice or the table is skipped with
+//                HP_ERR_LEN, one naming a page outside the pool with HP_ERR_PAGE_ID.
 #include <cuda_runtime.h>
 
 #include "hp_internal.cuh"
+#include "hp_resolve.cuh"
 
 namespace hp {
 namespace {
@@ -75,6 +88,93 @@ __global__ void __launch_bounds__(256) zero_kernel(const PlanArgs a, unsigned* l
     }
 }
 
+template <int VEC> struct VecOf;
+template <> struct VecOf<16> { using T = uint4; };
+template <> struct VecOf<8> { using T = uint2; };
+template <> struct VecOf<4> { using T = unsigned int; };
+template <> struct VecOf<2> { using T = unsigned short; };
+template <> struct VecOf<1> { using T = unsigned char; };
+
+template <typename IndexT, int VEC>
+__global__ void __launch_bounds__(256) append_rows_kernel(const CopyArgs a)
+{
+    using T = typename VecOf<VEC>::T;
+    constexpr int kHeld = 4;  // vectors per lane held for one row (rows up to 2 KiB at VEC 16)
+    const IndexT* np = static_cast<const IndexT*>(a.new_ptr);
+    const IndexT* lens = static_cast<const IndexT*>(a.lens);
+    const IndexT* sp = static_cast<const IndexT*>(a.seq_ptr);
+    const IndexT* table = static_cast<const IndexT*>(a.table);
+    const unsigned lane = threadIdx.x & 31;
+    if (a.hdr) {  // after a plan: wait for its verdict, write nothing unless it is OK
+        pdl_wait();
+        if (a.hdr->verdict != kVerdictOk) return;
+    }
+    const uint64_t P = a.page_size, nv = a.row_bytes / VEC;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
+    for (uint64_t s = (uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+         s < a.num_seqs; s += warps) {
+        const uint64_t r0 = np[s], r1 = np[s + 1], len = lens[s];
+        const uint64_t lo = sp[s], hi = sp[s + 1];
+        if (r1 < r0) continue;
+        for (uint64_t i = 0; i < r1 - r0; ++i) {
+            const T* src = reinterpret_cast<const T*>(a.src + (r0 + i) * a.row_bytes);
+            T held[kHeld];  // the row's first vectors, loaded before the table lookup lands
+#pragma unroll
+            for (int k = 0; k < kHeld; ++k) {
+                const uint64_t v = lane + 32 * k;
+                if (v < nv) held[k] = __ldg(src + v);
+            }
+            const uint64_t t = len + i, j = t / P;
+            if (lo > hi || j >= hi - lo || lo + j >= a.table_len) {
+                report(a.d_status, HP_ERR_LEN);
+                continue;
+            }
+            const uint64_t phys = table[lo + j];
+            if (phys >= a.num_pages) {
+                report(a.d_status, HP_ERR_PAGE_ID);
+                continue;
+            }
+            T* dst = reinterpret_cast<T*>(a.dst + (phys * P + (t - j * P)) * a.row_bytes);
+#pragma unroll
+            for (int k = 0; k < kHeld; ++k) {
+                const uint64_t v = lane + 32 * k;
+                if (v < nv) dst[v] = held[k];
+            }
+            for (uint64_t v = lane + 32 * kHeld; v < nv; v += 32) dst[v] = __ldg(src + v);
+        }
+    }
+}
+
+template <typename IndexT, int VEC>
+int launch_rows(const CopyArgs& a, cudaStream_t st)
+{
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms == 0) return HP_ERR_CUDA;
+    uint64_t grid = (a.num_seqs + 7) / 8;
+    const uint64_t cap = (uint64_t)sms * 8;
+    grid = grid < cap ? grid : cap;
+    if (a.hdr)  // a dependent of the plan and the table check
+        return launch_dependent(append_rows_kernel<IndexT, VEC>, (unsigned)grid, 256, 0, st, a) ==
+                       cudaSuccess
+                   ? HP_OK
+                   : HP_ERR_CUDA;
+    append_rows_kernel<IndexT, VEC><<<(unsigned)grid, 256, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
+template <typename IndexT>
+int launch_rows_v(const CopyArgs& a, int vec, cudaStream_t st)
+{
+    switch (vec) {
+    case 16: return launch_rows<IndexT, 16>(a, st);
+    case 8: return launch_rows<IndexT, 8>(a, st);
+    case 4: return launch_rows<IndexT, 4>(a, st);
+    case 2: return launch_rows<IndexT, 2>(a, st);
+    default: return launch_rows<IndexT, 1>(a, st);
+    }
+}
+
 template <typename IndexT>
 int launch_t(const PlanArgs& a, unsigned* live, uint64_t row_bytes, void* pool,
              cudaStream_t st)
@@ -95,6 +195,14 @@ int launch_t(const PlanArgs& a, unsigned* live, uint64_t row_bytes, void* pool,
 }
 
 }  // namespace
+
+int launch_append_rows(int index_u64, const CopyArgs& a, int vec, void* stream)
+{
+    if (a.num_seqs == 0) return HP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return index_u64 ? launch_rows_v<unsigned long long>(a, vec, st)
+                     : launch_rows_v<unsigned int>(a, vec, st);
+}
 
 int launch_zero_tails(int index_u64, const PlanArgs& a, unsigned* live, uint64_t row_bytes,
                       void* pool, void* stream)

@@ -199,3 +199,82 @@ def test_planned_append_steps_equal_one_call(hp, oracle):
     torch.cuda.synchronize()
     assert b1.status_value() == 0 and b2.status_value() == 0
     assert torch.equal(b1.pool, b2.pool)
+
+
+def _permissive_case(hp, oracle, w, before, new_ptr, rows, pool=None):
+    import torch
+    b = Batch(w, flags=1, lens=np.asarray(before, dtype=w.index_dtype), pool=pool)
+    host = b.host_pool().copy()
+    rc = hp.hp_scatter_append(b.desc, torch.from_numpy(np.ascontiguousarray(rows)).to("cuda"),
+                              index_tensor(np.asarray(new_ptr, dtype=w.index_dtype), "cuda"),
+                              int(new_ptr[-1]), b.ws, b.status)
+    torch.cuda.synchronize()
+    assert rc == 0
+    o = b.oracle_desc(pool_host=host, lens=np.asarray(before, dtype=w.index_dtype))
+    want = o.scatter_append(rows, np.asarray(new_ptr, dtype=w.index_dtype))
+    return b.pool.cpu().numpy(), host, want, hp.status_name(b.status_value())
+
+
+@pytest.mark.parametrize("case", ["decode", "u64", "narrow", "wide", "few_rows"])
+def test_permissive_decode_step_matches_oracle(hp, oracle, case):
+    """HP_PERMISSIVE with fewer new rows than one page per sequence: the one-kernel path
+    (one warp per sequence, no plan) writes exactly what the oracle writes."""
+    rng = np.random.default_rng(len(case))
+    geo = {"decode": (16, 8, 128, "bf16", np.uint32), "u64": (16, 4, 64, "f16", np.uint64),
+           "narrow": (5, 3, 7, "f16", np.uint32), "wide": (8, 8, 256, "bf16", np.uint64),
+           "few_rows": (16, 2, 64, "f32", np.uint32)}[case]
+    P, H, D, dt, it = geo
+    w = inputs.decode_gather(seed=90 + len(case), num_pages=3000, page_size=P, num_heads=H,
+                             head_dim=D, num_seqs=40, len_lo=1, len_hi=400, dtype=dt,
+                             index_dtype=it)
+    full = w.lens.astype(np.int64)
+    new_n = np.minimum(full, rng.integers(0, 4 if case == "few_rows" else 2, w.num_seqs))
+    before = full - new_n
+    new_ptr = np.concatenate([[0], np.cumsum(new_n)])
+    rows = rng.integers(0, 256, (int(new_ptr[-1]), w.row_bytes), dtype=np.uint8)
+    got, want_pool, code, st = _permissive_case(hp, oracle, w, before, new_ptr, rows)
+    assert code == "OK" and st == "HP_OK"
+    assert np.array_equal(got, want_pool)
+
+
+def test_permissive_decode_step_full_size(hp, oracle):
+    import torch
+    w = inputs.config("decode_append", "full")
+    b = Batch(w, flags=1, lens=w.lens_before)
+    new = inputs.device_new_rows(w, "cuda")
+    rc = hp.hp_scatter_append(b.desc, new, index_tensor(w.new_ptr, "cuda"), w.total_new, b.ws,
+                              b.status)
+    torch.cuda.synchronize()
+    assert rc == 0 and b.status_value() == 0
+    g = Batch(w, pool=b.pool)
+    T = w.total_tokens
+    out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device="cuda")
+    assert hp.hp_gather(g.desc, out, T, g.ws, g.status) == 0
+    torch.cuda.synchronize()
+    tok_off = np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))])
+    got = out.cpu().numpy().reshape(T, -1)
+    assert np.array_equal(got[tok_off[1:] - 1], new.cpu().numpy())
+
+
+@pytest.mark.parametrize("fault", ["LEN", "PAGE_ID"])
+def test_permissive_decode_step_skips_unwritable_rows(hp, oracle, fault):
+    rng = np.random.default_rng(7)
+    w = inputs.decode_gather(seed=61, num_pages=800, page_size=8, num_heads=2, head_dim=16,
+                             num_seqs=12, len_lo=1, len_hi=90, dtype="f16")
+    full = w.lens.astype(np.int64)
+    new_n = np.ones(w.num_seqs, np.int64)
+    before = full - 1
+    table = w.table.copy()
+    if fault == "LEN":  # sequence 3 appends at a token past its slice
+        span = int(w.seq_ptr[4] - w.seq_ptr[3])
+        before[3] = span * w.page_size
+    else:  # the page sequence 5's new row lands in is not in the pool
+        k = int(w.seq_ptr[5]) + int(before[5]) // w.page_size
+        table[k] = w.num_pages + 3
+    w2 = inputs.Workload(**{**w.__dict__, "table": table})
+    new_ptr = np.concatenate([[0], np.cumsum(new_n)])
+    rows = rng.integers(0, 256, (int(new_ptr[-1]), w.row_bytes), dtype=np.uint8)
+    got, want_pool, code, st = _permissive_case(hp, oracle, w2, before, new_ptr, rows,
+                                                pool=inputs.device_pool(w, "cuda"))
+    assert code == fault and st == "HP_ERR_" + fault
+    assert np.array_equal(got, want_pool)
