@@ -439,6 +439,38 @@ def attention_only(scale, dev, hp, inputs, peak, reps):
     return res
 
 
+def decode_step_only(dev, hp, inputs, steps):
+    """The decode append step alone (one new row for each of 256 sequences of the
+    decode_append batch), validated and permissive, issued back to back."""
+    import torch
+    w = inputs.config("decode_append")
+    pool = inputs.device_pool(w, dev)
+    table, sp = idx_tensor(w.table, dev), idx_tensor(w.seq_ptr, dev)
+    before, new_ptr = idx_tensor(w.lens_before, dev), idx_tensor(w.new_ptr, dev)
+    new = inputs.device_new_rows(w, dev)
+    kw = dict(num_pages=w.num_pages, page_size=w.page_size, num_heads=w.num_heads,
+              head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {"op": "decode_append_step", "rows": w.total_new}
+    for flags, name in ((0, "validated"), (1, "permissive")):
+        d = hp.PagedDesc(pool, table, sp, before, flags=flags, **kw)
+        ws = hp.workspace_for(d, dev)
+        one = lambda: hp.hp_scatter_append(d, new, new_ptr, w.total_new, ws, status)
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, hp.status_name(int(status.item()))
+        res[name + "_us_back_to_back"] = round(a.elapsed_time(b) / steps * 1e3, 2)
+    return res
+
+
 def transpose_only(dev, hp, peak, reps, nb=10000, bsz=16, H=32, D=128, x=8):
     """Both cache layout conversions on a [nb, bs, H, D] fp16 cache (1.31 GB each way)."""
     import torch
@@ -699,8 +731,18 @@ def main():
                     help="time only the two cache layout conversions (kernel-internal "
                          "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
                          "and print their line")
+    ap.add_argument("--decode-step", action="store_true",
+                    help="issue --steps decode append steps (256 rows into the decode_append "
+                         "pool), validated and then permissive, and print their timing")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.decode_step:
+        import torch
+        from paged_kv_cache_hp_gb300 import build, hp, inputs
+        build.build()
+        hp.lib()
+        print(json.dumps(decode_step_only("cuda", hp, inputs, args.steps)))
+        return
     if args.transpose:
         import torch
         from paged_kv_cache_hp_gb300 import build, hp
