@@ -358,13 +358,12 @@ int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace
 /* ---------------------------------------------------------- decode attention */
 /*
  * Bytes of device workspace hp_attention_decode needs: the plan's (hp_workspace_bytes)
- * plus fp32 partials for every work chunk and query head.  A chunk is cp consecutive pages
- * of one sequence, cp the largest power of two in [HP_ATTN_MIN_CHUNK_PAGES,
- * HP_ATTN_CHUNK_PAGES] with (table_len / cp) * num_heads >= 4096 (else the minimum), so
- * the size depends only on the descriptor's table_len, num_heads, num_seqs and head_dim.
+ * plus fp32 records (max, sum and head_dim accumulators per query head) for up to
+ * (num_seqs + HP_ATTN_MAX_CTAS * R) * num_heads sequence segments, R = 8 / num_heads
+ * when num_heads < 8, else 1.  It depends only on the descriptor's num_seqs, num_heads
+ * and head_dim, and on num_q_heads.
  */
-#define HP_ATTN_CHUNK_PAGES 32
-#define HP_ATTN_MIN_CHUNK_PAGES 4
+#define HP_ATTN_MAX_CTAS 512
 int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t num_q_heads,
                                         uint64_t* bytes);
 

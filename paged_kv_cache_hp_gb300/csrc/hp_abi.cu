@@ -593,33 +593,28 @@ HP_API int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t wo
 
 namespace {
 
-// Pages per attention work chunk: the largest power of two in [HP_ATTN_MIN_CHUNK_PAGES,
-// HP_ATTN_CHUNK_PAGES] that still cuts the batch into at least kAttnItems (chunk, K/V head)
-// items, so a small batch still spreads over the GPU's warp slots (152 SMs x 16 warps);
-// table_len stands in for the pages the sequences use.  Measured: a larger target (more,
-// shorter chunks) gains nothing on 32 or more long sequences and loses 10% at 16384.
-#ifndef HP_ATTN_TARGET_ITEMS
-#define HP_ATTN_TARGET_ITEMS 4096
-#endif
-constexpr u64 kAttnItems = HP_ATTN_TARGET_ITEMS;
-u64 attn_chunk_pages(const hp_paged_desc* d)
+// Decode attention: a step is TS tokens of one sequence for one K/V head, TS = min(32/G,
+// 32/E) with E = head_dim/32 (the kernel's register budget); R step ranges per CTA.
+u64 attn_step_tokens(u64 G, u64 D)
 {
-    u64 cp = HP_ATTN_CHUNK_PAGES;
-    while (cp > HP_ATTN_MIN_CHUNK_PAGES && (u128)(d->table_len / cp) * d->num_heads < kAttnItems)
-        cp >>= 1;
-    return cp;
+    const u64 E = D / 32;
+    return (32 / G) < (32 / E) ? 32 / G : 32 / E;
 }
+uint32_t attn_ranges_per_cta(u64 Hkv) { return Hkv < 8 ? (uint32_t)(8 / Hkv) : 1u; }
 
-// Chunks a batch can have: a sequence of need_s <= slice_s pages has
-// ceil(need_s / cp) <= slice_s / cp + 1 of them.
-u64 attn_max_chunks(const hp_paged_desc* d) { return d->table_len / attn_chunk_pages(d) + d->num_seqs + 1; }
+// Segment records a batch can leave: worker v (of at most HP_ATTN_MAX_CTAS * R) writes
+// record (s + v) * H_kv + g for each sequence s and head g it meets.
+u64 attn_records(const hp_paged_desc* d)
+{
+    return (d->num_seqs + (u64)HP_ATTN_MAX_CTAS * attn_ranges_per_cta(d->num_heads)) * d->num_heads;
+}
 
 int attention_ws(const hp_paged_desc* d, uint32_t hq, u64* bytes)
 {
     u64 plan = 0;
     int rc = ws_bytes(d, &plan);
     if (rc) return rc;
-    const u128 part = (u128)attn_max_chunks(d) * hq * (d->head_dim + 2) * 4;
+    const u128 part = (u128)attn_records(d) * (hq / d->num_heads) * (d->head_dim + 2) * 4;
     if ((part + plan) >> 64) return HP_ERR_OVERFLOW;
     *bytes = plan + (u64)part;
     return HP_OK;
@@ -646,7 +641,7 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     if (num_q_heads == 0 || num_q_heads % d->num_heads) return HP_ERR_ARG;
     const u64 G = num_q_heads / d->num_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return HP_ERR_ARG;
-    if (d->page_size > (1u << 26)) return HP_ERR_ARG;  // token offsets in a chunk fit 32 bits
+    if (d->page_size > (1u << 26)) return HP_ERR_ARG;  // offsets in a 32-page window fit 32 bits
     if (d->num_seqs && (!q || !out)) return HP_ERR_NULL;
     if (d->num_pages && !v_pool) return HP_ERR_NULL;
     if (misaligned(v_pool, 64) || misaligned(q, 16) || misaligned(out, 16)) return HP_ERR_ALIGN;
@@ -657,7 +652,7 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     u64 plan_bytes = 0;
     ws_bytes(d, &plan_bytes);
     hp::PlanArgs pa = plan_args(d, workspace, d_status);
-    pa.chunk_pages = attn_chunk_pages(d);
+    pa.step_tokens = attn_step_tokens(G, d->head_dim);
     rc = hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
     if (rc || d->num_seqs == 0) return rc;
     hp::AttnArgs a{};
@@ -676,12 +671,12 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     a.D = (uint32_t)d->head_dim;
     a.G = (uint32_t)G;
     hp::invariant_divisor(d->page_size, &a.p_m, &a.p_l);
-    a.chunk_pages = pa.chunk_pages;
+    a.R = attn_ranges_per_cta(d->num_heads);
     a.scale = scale;
     a.hdr = pa.ws.hdr;
     a.units_off = pa.ws.units_off;
     a.part_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes);
-    a.part_ml = a.part_acc + attn_max_chunks(d) * num_q_heads * d->head_dim;
+    a.part_ml = a.part_acc + attn_records(d) * G * d->head_dim;
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
     a.d_status = d_status;

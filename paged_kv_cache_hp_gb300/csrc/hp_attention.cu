@@ -9,24 +9,30 @@
 //
 // Decode attention reads every key and value once for about 2G flops per byte, so it is
 // bound by HBM, not by arithmetic: it runs on the CUDA cores.
-//   attn_kernel     works on (chunk of chunk_pages pages, K/V head) items: a CTA owns a
-//                   contiguous range of them and its eight warps take every eighth, so
-//                   they read the heads of one chunk together.  A warp streams its item's
-//                   rows into a ring of kStages shared-memory stages with cp.async (a
-//                   step's K rows, then its V rows; the page of each token comes from the
-//                   chunk's page IDs, held one per lane), so the loads of the next steps
-//                   are in flight while it computes.  Lane l owns dims [l*E, l*E+E)
-//                   (E = D/32).  A step is TS tokens: their (token, query head) partial
-//                   dot products are summed across the warp with a transposed butterfly
-//                   (one shuffle per product), then an online softmax per query head
-//                   updates the running max, sum and the lane's E dims of the weighted
-//                   value sum.  Each item leaves (max, sum, acc[D]) per query head in the
-//                   workspace.
-//   combine_kernel  one warp per (sequence, query head) merges its chunks' partials.
-// Partials: acc [chunks, Hq, D] and (max, sum) [chunks, Hq] in the workspace after the plan.
+//   attn_kernel     a step is TS tokens of one sequence for one K/V head.  The plan
+//                   counts each sequence's steps; CTA b owns an equal share of the
+//                   (sequence, step) space for every K/V head, split into R sub-ranges
+//                   (R = 8 / H_kv when H_kv < 8, else 1), and warp w takes head w mod H_kv
+//                   (or heads w, w+8, ...) of sub-range w / H_kv.  So the warps of a CTA
+//                   read the heads of the same tokens together, and every warp runs the
+//                   same number of steps whatever the sequence lengths.  A warp streams
+//                   each sequence segment of its range into a ring of kStages shared-memory
+//                   stages with cp.async (a step's K rows, then its V rows; the pages come
+//                   from a window of 32 page IDs held one per lane), so the loads of the
+//                   next steps are in flight while it computes.  Lane l owns dims
+//                   [l*E, l*E+E) (E = D/32).  The TS*G (token, query head) partial dot
+//                   products of a step are summed across the warp with a transposed
+//                   butterfly (one shuffle per product), then an online softmax per query
+//                   head updates the running max, sum and the lane's E dims of the weighted
+//                   value sum.  Each segment leaves (max, sum, acc[D]) per query head as
+//                   record (s + v) * H_kv + g, v the warp's worker index.
+//   combine_kernel  one warp per (sequence, query head) merges its segments' records.
+// Records: acc [records, G, D] and (max, sum) [records, G] in the workspace after the plan.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "hp_internal.cuh"
 #include "hp_resolve.cuh"
@@ -128,24 +134,27 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-// Request one step's rows: tokens x0 .. x0+TS-1 of the chunk (offsets from its first
-// token), K rows then V rows of head g.  Lane l copies token l / LT: pieces
-// l % LT + LT*m of both rows, so the LT lanes of a token read LT*16 contiguous bytes per
-// instruction.  Tokens at or past n_tok become zero rows.
+// Request one step's rows: tokens t0 .. t0+TS-1 of the sequence (len tokens), K rows then
+// V rows of head g.  The pages come from the window of 32 page IDs whose first slot is
+// token wbeg (lane j holds the window's page j; the step lies inside the window).  Lane l copies token
+// l / LT: pieces l % LT + LT*m of both rows, so the LT lanes of a token read LT*16
+// contiguous bytes per instruction.  Tokens at or past len become zero rows.
 template <typename IndexT, int G, int E>
-__device__ __forceinline__ void issue_step(const AttnArgs& a, unsigned char* stage, uint32_t x0,
-                                           uint32_t n_tok, IndexT my_page, uint32_t g,
-                                           unsigned lane)
+__device__ __forceinline__ void issue_step(const AttnArgs& a, unsigned char* stage, uint64_t t0,
+                                           uint64_t len, uint64_t wbeg, IndexT my_page,
+                                           uint32_t g, unsigned lane)
 {
     using S = Step<G, E>;
     const char* K = static_cast<const char*>(a.k_pool);
     const char* V = static_cast<const char*>(a.v_pool);
     const unsigned i = lane / S::LT, jp = lane % S::LT;
-    const uint32_t x = x0 + i;
-    const uint32_t pi = div_invariant(x, a.p_m, a.p_l);  // the chunk's page holding x
+    const uint64_t x = t0 + i;
+    const bool live = x < len;
+    // offset from the window's first slot: below 32 pages (< 2^31) for a live token
+    const uint32_t rel = (uint32_t)(x - wbeg);
+    const uint32_t pi = div_invariant(rel, a.p_m, a.p_l);
     const IndexT page = __shfl_sync(0xffffffffu, my_page, (int)(pi & 31));
-    const bool live = x < n_tok;
-    const uint64_t slot_row = (uint64_t)page * a.page_size + (x - pi * (uint32_t)a.page_size);
+    const uint64_t slot_row = (uint64_t)page * a.page_size + (rel - pi * (uint32_t)a.page_size);
     const uint64_t off = (slot_row * a.Hkv + g) * S::ROW + jp * 16;
     const char* ks = live ? K + off : K;
     const char* vs = live ? V + off : K;
@@ -164,7 +173,7 @@ template <typename IndexT, bool BF16, int G, int E>
 __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_kernel(const AttnArgs a)
 {
     using S = Step<G, E>;
-    constexpr int TS = S::TS, NP = S::NP, R = S::R;
+    constexpr int TS = S::TS, NP = S::NP, R_ = S::R;
     using RowT = typename Pack<E>::T;
     extern __shared__ __align__(16) unsigned char smem[];
     pdl_wait();  // the plan before this launch is complete
@@ -178,21 +187,21 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
     // step.  Before it, lane l keeps slot k ^ lx at array position k, so every level of
     // the transposed butterfly keeps the low half and sends the high half: position k
     // reads K row (k / G) ^ lt with query head (k % G) ^ lh.
-    const unsigned lx = lane / R, my_tok = lx / G, my_head = lx % G;
+    const unsigned lx = lane / R_, my_tok = lx / G, my_head = lx % G;
     const unsigned lt = my_tok, lh = my_head;
     uint32_t roff[TS];  // byte offset in a stage of the K row position i reads
 #pragma unroll
     for (int i = 0; i < TS; ++i) roff[i] = (i ^ lt) * S::ROW + lane * (2 * E);
     const float qscale = a.scale * 1.4426950408889634f;  // scores in log2 units
 
-    // CTA b owns the contiguous range [it_lo, it_hi) of the (chunk, K/V head) items, head-
-    // major within a chunk; warp w takes items it_lo + w, it_lo + w + kWarps, ...  So the
-    // eight warps read the eight heads of one chunk together (whole 8-head runs of every
-    // token row), and a warp's next item is usually the next chunk: its sequence is found
-    // by walking forward from the last one (a binary search only for the first item).
-    const uint64_t items = a.hdr->total_units * a.Hkv;
-    const uint64_t it_lo = (uint64_t)((unsigned __int128)items * blockIdx.x / gridDim.x) + warp;
-    const uint64_t it_hi = (uint64_t)((unsigned __int128)items * (blockIdx.x + 1) / gridDim.x);
+    const uint64_t S_steps = a.hdr->total_units;  // steps of all sequences, one head
+    const uint64_t Lw = (S_steps + a.workers - 1) / a.workers;
+    const uint32_t R = a.R;
+    const uint32_t r = a.Hkv >= kWarps ? 0 : warp / a.Hkv;  // this warp's sub-range
+    if (r >= R || S_steps == 0) return;  // whole warp; no block-wide barrier in this kernel
+    const uint64_t v = (uint64_t)blockIdx.x * R + r;       // worker index
+    const uint64_t beg = umin(v * Lw, S_steps), end = umin(beg + Lw, S_steps);
+    if (beg >= end) return;
     const IndexT* table = static_cast<const IndexT*>(a.table);
     const IndexT* spp = static_cast<const IndexT*>(a.seq_ptr);
     const IndexT* lensp = static_cast<const IndexT*>(a.lens);
@@ -200,128 +209,143 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
     f2 qp[G][E / 2];   // position h holds query head h ^ lh, scaled
     float m[G], l[G];
     f2 acc[G][E / 2];  // the lane's dims of each head's weighted value sum
-    uint64_t s = it_lo < it_hi ? find_seq(a.units_off, a.num_seqs, it_lo / a.Hkv) : 0;
-    for (uint64_t it = it_lo; it < it_hi; it += kWarps) {
-        const uint64_t u = it / a.Hkv;
-        const uint32_t g = (uint32_t)(it - u * a.Hkv);
-        while (a.units_off[s + 1] <= u) ++s;  // skips sequences without chunks
-        const uint64_t c = u - a.units_off[s];
-        const uint64_t t_begin = c * a.chunk_pages * P;
-        const uint32_t n_tok = (uint32_t)(umin(lensp[s], t_begin + a.chunk_pages * P) - t_begin);
-        const uint64_t n_pg = (n_tok + P - 1) / P;
-        // the chunk's page IDs, one per lane (a chunk has at most 32 pages)
-        const IndexT my_page =
-            lane < n_pg ? table[(uint64_t)spp[s] + c * a.chunk_pages + lane] : IndexT(0);
-        const uint32_t steps = (n_tok + TS - 1) / TS;
-#pragma unroll
-        for (int k = 0; k < kStages - 1; ++k) {
-            if ((uint32_t)k < steps)
-                issue_step<IndexT, G, E>(a, ring + k * S::STAGE, k * TS, n_tok, my_page, g, lane);
-            cp_async_commit();
-        }
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            const RowT raw = __ldg(reinterpret_cast<const RowT*>(
-                Q + ((s * a.Hq + (uint64_t)g * G + (hh ^ lh)) * D + lane * E)));
-            widen_row<BF16, E>(raw, qp[hh]);
-#pragma unroll
-            for (int e = 0; e < E / 2; ++e) qp[hh][e] = mul2(qp[hh][e], pack2(qscale, qscale));
-            m[hh] = -INFINITY;
-            l[hh] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < E / 2; ++e) acc[hh][e] = 0ull;
-        }
-
-        for (uint32_t k = 0; k < steps; ++k) {
-            const uint32_t kn = k + kStages - 1;
-            if (kn < steps)
-                issue_step<IndexT, G, E>(a, ring + (kn % kStages) * S::STAGE, kn * TS, n_tok,
-                                         my_page, g, lane);
-            cp_async_commit();
-            cp_async_wait<kStages - 1>();  // this lane's pieces of step k have landed
-            __syncwarp();                  // and every other lane's
-            const unsigned char* st = ring + (k % kStages) * S::STAGE;
-
-            float part[NP];
-#pragma unroll
-            for (int i = 0; i < TS; ++i) {
-                f2 kv[E / 2];
-                widen_row<BF16, E>(*reinterpret_cast<const RowT*>(st + roff[i]), kv);
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    f2 d = mul2(qp[hh][0], kv[0]);
-#pragma unroll
-                    for (int e = 1; e < E / 2; ++e) d = fma2(qp[hh][e], kv[e], d);
-                    float d0, d1;
-                    unpack2(d, d0, d1);
-                    part[i * G + hh] = d0 + d1;
+    const uint64_t s_first = find_seq(a.units_off, a.num_seqs, beg);
+    for (uint32_t g = a.Hkv >= kWarps ? warp : warp % a.Hkv; g < a.Hkv;
+         g += a.Hkv >= kWarps ? kWarps : a.Hkv) {
+        uint64_t s = s_first;
+        for (uint64_t pos = beg; pos < end;) {
+            while (a.units_off[s + 1] <= pos) ++s;  // skips sequences without steps
+            const uint64_t so = a.units_off[s];
+            const uint64_t k0 = pos - so, k1 = umin(a.units_off[s + 1], end) - so;
+            pos = so + k1;
+            const uint64_t len = lensp[s], tab0 = spp[s];
+            // the window of 32 page IDs the issuing steps read from: logical pages
+            // pw0 .. pw0+31, tokens [wbeg, wend)
+            const uint64_t tab1 = spp[s + 1];
+            uint64_t pw0 = k0 * TS / P, wbeg = pw0 * P, wend = wbeg + 32 * P;
+            IndexT my_page = tab0 + pw0 + lane < tab1 ? table[tab0 + pw0 + lane] : IndexT(0);
+            auto issue = [&](uint64_t k, unsigned char* stage) {
+                const uint64_t t0 = k * TS;
+                if (umin(t0 + TS, len) > wend) {  // move the window to this step's first page
+                    pw0 = t0 / P;
+                    wbeg = pw0 * P;
+                    wend = wbeg + 32 * P;
+                    my_page = tab0 + pw0 + lane < tab1 ? table[tab0 + pw0 + lane] : IndexT(0);
                 }
+                issue_step<IndexT, G, E>(a, stage, t0, len, wbeg, my_page, g, lane);
+            };
+#pragma unroll
+            for (int j = 0; j < kStages - 1; ++j) {
+                if (k0 + j < k1) issue(k0 + j, ring + j * S::STAGE);
+                cp_async_commit();
             }
-            // transposed butterfly: every level keeps the low half and sends the high half
-#pragma unroll
-            for (int o = 16, n = NP; n > 1; o >>= 1, n >>= 1) {
-#pragma unroll
-                for (int e = 0; e < n / 2; ++e)
-                    part[e] += __shfl_xor_sync(0xffffffffu, part[e + n / 2], o);
-            }
-#pragma unroll
-            for (int o = R / 2; o >= 1; o >>= 1) part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
-            const float sc = (k * TS + my_tok < n_tok) ? part[0] : -INFINITY;
-            // per-head step maximum: lanes of one head differ only in the token bits (>= R*G)
-            float bm = sc;
-#pragma unroll
-            for (int o = R * G; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-            float mnew[G], corr[G], my_m = 0.0f;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-                mnew[hh] = fmaxf(m[hh], __shfl_sync(0xffffffffu, bm, hh * R));
-                corr[hh] = exp2_approx(m[hh] - mnew[hh]);  // 0 on the first step (m = -inf)
-                if ((int)my_head == hh) my_m = mnew[hh];
+                const RowT raw = __ldg(reinterpret_cast<const RowT*>(
+                    Q + ((s * a.Hq + (uint64_t)g * G + (hh ^ lh)) * D + lane * E)));
+                widen_row<BF16, E>(raw, qp[hh]);
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) qp[hh][e] = mul2(qp[hh][e], pack2(qscale, qscale));
+                m[hh] = -INFINITY;
+                l[hh] = 0.0f;
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) acc[hh][e] = 0ull;
             }
-            const float p = exp2_approx(sc - my_m);  // 0 for tokens past the chunk
-            if (lane % R == 0) wbuf[lx] = pack2(p, p);
-            float ps = p;
+
+            uint32_t slot = 0;
+            for (uint64_t k = k0; k < k1; ++k) {
+                const uint64_t kn = k + kStages - 1;
+                if (kn < k1)
+                    issue(kn, ring + (slot == 0 ? kStages - 1 : slot - 1) * S::STAGE);
+                cp_async_commit();
+                cp_async_wait<kStages - 1>();  // this lane's pieces of step k have landed
+                __syncwarp();                  // and every other lane's
+                const unsigned char* st = ring + slot * S::STAGE;
+                if (++slot == kStages) slot = 0;
+
+                float part[NP];
 #pragma unroll
-            for (int o = R * G; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                for (int i = 0; i < TS; ++i) {
+                    f2 kv[E / 2];
+                    widen_row<BF16, E>(*reinterpret_cast<const RowT*>(st + roff[i]), kv);
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                l[hh] = l[hh] * corr[hh] + __shfl_sync(0xffffffffu, ps, hh * R);
-                m[hh] = mnew[hh];
-                const f2 c2 = pack2(corr[hh], corr[hh]);
+                    for (int hh = 0; hh < G; ++hh) {
+                        f2 d = mul2(qp[hh][0], kv[0]);
 #pragma unroll
-                for (int e = 0; e < E / 2; ++e) acc[hh][e] = mul2(acc[hh][e], c2);
-            }
-            __syncwarp();  // the weights are in wbuf
+                        for (int e = 1; e < E / 2; ++e) d = fma2(qp[hh][e], kv[e], d);
+                        float d0, d1;
+                        unpack2(d, d0, d1);
+                        part[i * G + hh] = d0 + d1;
+                    }
+                }
+                // transposed butterfly: every level keeps the low half and sends the high half
 #pragma unroll
-            for (int i = 0; i < TS; ++i) {
-                f2 vv[E / 2];  // rows past the chunk are zeros with weight 0
-                widen_row<BF16, E>(
-                    *reinterpret_cast<const RowT*>(st + (TS + i) * S::ROW + lane * (2 * E)), vv);
+                for (int o = 16, n = NP; n > 1; o >>= 1, n >>= 1) {
+#pragma unroll
+                    for (int e = 0; e < n / 2; ++e)
+                        part[e] += __shfl_xor_sync(0xffffffffu, part[e + n / 2], o);
+                }
+#pragma unroll
+                for (int o = R_ / 2; o >= 1; o >>= 1) part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
+                const float sc = (k * TS + my_tok < len) ? part[0] : -INFINITY;
+                // per-head step maximum: lanes of one head differ only in the token bits
+                float bm = sc;
+#pragma unroll
+                for (int o = R_ * G; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+                float mnew[G], corr[G], my_m = 0.0f;
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
-                    const f2 w = wbuf[i * G + hh];
-#pragma unroll
-                    for (int e = 0; e < E / 2; ++e) acc[hh][e] = fma2(w, vv[e], acc[hh][e]);
+                    mnew[hh] = fmaxf(m[hh], __shfl_sync(0xffffffffu, bm, hh * R_));
+                    corr[hh] = exp2_approx(m[hh] - mnew[hh]);  // 0 on the first step (m = -inf)
+                    if ((int)my_head == hh) my_m = mnew[hh];
                 }
+                const float p = exp2_approx(sc - my_m);  // 0 for tokens past the sequence
+                if (lane % R_ == 0) wbuf[lx] = pack2(p, p);
+                float ps = p;
+#pragma unroll
+                for (int o = R_ * G; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    l[hh] = l[hh] * corr[hh] + __shfl_sync(0xffffffffu, ps, hh * R_);
+                    m[hh] = mnew[hh];
+                    const f2 c2 = pack2(corr[hh], corr[hh]);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) acc[hh][e] = mul2(acc[hh][e], c2);
+                }
+                __syncwarp();  // the weights are in wbuf
+#pragma unroll
+                for (int i = 0; i < TS; ++i) {
+                    f2 vv[E / 2];  // rows past the sequence are zeros with weight 0
+                    widen_row<BF16, E>(
+                        *reinterpret_cast<const RowT*>(st + (TS + i) * S::ROW + lane * (2 * E)), vv);
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        const f2 w = wbuf[i * G + hh];
+#pragma unroll
+                        for (int e = 0; e < E / 2; ++e) acc[hh][e] = fma2(w, vv[e], acc[hh][e]);
+                    }
+                }
+                __syncwarp();  // the stage and wbuf are rewritten by later steps
             }
-            __syncwarp();  // the stage and wbuf are rewritten by later steps
-        }
-        // the item's partial result
-        const uint64_t row0 = u * a.Hq + (uint64_t)g * G;
+            // the segment's record
+            const uint64_t row0 = ((s + v) * a.Hkv + g) * G;
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            if (lane == 0)
-                reinterpret_cast<float2*>(a.part_ml)[row0 + hh] = make_float2(m[hh], l[hh]);
-            f2* o = reinterpret_cast<f2*>(a.part_acc + (row0 + hh) * D + lane * E);
+            for (int hh = 0; hh < G; ++hh) {
+                if (lane == 0)
+                    reinterpret_cast<float2*>(a.part_ml)[row0 + hh] = make_float2(m[hh], l[hh]);
+                f2* o = reinterpret_cast<f2*>(a.part_acc + (row0 + hh) * D + lane * E);
 #pragma unroll
-            for (int e = 0; e < E / 2; ++e) o[e] = acc[hh][e];
+                for (int e = 0; e < E / 2; ++e) o[e] = acc[hh][e];
+            }
         }
     }
 }
 
-// One warp per (sequence, query head) merges its chunks' partials: the maximum and the
-// rescaled sum over the chunks with the lanes striding the chunks, then the weighted
-// accumulators with each lane owning EV = D/32 dims (vector loads, four chunks in flight).
+// One warp per (sequence, query head) merges its segments' records: the sequence's steps
+// [SO, SO + n) met workers f = SO / Lw .. l = (SO + n - 1) / Lw, and worker v left record
+// (s + v) * H_kv + g.  The maximum and the rescaled sum over the records with the lanes
+// striding them, then the weighted accumulators with each lane owning EV = D/32 dims
+// (vector loads, four records in flight).
 template <int EV>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a)
 {
@@ -329,54 +353,59 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a)
     pdl_wait();
     if (a.hdr->verdict != kVerdictOk) return;
     const unsigned lane = threadIdx.x & 31;
-    const uint64_t pairs = a.num_seqs * a.Hq, D = a.D;
+    const uint64_t pairs = a.num_seqs * a.Hq, D = a.D, G = a.G;
     const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
+    const uint64_t S_steps = a.hdr->total_units;
+    const uint64_t Lw = S_steps ? (S_steps + a.workers - 1) / a.workers : 1;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
     for (uint64_t w = (uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < pairs;
          w += warps) {
-        const uint64_t s = w / a.Hq, qh = w - s * a.Hq;
-        const uint64_t c0 = a.units_off[s], c1 = a.units_off[s + 1];
+        const uint64_t s = w / a.Hq, qh = w - s * a.Hq, g = qh / G, hh = qh - g * G;
+        const uint64_t so = a.units_off[s], n = a.units_off[s + 1] - so;
         float acc[EV];
 #pragma unroll
         for (int e = 0; e < EV; ++e) acc[e] = 0.0f;
-        if (c1 > c0) {
+        if (n > 0) {
+            const uint64_t f = so / Lw, nr = (so + n - 1) / Lw - f + 1;
+            // record j of this (sequence, query head): row ((s + f + j) * H_kv + g) * G + hh
+            const uint64_t row0 = ((s + f) * a.Hkv + g) * G + hh, stride = (uint64_t)a.Hkv * G;
             float M = -INFINITY;
-            for (uint64_t c = c0 + lane; c < c1; c += 32) M = fmaxf(M, ml[c * a.Hq + qh].x);
+            for (uint64_t j = lane; j < nr; j += 32) M = fmaxf(M, ml[row0 + j * stride].x);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             float L = 0.0f;
-            for (uint64_t c = c0 + lane; c < c1; c += 32) {
-                const float2 v = ml[c * a.Hq + qh];
+            for (uint64_t j = lane; j < nr; j += 32) {
+                const float2 v = ml[row0 + j * stride];
                 L += v.y * exp2f(v.x - M);
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
             const float inv = 1.0f / L;
-            uint64_t c = c0;
-            for (; c + 4 <= c1; c += 4) {
+            uint64_t j = 0;
+            for (; j + 4 <= nr; j += 4) {
                 VT v[4];
                 float wt[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint64_t row = (c + j) * a.Hq + qh;
-                    v[j] = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
-                    wt[j] = ml[row].x;
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t row = row0 + (j + k) * stride;
+                    v[k] = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
+                    wt[k] = ml[row].x;
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float x = exp2f(wt[j] - M);
-                    const float* f = reinterpret_cast<const float*>(&v[j]);
+                for (int k = 0; k < 4; ++k) {
+                    const float x = exp2f(wt[k] - M);
+                    const float* f4 = reinterpret_cast<const float*>(&v[k]);
 #pragma unroll
-                    for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f[e], acc[e]);
+                    for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f4[e], acc[e]);
                 }
             }
-            for (; c < c1; ++c) {
-                const uint64_t row = c * a.Hq + qh;
+            for (; j < nr; ++j) {
+                const uint64_t row = row0 + j * stride;
                 const VT v = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
                 const float x = exp2f(ml[row].x - M);
-                const float* f = reinterpret_cast<const float*>(&v);
+                const float* f4 = reinterpret_cast<const float*>(&v);
 #pragma unroll
-                for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f[e], acc[e]);
+                for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f4[e], acc[e]);
             }
 #pragma unroll
             for (int e = 0; e < EV; ++e) acc[e] *= inv;
@@ -395,14 +424,17 @@ int launch_g(const AttnArgs& a, cudaStream_t st)
     if (!allow_dynamic_smem<attn_kernel<IndexT, BF16, G, E>>(dev, smem)) return HP_ERR_CUDA;
     const int per_sm = resident_ctas<attn_kernel<IndexT, BF16, G, E>>(dev, kThreads, smem);
     if (per_sm == 0) return HP_ERR_CUDA;
-    if (launch_dependent(attn_kernel<IndexT, BF16, G, E>, (unsigned)(sms * per_sm), kThreads,
-                         smem, st, a) != cudaSuccess)
+    AttnArgs b = a;
+    const uint64_t ctas = std::min<uint64_t>((uint64_t)sms * per_sm, HP_ATTN_MAX_CTAS);
+    b.workers = ctas * b.R;
+    if (launch_dependent(attn_kernel<IndexT, BF16, G, E>, (unsigned)ctas, kThreads, smem, st,
+                         b) != cudaSuccess)
         return HP_ERR_CUDA;
     uint64_t g2 = (a.num_seqs * a.Hq + 7) / 8;
     const uint64_t cap = (uint64_t)sms * 8;
     g2 = g2 == 0 ? 1 : (g2 < cap ? g2 : cap);
     auto comb = E == 2 ? combine_kernel<2> : (E == 4 ? combine_kernel<4> : combine_kernel<8>);
-    return launch_dependent(comb, (unsigned)g2, 256, 0, st, a) == cudaSuccess
+    return launch_dependent(comb, (unsigned)g2, 256, 0, st, b) == cudaSuccess
                ? HP_OK
                : HP_ERR_CUDA;
 }

@@ -99,7 +99,7 @@ struct PlanArgs {
     uint64_t num_seqs, page_size, table_len, num_pages;
     uint64_t out_tokens;      // gather: expected total rows
     uint64_t total_new;       // append: expected new_ptr[S]
-    uint64_t chunk_pages;     // attention: pages per work chunk
+    uint64_t step_tokens;     // attention: tokens per step (its units are steps)
     int strict;               // check the storage invariants
     int check_out;            // gather: compare the total with out_tokens
     int* d_status;
@@ -120,12 +120,13 @@ struct AttnArgs {
     uint64_t num_seqs, page_size, num_pages, table_len;
     uint32_t Hkv, Hq, D, G;   // G = Hq / Hkv query heads per K/V head
     uint32_t p_m, p_l;        // div_invariant constants of page_size
-    uint64_t chunk_pages;
+    uint32_t R;               // workers per CTA: step ranges a CTA splits among its warps
+    uint64_t workers;         // CTAs * R
     float scale;
     const WsHeader* hdr;
     const unsigned long long* units_off;  // chunks per sequence, prefix
-    float* part_acc;          // [max chunks, Hq, D]: each chunk's weighted value sums
-    float* part_ml;           // [max chunks, Hq, 2]: its score maximum and weight sum
+    float* part_acc;          // [records, G, D]: each segment's weighted value sums
+    float* part_ml;           // [records, G, 2]: its score maximum and weight sum
     float* out;               // [num_seqs, Hq, D] fp32
     int elem_bf16;            // element type: bf16 (1) or f16 (0)
     int* d_status;

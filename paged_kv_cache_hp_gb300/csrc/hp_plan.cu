@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a)
                     else if (units > hi - lo)
                         atomicMin(&s_key, verdict_key(kRankLen, s));
                 }
-                if (MODE == kPlanAttention)  // pages -> chunks of chunk_pages pages
-                    units = units / a.chunk_pages + (units % a.chunk_pages != 0);
+                if (MODE == kPlanAttention)  // tokens -> steps of step_tokens tokens
+                    units = len / a.step_tokens + (len % a.step_tokens != 0);
             } else {
                 const unsigned long long n0 = np[s], n1 = np[s + 1];
                 const bool ok_new = n0 <= n1 && n1 <= a.total_new;

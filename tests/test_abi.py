@@ -158,23 +158,19 @@ def test_lane_host_checks(hpc):
                                             None, None)) == "HP_ERR_LANE_OVERFLOW"
 
 
-@pytest.mark.parametrize("table_len,num_heads,cp", [
-    (273_000, 8, 32), (31_300, 8, 32), (20_000, 8, 32), (8_200, 8, 16), (4_100, 8, 8),
-    (4_000, 8, 4), (100, 2, 4), (0, 8, 4), (1_000_000, 1, 32), (40_000, 1, 8),
+@pytest.mark.parametrize("num_seqs,num_heads,G,D", [
+    (256, 8, 4, 128), (32, 8, 4, 128), (0, 8, 4, 128), (1, 1, 8, 64), (2048, 2, 2, 256),
+    (7, 3, 1, 64), (100, 12, 2, 128), (5, 16, 1, 256),
 ])
-def test_attention_workspace_follows_the_chunk_rule(hpc, table_len, num_heads, cp):
-    """hp_attention_decode_workspace_bytes = the plan's workspace + fp32 (max, sum, acc[D])
-    for table_len / cp + num_seqs + 1 chunks and every query head, cp the documented chunk
-    size: the largest power of two in [4, 32] with (table_len / cp) * num_heads >= 4096."""
-    W, f = fake_desc(hpc, num_seqs=37, table_len=table_len, num_heads=num_heads, head_dim=128,
-                     num_pages=max(table_len, 1), block_table=0x20000 if table_len else 0)
-    rule = 32
-    while rule > 4 and (table_len // rule) * num_heads < 4096:
-        rule //= 2
-    assert rule == cp
+def test_attention_workspace_bound(hpc, num_seqs, num_heads, G, D):
+    """hp_attention_decode_workspace_bytes = the plan's workspace + fp32 records (max, sum,
+    acc[D]) of every query head for (num_seqs + 512 * R) * num_heads segments, R = 8 /
+    num_heads below 8 K/V heads, else 1."""
+    W, f = fake_desc(hpc, num_seqs=num_seqs, table_len=3, num_heads=num_heads, head_dim=D,
+                     num_pages=4)
     plan = ctypes.c_uint64(0)
     assert hpc.lib().hp_workspace_bytes(W.ref, ctypes.byref(plan)) == 0
-    Hq = 4 * num_heads
-    rc, n = hpc.hp_attention_decode_workspace_bytes(W, Hq)
+    R = 8 // num_heads if num_heads < 8 else 1
+    rc, n = hpc.hp_attention_decode_workspace_bytes(W, G * num_heads)
     assert rc == 0
-    assert n == plan.value + (table_len // cp + 37 + 1) * Hq * (128 + 2) * 4
+    assert n == plan.value + (num_seqs + 512 * R) * num_heads * G * (D + 2) * 4
