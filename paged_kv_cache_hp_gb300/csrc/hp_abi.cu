@@ -12,6 +12,7 @@
 #include <cstring>
 #include <vector>
 
+#include "hp_attn.cuh"
 #include "hp_internal.cuh"
 
 #define HP_API extern "C" __attribute__((visibility("default")))

@@ -34,6 +34,7 @@
 
 #include <algorithm>
 
+#include "hp_attn.cuh"
 #include "hp_internal.cuh"
 #include "hp_resolve.cuh"
 

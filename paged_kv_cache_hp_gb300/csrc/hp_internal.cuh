@@ -109,30 +109,6 @@ struct PlanArgs {
 // Launches the plan (and, when strict, the block-table check) on `stream`.
 int launch_plan(PlanMode mode, int index_u64, const PlanArgs& a, void* stream);
 
-// Decode attention (hp_attention.cu), after a kPlanAttention plan on the same stream.
-struct AttnArgs {
-    const void* k_pool;
-    const void* v_pool;
-    const void* q;            // [num_seqs, Hq, D]
-    const void* table;
-    const void* seq_ptr;
-    const void* lens;
-    uint64_t num_seqs, page_size, num_pages, table_len;
-    uint32_t Hkv, Hq, D, G;   // G = Hq / Hkv query heads per K/V head
-    uint32_t p_m, p_l;        // div_invariant constants of page_size
-    uint32_t R;               // workers per CTA: step ranges a CTA splits among its warps
-    uint64_t workers;         // CTAs * R
-    float scale;
-    const WsHeader* hdr;
-    const unsigned long long* units_off;  // chunks per sequence, prefix
-    float* part_acc;          // [records, G, D]: each segment's weighted value sums
-    float* part_ml;           // [records, G, 2]: its score maximum and weight sum
-    float* out;               // [num_seqs, Hq, D] fp32
-    int elem_bf16;            // element type: bf16 (1) or f16 (0)
-    int* d_status;
-};
-int launch_attention(int index_u64, const AttnArgs& a, void* stream);
-
 // Block-table forms (hp_plan.cu): padded [batch, max_blocks] + counts <-> CSR slices.
 struct TableArgs {
     bool to_csr;
