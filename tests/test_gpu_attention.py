@@ -3,9 +3,10 @@ oracle's float64 attention.
 
 Tolerance, derived from the fp32 path: each output is a convex combination of value rows,
 so |out| <= max|V|; the kernel's errors come from fp32 dot products of head_dim terms,
-a base-2 exponential with relative error below 2^-22, and fp32 accumulation over at most
-a few thousand weighted rows per chunk plus the chunk merge -- a relative error well
-under 1e-3 of max|V| (about n * 2^-24 for n terms in the worst case).  The bar is |gpu - oracle| <= 1e-3 * max|V| + 1e-6 per element."""
+a base-2 exponential with relative error below 2^-22, and fp32 accumulation over the
+weighted rows of each sequence segment plus the merge of the segments' records -- a
+relative error well under 1e-3 of max|V| (about n * 2^-24 for n terms in the worst
+case).  The bar is |gpu - oracle| <= 1e-3 * max|V| + 1e-6 per element."""
 import numpy as np
 import pytest
 
@@ -51,7 +52,7 @@ def _check(got, want, vmax):
     ("bf16", 8, 4, 128, 16, 1.5),  # peaked softmax: a few tokens carry the weight
 ])
 def test_attention_matches_oracle(hp, oracle, dtype, Hkv, G, D, P, scale):
-    # lengths up to ~1300 tokens: several chunks of 32 pages for small pages
+    # lengths up to ~1300 tokens: small pages move the 32-page window many times
     w = inputs.decode_gather(seed=Hkv * 10 + G + D + P, num_pages=4000, page_size=P,
                              num_heads=Hkv, head_dim=D, num_seqs=5, len_lo=0, len_hi=1300,
                              dtype=dtype, index_dtype=np.uint32 if P % 2 == 0 else np.uint64)
@@ -135,3 +136,35 @@ def test_attention_rejections(hp, oracle):
         "HP_ERR_ARG"   # 48 query heads over 32 K/V heads
     assert hp.status_name(hp.hp_attention_decode(b.desc, b.pool, q, 32, 1.0, out, ws[:100])) == \
         "HP_ERR_WORKSPACE"
+
+
+def test_attention_one_long_sequence_split_over_many_warps(hp, oracle):
+    """One sequence of 30,000 tokens: the step space is shared by every CTA, so the
+    sequence is cut into hundreds of segments whose records the combine merges."""
+    import torch
+    table = np.random.default_rng(3).permutation(2000)[:1875].astype(np.uint32)
+    w = inputs.Workload("long", 2000, 16, 2, 128, "bf16", np.uint32, table,
+                        np.array([0, 1875], np.uint32), np.array([30000], np.uint32), 5, "normal")
+    b, vpool, qt, got, scale = _run(hp, oracle, w, 8, seed=4)
+    od = b.oracle_desc()
+    want = od.attention_decode(vpool.cpu().numpy(), qt.view(torch.int16).numpy().view(np.uint16),
+                               8, scale)
+    _check(got, want, _vmax_read(od, vpool.cpu().numpy(), "bf16"))
+
+
+def test_attention_mostly_empty_batch(hp, oracle):
+    """600 sequences, all but three empty: empty ones give zeros, the others match."""
+    import torch
+    rng = np.random.default_rng(8)
+    lens = np.zeros(600, np.uint32)
+    lens[[5, 300, 599]] = [17, 700, 1]
+    pages = -(-lens.astype(np.int64) // 16)
+    sp = np.concatenate([[0], np.cumsum(pages)]).astype(np.uint32)
+    table = rng.permutation(400)[:int(sp[-1])].astype(np.uint32)
+    w = inputs.Workload("sparse", 400, 16, 4, 64, "f16", np.uint32, table, sp, lens, 6, "normal")
+    b, vpool, qt, got, scale = _run(hp, oracle, w, 8, seed=5)
+    od = b.oracle_desc()
+    want = od.attention_decode(vpool.cpu().numpy(), qt.view(torch.int16).numpy().view(np.uint16),
+                               8, scale)
+    _check(got, want, _vmax_read(od, vpool.cpu().numpy(), "f16"))
+    assert (got[lens == 0] == 0).all()
