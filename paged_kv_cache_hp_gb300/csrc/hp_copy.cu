@@ -196,21 +196,25 @@ __device__ __forceinline__ uint2 ld_stream8(const uint2* p)
     return v;
 }
 
+// 8-byte loads in flight per thread, by measurement on GB300 (a 2.5 GB pool, fraction of
+// the copy bandwidth): per slot 0.85 / 0.90 / 0.81 at 16 / 12 / 24; per head 0.83 at 8,
+// 0.86 at 12; per head_dim 0.84 at 8, 0.79 at 6 and 12.  Fewer loads leave too little in
+// flight; more cost registers and resident CTAs.
 #ifndef HP_DQ_UNROLL
-#define HP_DQ_UNROLL 16
+#define HP_DQ_UNROLL 12
 #endif
-constexpr int kDqUnroll = HP_DQ_UNROLL;  // 8-byte loads in flight per thread
+#ifndef HP_DQ_UNROLL_DIM
+#define HP_DQ_UNROLL_DIM 8
+#endif
+constexpr int kDqUnroll = HP_DQ_UNROLL;
+constexpr int kDqUnrollDim = HP_DQ_UNROLL_DIM;  // per-head_dim scales and zero points
 #ifndef HP_DQ_DIM_HOIST
 #define HP_DQ_DIM_HOIST 0
-#endif
-#ifndef HP_DQ_DIM_DIV
-#define HP_DQ_DIM_DIV 2
 #endif
 // Per-head_dim scales and zero points held in registers cost 16 live values per thread
 // (101 registers, 2 CTAs per SM); read per group from L1 instead the kernel keeps 4 CTAs
 // per SM and its loads in flight (0.76 -> 0.83 of the copy bandwidth on a 2.5 GB pool).
 constexpr bool kDqDimHoist = HP_DQ_DIM_HOIST;
-constexpr int kDqDimDiv = HP_DQ_DIM_DIV;       // per-head_dim: kDqUnroll / this in flight
 
 // 8-bit rows -> bfloat16 rows, 8 elements per thread step.  `n8` groups of 8; the row of
 // group v within the unit is v / (row_elems/8) and, for per-channel schemes, its head is
@@ -259,10 +263,7 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
             }
         }
     }
-    // per-channel groups keep 16 more values live: half the loads in flight per thread,
-    // for more resident CTAs
-    constexpr int kU = kScheme == kQHead ? kDqUnroll / 2
-                       : kScheme == kQDim ? kDqUnroll / kDqDimDiv : kDqUnroll;
+    constexpr int kU = kScheme == kQDim ? kDqUnrollDim : kDqUnroll;
     const uint2* s = reinterpret_cast<const uint2*>(src);
     uint4* d = reinterpret_cast<uint4*>(dst);
     for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kU) {
