@@ -369,6 +369,26 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
     const uint64_t lo = b * per + umin(b, rem);
     const uint64_t hi = lo + per + (b < rem ? 1 : 0);
 
+    if (WARP_UNITS) {
+        // Each warp resolves 32 units at a time (one per lane) and copies them one after
+        // the other, descriptors handed over by shuffle: no CTA-wide barrier, so one
+        // warp's resolution overlaps the other warps' copies.
+        const unsigned lane = threadIdx.x & 31;
+        for (uint64_t w0 = lo + (threadIdx.x >> 5) * 32; w0 < hi; w0 += kThreads) {
+            Unit r{0, 0, 0, 0};
+            if (w0 + lane < hi) r = resolve<MODE, IndexT>(a, w0 + lane);
+            const int nb = (int)umin(32, hi - w0);
+            for (int i = 0; i < nb; ++i) {
+                const unsigned rows = __shfl_sync(0xffffffffu, r.rows, i);
+                if (rows == 0) continue;
+                const unsigned long long us = __shfl_sync(0xffffffffu, r.src, i);
+                const unsigned long long ud = __shfl_sync(0xffffffffu, r.dst, i);
+                copy_run_warp<VEC>(a.src + us, a.dst + ud, rows * a.row_bytes / VEC);
+            }
+        }
+        return;
+    }
+
     for (uint64_t u0 = lo; u0 < hi; u0 += kThreads) {
         const uint64_t u = u0 + threadIdx.x;
         if (u < hi) {
@@ -380,14 +400,6 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
         }
         __syncthreads();
         const int nb = (int)umin(kThreads, hi - u0);
-        if (WARP_UNITS) {
-            for (int i = threadIdx.x >> 5; i < nb; i += kThreads / 32)
-                if (s_rows[i])
-                    copy_run_warp<VEC>(a.src + s_src[i], a.dst + s_dst[i],
-                                       s_rows[i] * a.row_bytes / VEC);
-            __syncthreads();
-            continue;
-        }
         for (int i = 0; i < nb; ++i) {
             const unsigned rows = s_rows[i];
             if (rows == 0) continue;
