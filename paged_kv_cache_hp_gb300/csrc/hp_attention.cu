@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
     const IndexT* lensp = static_cast<const IndexT*>(a.lens);
     const uint64_t P = a.page_size;
     f2 qp[G][E / 2];   // position h holds query head h ^ lh, scaled
-    float m[G], l[G];
+    float m[G];        // each head's running maximum (the same in every lane)
     f2 acc[G][E / 2];  // the lane's dims of each head's weighted value sum
     const uint64_t s_first = find_seq(a.units_off, a.num_seqs, beg);
     for (uint32_t g = a.Hkv >= kWarps ? warp : warp % a.Hkv; g < a.Hkv;
@@ -248,10 +248,10 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
 #pragma unroll
                 for (int e = 0; e < E / 2; ++e) qp[hh][e] = mul2(qp[hh][e], pack2(qscale, qscale));
                 m[hh] = -INFINITY;
-                l[hh] = 0.0f;
 #pragma unroll
                 for (int e = 0; e < E / 2; ++e) acc[hh][e] = 0ull;
             }
+            float my_m = -INFINITY, lp = 0.0f;  // this lane's head: running max, weight sum
 
             uint32_t slot = 0;
             for (uint64_t k = k0; k < k1; ++k) {
@@ -289,30 +289,32 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
 #pragma unroll
                 for (int o = R_ / 2; o >= 1; o >>= 1) part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
                 const float sc = (k * TS + my_tok < len) ? part[0] : -INFINITY;
-                // per-head step maximum: lanes of one head differ only in the token bits
-                float bm = sc;
+                // Online softmax.  The running maxima change only when some score exceeds
+                // its head's: then (always on a segment's first step) the step maximum
+                // per head moves m and rescales the sums; otherwise the step skips it.
+                if (__any_sync(0xffffffffu, sc > my_m)) {
+                    // per-head step maximum: lanes of one head differ in the token bits
+                    float bm = sc;
 #pragma unroll
-                for (int o = R_ * G; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-                float mnew[G], corr[G], my_m = 0.0f;
+                    for (int o = R_ * G; o < 32; o <<= 1)
+                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    mnew[hh] = fmaxf(m[hh], __shfl_sync(0xffffffffu, bm, hh * R_));
-                    corr[hh] = exp2_approx(m[hh] - mnew[hh]);  // 0 on the first step (m = -inf)
-                    if ((int)my_head == hh) my_m = mnew[hh];
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float mnew = fmaxf(m[hh], __shfl_sync(0xffffffffu, bm, hh * R_));
+                        const float corr = exp2_approx(m[hh] - mnew);  // 0 when m = -inf
+                        m[hh] = mnew;
+                        const f2 c2 = pack2(corr, corr);
+#pragma unroll
+                        for (int e = 0; e < E / 2; ++e) acc[hh][e] = mul2(acc[hh][e], c2);
+                        if ((int)my_head == hh) {
+                            lp *= corr;
+                            my_m = mnew;
+                        }
+                    }
                 }
                 const float p = exp2_approx(sc - my_m);  // 0 for tokens past the sequence
+                lp += p;  // this lane's share of its head's weight sum
                 if (lane % R_ == 0) wbuf[lx] = pack2(p, p);
-                float ps = p;
-#pragma unroll
-                for (int o = R_ * G; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    l[hh] = l[hh] * corr[hh] + __shfl_sync(0xffffffffu, ps, hh * R_);
-                    m[hh] = mnew[hh];
-                    const f2 c2 = pack2(corr[hh], corr[hh]);
-#pragma unroll
-                    for (int e = 0; e < E / 2; ++e) acc[hh][e] = mul2(acc[hh][e], c2);
-                }
                 __syncwarp();  // the weights are in wbuf
 #pragma unroll
                 for (int i = 0; i < TS; ++i) {
@@ -328,12 +330,16 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
                 }
                 __syncwarp();  // the stage and wbuf are rewritten by later steps
             }
-            // the segment's record
+            // the segment's record; each head's weight sum from its lanes' shares
+            // (lanes of one head differ in the token bits; the low bits are copies)
+#pragma unroll
+            for (int o = R_ * G; o < 32; o <<= 1) lp += __shfl_xor_sync(0xffffffffu, lp, o);
             const uint64_t row0 = ((s + v) * a.Hkv + g) * G;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
+                const float lh = __shfl_sync(0xffffffffu, lp, hh * R_);
                 if (lane == 0)
-                    reinterpret_cast<float2*>(a.part_ml)[row0 + hh] = make_float2(m[hh], l[hh]);
+                    reinterpret_cast<float2*>(a.part_ml)[row0 + hh] = make_float2(m[hh], lh);
                 f2* o = reinterpret_cast<f2*>(a.part_acc + (row0 + hh) * D + lane * E);
 #pragma unroll
                 for (int e = 0; e < E / 2; ++e) o[e] = acc[hh][e];

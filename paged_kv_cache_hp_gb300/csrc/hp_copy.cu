@@ -480,9 +480,13 @@ int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* 
 #ifndef HP_BULK_MIN_UNIT
 #define HP_BULK_MIN_UNIT 16384
 #endif
+#ifndef HP_BULK_BIG_STAGES_BELOW
+#define HP_BULK_BIG_STAGES_BELOW 65536
+#endif
 #ifndef HP_COPY_ENGINE_LDG
     if (vec == 16 && mode != kDequant && a.unit_bytes >= HP_BULK_MIN_UNIT)
-        return launch_bulk(mode, index_u64, a, a.unit_bytes < 65536 ? 1 : 0, stream);
+        return launch_bulk(mode, index_u64, a, a.unit_bytes < HP_BULK_BIG_STAGES_BELOW ? 1 : 0,
+                           stream);
 #endif
     switch (mode) {
     case kGather:
