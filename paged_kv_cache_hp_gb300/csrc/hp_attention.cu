@@ -23,9 +23,11 @@
 //                   [l*E, l*E+E) (E = D/32).  The TS*G (token, query head) partial dot
 //                   products of a step are summed across the warp with a transposed
 //                   butterfly (one shuffle per product), then an online softmax per query
-//                   head updates the running max, sum and the lane's E dims of the weighted
-//                   value sum.  Each segment leaves (max, sum, acc[D]) per query head as
-//                   record (s + v) * H_kv + g, v the warp's worker index.
+//                   head updates the lane's E dims of the weighted value sum; the running
+//                   maxima move (and the sums are rescaled) only on steps where some score
+//                   exceeds its head's, and each lane keeps its share of its head's weight
+//                   sum.  Each segment leaves (max, sum, acc[D]) per query head as record
+//                   (s + v) * H_kv + g, v the warp's worker index.
 //   combine_kernel  one warp per (sequence, query head) merges its segments' records.
 // Records: acc [records, G, D] and (max, sum) [records, G] in the workspace after the plan.
 #include <cuda_bf16.h>
@@ -184,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
     f2* wbuf = reinterpret_cast<f2*>(ring + kStages * S::STAGE);
     const unsigned short* Q = static_cast<const unsigned short*>(a.q);
     const uint64_t D = a.D;
-    // After the reduction lane l holds slot lx = l / R: token lx / G, head lx % G of the
-    // step.  Before it, lane l keeps slot k ^ lx at array position k, so every level of
+    // After the reduction lane l holds slot lx = l / R_ (R_ lanes per slot): token lx / G,
+    // head lx % G of the step.  Before it, lane l keeps slot k ^ lx at array position k, so every level of
     // the transposed butterfly keeps the low half and sends the high half: position k
     // reads K row (k / G) ^ lt with query head (k % G) ^ lh.
     const unsigned lx = lane / R_, my_tok = lx / G, my_head = lx % G;
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
 
     const uint64_t S_steps = a.hdr->total_units;  // steps of all sequences, one head
     const uint64_t Lw = (S_steps + a.workers - 1) / a.workers;
-    const uint32_t R = a.R;
+    const uint32_t R = a.R;                                 // step ranges per CTA
     const uint32_t r = a.Hkv >= kWarps ? 0 : warp / a.Hkv;  // this warp's sub-range
     if (r >= R || S_steps == 0) return;  // whole warp; no block-wide barrier in this kernel
     const uint64_t v = (uint64_t)blockIdx.x * R + r;       // worker index
