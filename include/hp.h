@@ -116,6 +116,12 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
 #define HP_PERMISSIVE 0x1u /* [HF] Storage Invariants: a reader in permissive mode does not
                               reject descriptors that violate invariants (1)-(3)          */
 #define HP_HAS_QUANT 0x2u  /* [HF] Buffer Table: quantisation parameters present          */
+/* Test hook for the bounded waits (no counterpart in the pages): the TMA copy engine sets
+ * up the first load of each of its CTAs but never issues it, so the wait for it runs out
+ * (after about 2 s), the call stores HP_ERR_TIMEOUT in *d_status and returns without
+ * copying the rest.  Only a gather or append that takes the TMA engine (16-byte rows and
+ * bases, copy units of 16 KiB or more) sees it; never set it outside tests. */
+#define HP_TEST_STALL 0x100u
 
 /*
  * A block-paged descriptor ([HF] Buffer Table, Additional Descriptor Fields):
@@ -145,7 +151,7 @@ typedef struct hp_paged_desc {
     uint32_t rank;
     uint32_t paged_axis;
     uint32_t has_shard;
-    uint32_t flags;        /* HP_PERMISSIVE | HP_HAS_QUANT */
+    uint32_t flags;        /* HP_PERMISSIVE | HP_HAS_QUANT (| HP_TEST_STALL in tests) */
     uint32_t dtype;        /* hp_dtype */
     uint32_t index_type;   /* hp_index_type */
     uint64_t num_pages;

@@ -134,6 +134,7 @@ hp::CopyArgs copy_args(const hp_paged_desc* d, const void* ws, int* d_status)
     a.row_bytes = row_bytes_of(d);
     a.row_elems = d->num_heads * d->head_dim;
     a.unit_bytes = d->page_size * a.row_bytes;
+    a.test_stall = (d->flags & HP_TEST_STALL) != 0;
     a.d_status = d_status;
     return a;
 }

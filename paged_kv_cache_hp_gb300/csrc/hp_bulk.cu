@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const CopyArgs a)
             chunk_bytes[st] = bytes;
             const uint32_t bar = smem_u32(&stage_bar[st]);
             mbar_expect_tx(bar, bytes);
-            bulk_load(ring0 + st * kStage, a.src + desc.src[buf][li] + loff, bytes, bar);
+            if (!(a.test_stall && L == 0))  // HP_TEST_STALL: the first load is never issued
+                bulk_load(ring0 + st * kStage, a.src + desc.src[buf][li] + loff, bytes, bar);
             ++L;
             loff += bytes;
         }
@@ -249,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_kernel(const CopyArgs a)
     }
     if (!ok) {
         report(a.d_status, HP_ERR_TIMEOUT);
-        for (; S < L; ++S)  // let the loads in flight land before the CTA's shared memory goes
-            if (!mbar_wait(smem_u32(&stage_bar[S % kStages]), (uint32_t)((S / kStages) & 1))) break;
+        // let every load in flight land before the CTA's shared memory goes (each wait
+        // bounded; a stage that never completes costs one more wait limit)
+        for (; S < L; ++S)
+            mbar_wait(smem_u32(&stage_bar[S % kStages]), (uint32_t)((S / kStages) & 1));
     }
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }

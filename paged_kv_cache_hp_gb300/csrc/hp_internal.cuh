@@ -180,6 +180,7 @@ struct CopyArgs {
     uint32_t q_hd_m, q_hd_l;  // divide a group-in-row index by q_gph
     uint64_t q_head_dim;
     int q_fixed;              // per channel: q_gpr divides the CTA width (a power of two)
+    int test_stall;           // HP_TEST_STALL: the TMA engine never issues its first load
     int* d_status;
 };
 

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "libhp.so")
 HP_OK = 0
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "u8": 4, "f64": 5}
 IDX_U32, IDX_U64 = 0, 1
-PERMISSIVE, HAS_QUANT = 0x1, 0x2
+PERMISSIVE, HAS_QUANT, TEST_STALL = 0x1, 0x2, 0x100
 
 _lock = threading.Lock()
 _lib = None
