@@ -603,6 +603,11 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     out["tiny_prefix_gather"]["us_per_step_l2_cold"] = round(
         1e3 * med_ms(lambda: (st.plan(stream), st.copy(stream)), between=cold), 2)
     st.check_status()
+    # the same gather as one hp_gather call: a small validated batch takes the one-launch
+    # path (plan, table check and copy in one kernel)
+    out["tiny_prefix_gather_one_call"] = step_us(
+        lambda: hp.hp_gather(st.desc, st.out, st.T, st.ws, st.status))
+    st.check_status()
     del st
 
     # prefix sharing at scale

@@ -209,7 +209,9 @@ int hp_plan(const hp_paged_desc* desc, uint64_t out_tokens, void* workspace,
  * page_pool[((phys*page_size + t % page_size)*num_heads + h)*head_dim + d] with
  * phys = block_table[seq_ptr[s] + t / page_size] ([HF] Element Lookup).
  * Elements are copied as bytes.  No slot past a sequence's token count is read
- * ([HF] Partial trailing page).  Equivalent to hp_plan then hp_gather_planned.
+ * ([HF] Partial trailing page).  Equivalent to hp_plan then hp_gather_planned
+ * (same verdicts, same workspace contents); a validated batch of at most 1024
+ * sequences, 8192 table entries and 8 MiB of pages runs as a single kernel.
  * `out` must be 16-byte aligned for the vector path (any alignment works).
  */
 int hp_gather(const hp_paged_desc* desc, void* out, uint64_t out_tokens, void* workspace,

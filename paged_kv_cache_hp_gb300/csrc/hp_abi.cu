@@ -14,6 +14,7 @@
 
 #include "hp_attn.cuh"
 #include "hp_internal.cuh"
+#include "hp_small.cuh"
 
 #define HP_API extern "C" __attribute__((visibility("default")))
 
@@ -422,6 +423,33 @@ HP_API int hp_gather(const hp_paged_desc* desc, void* out, uint64_t out_tokens, 
     int rc = check_desc(desc);
     if (rc) return rc;
     if (out_tokens && !out) return HP_ERR_NULL;
+    const hp_paged_desc* d = desc;
+    if (!(d->flags & (HP_PERMISSIVE | HP_TEST_STALL)) && d->num_seqs <= hp::kMaxSeqs &&
+        d->table_len <= hp::kMaxTable &&
+        (u128)d->table_len * d->page_size * row_bytes_of(d) <= hp::kMaxBytes) {
+        // a small validated batch: plan, table check and copy in one launch
+        rc = check_ws(d, workspace, workspace_bytes);
+        if (rc) return rc;
+        if (((u128)out_tokens * row_bytes_of(d)) >> 64) return HP_ERR_OUT_SIZE;
+        hp::SmallGatherArgs a{};
+        a.seq_ptr = d->seq_ptr;
+        a.lens = d->seq_lens;
+        a.table = d->block_table;
+        a.pool = static_cast<const char*>(d->page_pool);
+        a.out = static_cast<char*>(out);
+        a.num_seqs = d->num_seqs;
+        a.page_size = d->page_size;
+        a.table_len = d->table_len;
+        a.num_pages = d->num_pages;
+        a.row_bytes = row_bytes_of(d);
+        a.out_tokens = out_tokens;
+        a.ws = hp::ws_view(workspace, d->num_seqs);
+        a.d_status = d_status;
+        if (!a.pool) a.pool = static_cast<const char*>(out);  // no pages: never read
+        if (!a.out) a.out = static_cast<char*>(const_cast<void*>(d->page_pool));  // no rows
+        return hp::launch_small_gather(d->index_type == HP_IDX_U64, a,
+                                       pick_vec(a.row_bytes, d->page_pool, out), stream);
+    }
     rc = plan_gather(desc, out_tokens, workspace, workspace_bytes, d_status, stream, true);
     if (rc) return rc;
     return gather_planned(desc, out, workspace, d_status, stream, false);

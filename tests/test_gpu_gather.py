@@ -306,3 +306,53 @@ def test_planned_steps_equal_one_call(hp, oracle):
         assert hp.hp_gather_planned(b.desc, out2, ws2, None, stream=s) == 0
     torch.cuda.synchronize()
     assert torch.equal(out1, out2)
+
+
+def test_one_launch_gather_random_verdicts_and_rows(hp, oracle):
+    """Small validated batches take the one-launch gather: on random small descriptors,
+    valid and invalid, its status is the oracle's rule, the verdict key it leaves in the
+    workspace names the oracle's first failing index, and a valid batch gathers the
+    oracle's rows."""
+    import torch
+    rng = np.random.default_rng(33)
+    ranks = {"SEQ_PTR_START": 1, "SEQ_PTR_ORDER": 2, "SEQ_PTR_END": 3, "PAGE_ID": 4, "LEN": 5}
+    seen = set()
+    for trial in range(200):
+        S = int(rng.integers(0, 6))
+        tlen = int(rng.integers(0, 8))
+        N = int(rng.integers(1, 6))
+        if S == 0:
+            seq_ptr = np.array([0 if trial % 2 else tlen])
+        else:
+            inner = np.sort(rng.integers(0, tlen + 1, S - 1))
+            seq_ptr = np.concatenate([[0], inner, [tlen]])
+        if trial % 3 == 0:
+            seq_ptr = rng.integers(0, 5, S + 1)
+        table = rng.integers(0, N + (trial % 4 == 0), tlen)
+        slices = np.maximum(np.diff(seq_ptr), 0)
+        lens = np.array([rng.integers(0, 2 * k + 2) for k in slices], dtype=np.int64)
+        it = trial % 2
+        pool_h = rng.integers(0, 256, N * 2 * 4, dtype=np.uint8)
+        pool = torch.from_numpy(pool_h).to("cuda")
+        kw = dict(num_pages=N, page_size=2, num_heads=1, head_dim=4, dtype="i8")
+        d = _mk(hp, pool, list(table), list(seq_ptr), list(lens), it=it, **kw)
+        ws = hp.workspace_for(d)
+        T = int(lens.sum())
+        buf, out = guarded(T * 4)
+        st = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+        assert hp.hp_gather(d, out, T, ws, st) == 0
+        torch.cuda.synchronize()
+        od = oracle.Desc(pool_h, list(table) if tlen else None, list(seq_ptr), list(lens),
+                         index_type=it, **kw)
+        code, first = od.validate()
+        seen.add(code)
+        assert hp.status_name(st.item()) == lib_name(code), (seq_ptr, table, lens)
+        key = int(ws[:8].cpu().numpy().view(np.uint64)[0])
+        if code == "OK":
+            assert key == (1 << 64) - 1
+            want = od.gather()[0].reshape(-1)
+            assert np.array_equal(out.cpu().numpy()[:T * 4], want)
+        else:
+            assert (key >> 58, key & ((1 << 58) - 1)) == (ranks[code], first)
+            assert (buf.cpu().numpy() == 0xEE).all()
+    assert {"OK", "SEQ_PTR_START", "SEQ_PTR_ORDER", "SEQ_PTR_END", "PAGE_ID", "LEN"} <= seen
