@@ -119,8 +119,9 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
 /* Test hook for the bounded waits (no counterpart in the pages): the TMA copy engine sets
  * up the first load of each of its CTAs but never issues it, so the wait for it runs out
  * (after about 2 s), the call stores HP_ERR_TIMEOUT in *d_status and returns without
- * copying the rest.  Only a gather or append that takes the TMA engine (16-byte rows and
- * bases, copy units of 16 KiB or more) sees it; never set it outside tests. */
+ * copying the rest.  Only a gather that takes the TMA engine (16-byte rows and bases,
+ * copy units of 16 KiB or more, a batch too large for the one-launch path) sees it;
+ * never set it outside tests. */
 #define HP_TEST_STALL 0x100u
 
 /*

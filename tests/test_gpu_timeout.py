@@ -13,10 +13,14 @@ from paged_kv_cache_hp_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_bulk_gather_times_out_and_the_context_survives(hp, oracle):
+@pytest.mark.parametrize("heads", [32, 8])
+def test_stalled_bulk_gather_times_out_and_the_context_survives(hp, oracle, heads):
+    """32 heads: rows of 8 KiB, 128 KiB copy units (the one-thread producer with 8 KiB
+    stages); 8 heads: rows of 2 KiB, 32 KiB units (loader and storer threads with 32 KiB
+    stages).  Both batches are too large for the one-launch path."""
     import torch
-    # 8 KiB rows in pages of 16: 128 KiB copy units, the TMA engine's territory
-    w = inputs.config("decode_gather", "small")
+    w = inputs.decode_gather(seed=12, num_pages=1200, num_heads=heads, head_dim=128,
+                             num_seqs=9, len_lo=400, len_hi=1400, dtype="f16")
     b = Batch(w, flags=hp.TEST_STALL)
     out = torch.full((w.total_tokens * w.row_bytes,), 0xEE, dtype=torch.uint8, device="cuda")
     t0 = time.time()
