@@ -5,8 +5,9 @@ Tolerance, derived from the fp32 path: each output is a convex combination of va
 so |out| <= max|V|; the kernel's errors come from fp32 dot products of head_dim terms,
 a base-2 exponential with relative error below 2^-22, and fp32 accumulation over the
 weighted rows of each sequence segment plus the merge of the segments' records -- a
-relative error well under 1e-3 of max|V| (about n * 2^-24 for n terms in the worst
-case).  The bar is |gpu - oracle| <= 1e-3 * max|V| + 1e-6 per element."""
+relative error well under 1e-4 of max|V| (about n * 2^-24 for n terms in the worst
+case; measured on GB300: 1e-8 to 3e-8 of max|V|, 2e-6 with a peaked softmax).  The bar is
+|gpu - oracle| <= 1e-4 * max|V| + 1e-6 per element."""
 import numpy as np
 import pytest
 
@@ -40,7 +41,7 @@ def _run(hp, oracle, w, Hq, seed, scale=None):
 
 
 def _check(got, want, vmax):
-    tol = 1e-3 * vmax + 1e-6
+    tol = 1e-4 * vmax + 1e-6
     err = np.abs(got - want)
     assert np.all(np.isfinite(got)) and err.max() <= tol, (err.max(), tol)
 
