@@ -468,6 +468,27 @@ def attention_only(scale, dev, hp, inputs, peak, reps):
     return res
 
 
+def lane_only(dev, hp, inputs, peak, reps):
+    """The per-lane snapshot gather of the lane_synthetic layout ([512, 32, 8, 16, 128]
+    bf16, 256 lanes of about 6,555 rows)."""
+    import torch
+    lw = inputs.lane_synthetic()
+    g = torch.Generator(device=dev)
+    g.manual_seed(lw.seed)
+    lpool = torch.randn(lw.pool_shape, generator=g, device=dev).to(torch.bfloat16)
+    lt = torch.from_numpy(lw.table.view(np.int64).copy()).to(dev)
+    lo = torch.empty((lw.batch, lw.kv_heads, lw.n, lw.width), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    ms = median_ms(lambda: hp.hp_lane_gather(lpool, lt, lw.capacity, lw.page_tokens, lw.batch,
+                                             lw.kv_heads, lw.width, "bf16", lw.n, lo, status),
+                   stream, reps)
+    assert int(status.item()) == 0
+    res = rate_entry(2 * lw.lanes * lw.n * lw.width * 2 + lw.pages * 8, ms, peak)
+    res.update(op="lane_gather", lanes=lw.lanes, rows=lw.n)
+    return res
+
+
 def decode_step_only(dev, hp, inputs, steps):
     """The decode append step alone (one new row for each of 256 sequences of the
     decode_append batch), validated and permissive, issued back to back."""
@@ -765,11 +786,21 @@ def main():
                     help="time only the two cache layout conversions (kernel-internal "
                          "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
                          "and print their line")
+    ap.add_argument("--lane", action="store_true",
+                    help="time only the per-lane snapshot gather (256 lanes of the "
+                         "lane_synthetic layout) and print its line")
     ap.add_argument("--decode-step", action="store_true",
                     help="issue --steps decode append steps (256 rows into the decode_append "
                          "pool), validated and then permissive, and print their timing")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.lane:
+        import torch
+        from paged_kv_cache_hp_gb300 import build, hp, inputs
+        build.build()
+        hp.lib()
+        print(json.dumps(lane_only("cuda", hp, inputs, peak_hbm()[0], args.steps)))
+        return
     if args.decode_step:
         import torch
         from paged_kv_cache_hp_gb300 import build, hp, inputs
