@@ -426,7 +426,10 @@ def release_device_memory():
 
 def median_ms(fn, stream, n=20, warm=3, between=None):
     """Median of n CUDA-event timings of fn() on `stream`, after `warm` untimed calls;
-    `between` (untimed) runs before each timed call, e.g. an L2 scrub."""
+    `between` (untimed) runs before each timed call, e.g. an L2 scrub.  A spin kernel of
+    about 0.1 ms (no memory traffic) precedes each timed call, so the launches of fn() are
+    queued by the time the first event fires: the time is the device's, as in a loop that
+    keeps the queue full, not the host's launch latency."""
     import torch
     for _ in range(warm):
         fn()
@@ -435,6 +438,8 @@ def median_ms(fn, stream, n=20, warm=3, between=None):
     for _ in range(n):
         if between is not None:
             between()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(200000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -491,7 +496,8 @@ def lane_only(dev, hp, inputs, peak, reps):
 
 def decode_step_only(dev, hp, inputs, steps):
     """The decode append step alone (one new row for each of 256 sequences of the
-    decode_append batch), validated and permissive, issued back to back."""
+    decode_append batch), validated and permissive, issued back to back; then the
+    zeroing of the grown batch's dead slots."""
     import torch
     w = inputs.config("decode_append")
     pool = inputs.device_pool(w, dev)
@@ -518,6 +524,21 @@ def decode_step_only(dev, hp, inputs, steps):
         torch.cuda.synchronize()
         assert int(status.item()) == 0, hp.status_name(int(status.item()))
         res[name + "_us_back_to_back"] = round(a.elapsed_time(b) / steps * 1e3, 2)
+    # zeroing the slots past every sequence's count after the step (273k table entries)
+    d = hp.PagedDesc(pool, table, sp, idx_tensor(w.lens, dev), **kw)
+    ws = hp.workspace_for(d, dev)
+    rc, nsc = hp.hp_zero_tails_scratch_bytes(d)
+    scratch = torch.empty(nsc, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        hp.hp_zero_tails(d, ws, scratch, status)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        hp.hp_zero_tails(d, ws, scratch, status)
+    b.record(stream)
+    torch.cuda.synchronize()
+    res["zero_tails_us_back_to_back"] = round(a.elapsed_time(b) / steps * 1e3, 2)
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
     return res
 
 

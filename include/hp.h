@@ -369,8 +369,8 @@ int hp_zero_tails(const hp_paged_desc* desc, void* workspace, uint64_t workspace
  * Bytes of device workspace hp_attention_decode needs: the plan's (hp_workspace_bytes)
  * plus fp32 records (max, sum and head_dim accumulators per query head) for up to
  * (num_seqs + HP_ATTN_MAX_CTAS * R) * num_heads sequence segments, R = 8 / num_heads
- * when num_heads < 8, else 1.  It depends only on the descriptor's num_seqs, num_heads
- * and head_dim, and on num_q_heads.
+ * when num_heads < 8, else 1, plus a 4-byte count per (sequence, K/V head).  It depends
+ * only on the descriptor's num_seqs, num_heads and head_dim, and on num_q_heads.
  */
 #define HP_ATTN_MAX_CTAS 512
 int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t num_q_heads,

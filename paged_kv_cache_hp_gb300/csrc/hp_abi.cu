@@ -645,8 +645,9 @@ int attention_ws(const hp_paged_desc* d, uint32_t hq, u64* bytes)
     int rc = ws_bytes(d, &plan);
     if (rc) return rc;
     const u128 part = (u128)attn_records(d) * (hq / d->num_heads) * (d->head_dim + 2) * 4;
-    if ((part + plan) >> 64) return HP_ERR_OVERFLOW;
-    *bytes = plan + (u64)part;
+    const u128 counts = (u128)d->num_seqs * d->num_heads * 4;
+    if ((part + plan + counts) >> 64) return HP_ERR_OVERFLOW;
+    *bytes = plan + (u64)part + (u64)counts;
     return HP_OK;
 }
 
@@ -683,6 +684,12 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     ws_bytes(d, &plan_bytes);
     hp::PlanArgs pa = plan_args(d, workspace, d_status);
     pa.step_tokens = attn_step_tokens(G, d->head_dim);
+    char* part = static_cast<char*>(workspace) + plan_bytes;
+    const u64 part_bytes = attn_records(d) * G * (d->head_dim + 2) * 4;
+    unsigned* seg_done = reinterpret_cast<unsigned*>(part + part_bytes);
+    if (d->num_seqs && cudaMemsetAsync(seg_done, 0, 4 * d->num_seqs * d->num_heads,
+                                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return HP_ERR_CUDA;
     rc = hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
     if (rc || d->num_seqs == 0) return rc;
     hp::AttnArgs a{};
@@ -705,8 +712,9 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     a.scale = scale;
     a.hdr = pa.ws.hdr;
     a.units_off = pa.ws.units_off;
-    a.part_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes);
+    a.part_acc = reinterpret_cast<float*>(part);
     a.part_ml = a.part_acc + attn_records(d) * G * d->head_dim;
+    a.seg_done = seg_done;
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
     a.d_status = d_status;

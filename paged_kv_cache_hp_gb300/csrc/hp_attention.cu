@@ -26,10 +26,14 @@
 //                   head updates the lane's E dims of the weighted value sum; the running
 //                   maxima move (and the sums are rescaled) only on steps where some score
 //                   exceeds its head's, and each lane keeps its share of its head's weight
-//                   sum.  Each segment leaves (max, sum, acc[D]) per query head as record
-//                   (s + v) * H_kv + g, v the warp's worker index.
-//   combine_kernel  one warp per (sequence, query head) merges its segments' records.
-// Records: acc [records, G, D] and (max, sum) [records, G] in the workspace after the plan.
+//                   sum.  A warp that covers a whole sequence writes its normalised
+//                   result.  Otherwise each segment leaves (max, sum, acc[D]) per query
+//                   head as record (s + v) * H_kv + g, v the warp's worker index, and
+//                   counts itself done for (s, g); the warp that finishes the last
+//                   segment merges the records into the result, so no second kernel and
+//                   no pass over the sequences follow.
+// Records: acc [records, G, D] and (max, sum) [records, G] in the workspace after the
+// plan, then one count per (sequence, K/V head), zeroed before the launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -51,12 +55,6 @@ template <int E> struct Pack;
 template <> struct Pack<2> { using T = unsigned int; };
 template <> struct Pack<4> { using T = uint2; };
 template <> struct Pack<8> { using T = uint4; };
-
-template <int EV> struct FVec;
-template <> struct FVec<2> { using T = float2; };
-template <> struct FVec<4> { using T = float4; };
-struct __align__(16) Float8 { float4 lo, hi; };
-template <> struct FVec<8> { using T = Float8; };
 
 // Geometry of one step for G query heads per K/V head and E = D/32 dims per lane.
 template <int G, int E> struct Step {
@@ -170,6 +168,92 @@ __device__ __forceinline__ void issue_step(const AttnArgs& a, unsigned char* sta
     }
 }
 
+// E floats of a record written earlier in this launch by another warp (L2, not L1).
+template <int E>
+__device__ __forceinline__ void load_dims(const float* p, float (&x)[E])
+{
+    if constexpr (E == 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+        x[0] = v.x;
+        x[1] = v.y;
+    } else {
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p) + k);
+            x[4 * k] = v.x;
+            x[4 * k + 1] = v.y;
+            x[4 * k + 2] = v.z;
+            x[4 * k + 3] = v.w;
+        }
+    }
+}
+
+// Merges the nr segment records of one (sequence, K/V head) -- record j's query head hh
+// at row row0 + j * H_kv * G + hh -- into the G normalised results at out + hh * D (the
+// lane's E dims).  The maxima and weight sums first: lane l takes head l % G of records
+// l / G, l / G + 32 / G, ... with a running (max, sum), and the lanes of a head merge
+// theirs pairwise; then the weighted accumulators, CH records at a time.
+template <int G, int E>
+__device__ __forceinline__ void merge_segments(const AttnArgs& a, uint64_t row0, uint64_t nr,
+                                            float* out, unsigned lane)
+{
+    constexpr int CH = G >= 8 ? 1 : 8 / G;  // records per pass of the accumulator loop
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+    const uint64_t stride = (uint64_t)a.Hkv * G, D = a.D;
+    float mx = -INFINITY, sm = 0.0f;
+    for (uint64_t j = lane / G; j < nr; j += 32 / G) {
+        const float2 x = __ldcg(ml + row0 + j * stride + lane % G);  // x.x finite
+        const float mn = fmaxf(mx, x.x);
+        sm = sm * exp2_approx(mx - mn) + x.y * exp2_approx(x.x - mn);
+        mx = mn;
+    }
+#pragma unroll
+    for (int o = G; o < 32; o <<= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+        const float os = __shfl_xor_sync(0xffffffffu, sm, o);
+        const float mn = fmaxf(mx, om);
+        if (mn != -INFINITY) {
+            sm = sm * exp2_approx(mx - mn) + os * exp2_approx(om - mn);
+            mx = mn;
+        }
+    }
+    float M[G], acc[G][E];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        M[hh] = __shfl_sync(0xffffffffu, mx, hh);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[hh][e] = 0.0f;
+    }
+    const float L = sm;  // lane hh < G holds head hh's sum
+    for (uint64_t j = 0; j < nr; j += CH) {
+        float x[CH][G][E], w[CH][G];
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const uint64_t row = row0 + (j + c < nr ? j + c : j) * stride + hh;
+                load_dims<E>(a.part_acc + row * D + lane * E, x[c][hh]);
+                w[c][hh] = j + c < nr ? __ldcg(ml + row).x : -INFINITY;
+            }
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float wt = exp2_approx(w[c][hh] - M[hh]);  // 0 past the last record
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[hh][e] = fmaf(wt, x[c][hh][e], acc[hh][e]);
+            }
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        const float inv = 1.0f / __shfl_sync(0xffffffffu, L, hh);
+        float* o = out + hh * D;
+#pragma unroll
+        for (int e = 0; e < E; e += 2)
+            *reinterpret_cast<float2*>(o + e) = make_float2(acc[hh][e] * inv, acc[hh][e + 1] * inv);
+    }
+}
+
 // G = 8 query heads at D >= 128 keep 64 to 128 fp32 query and accumulator values per
 // lane: those variants run one CTA per SM with the registers they need instead of spilling.
 template <typename IndexT, bool BF16, int G, int E>
@@ -182,6 +266,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
     pdl_wait();  // the plan before this launch is complete
     if (a.hdr->verdict != kVerdictOk) return;
     const unsigned warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a sequence without tokens has no step: one warp of the grid writes its zeros
+    for (uint64_t s = (uint64_t)blockIdx.x * kWarps + warp; s < a.num_seqs;
+         s += (uint64_t)gridDim.x * kWarps)
+        if (a.units_off[s] == a.units_off[s + 1]) {
+            float4* o = reinterpret_cast<float4*>(a.out + s * a.Hq * a.D);
+            for (uint64_t i = lane; i < a.Hq * a.D / 4; i += 32) o[i] = make_float4(0, 0, 0, 0);
+        }
     unsigned char* ring = smem + warp * S::WARP_SMEM;
     f2* wbuf = reinterpret_cast<f2*>(ring + kStages * S::STAGE);
     const unsigned short* Q = static_cast<const unsigned short*>(a.q);
@@ -215,6 +306,26 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
     const uint64_t s_first = find_seq(a.units_off, a.num_seqs, beg);
     for (uint32_t g = a.Hkv >= kWarps ? warp : warp % a.Hkv; g < a.Hkv;
          g += a.Hkv >= kWarps ? kWarps : a.Hkv) {
+        // A segment's count of (sequence, head) -- and, for its last segment, the merge --
+        // waits until the next segment's first loads are in flight.
+        uint64_t pend = ~0ull;  // the sequence of the record waiting to be counted
+        auto settle = [&]() {
+            if (pend == ~0ull) return;
+            __threadfence();  // the record is visible before the count moves
+            __syncwarp();
+            unsigned done = 0;
+            if (lane == 0) done = atomicAdd(a.seg_done + pend * a.Hkv + g, 1u);
+            done = __shfl_sync(0xffffffffu, done, 0);
+            const uint64_t so = a.units_off[pend], ns = a.units_off[pend + 1] - so;
+            const uint64_t f = so / Lw, nr = (so + ns - 1) / Lw - f + 1;
+            if (done + 1 == nr) {
+                __threadfence();  // every other segment's record is visible
+                merge_segments<G, E>(a, ((pend + f) * a.Hkv + g) * G, nr,
+                                     a.out + (pend * a.Hq + (uint64_t)g * G) * D + lane * E,
+                                     lane);
+            }
+            pend = ~0ull;
+        };
         uint64_t s = s_first;
         for (uint64_t pos = beg; pos < end;) {
             while (a.units_off[s + 1] <= pos) ++s;  // skips sequences without steps
@@ -242,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
                 if (k0 + j < k1) issue(k0 + j, ring + j * S::STAGE);
                 cp_async_commit();
             }
+            settle();  // the previous segment's count, behind this one's first loads
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
                 const RowT raw = __ldg(reinterpret_cast<const RowT*>(
@@ -332,10 +444,26 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
                 }
                 __syncwarp();  // the stage and wbuf are rewritten by later steps
             }
-            // the segment's record; each head's weight sum from its lanes' shares
-            // (lanes of one head differ in the token bits; the low bits are copies)
+            // each head's weight sum from its lanes' shares (lanes of one head differ in
+            // the token bits; the low bits are copies)
 #pragma unroll
             for (int o = R_ * G; o < 32; o <<= 1) lp += __shfl_xor_sync(0xffffffffu, lp, o);
+            // the sequence's steps met workers f .. f + nr - 1 (equal shares of Lw steps)
+            const uint64_t ns = a.units_off[s + 1] - so;
+            const uint64_t f = so / Lw, nr = (so + ns - 1) / Lw - f + 1;
+            float* out = a.out + (s * a.Hq + (uint64_t)g * G) * D + lane * E;
+            if (nr == 1) {  // the whole sequence: its result, normalised
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float inv = 1.0f / __shfl_sync(0xffffffffu, lp, hh * R_);
+                    f2* o = reinterpret_cast<f2*>(out + hh * D);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) o[e] = mul2(acc[hh][e], pack2(inv, inv));
+                }
+                continue;
+            }
+            // one segment of several: its record now, its count later (settle); the warp
+            // that finishes the last one merges them all
             const uint64_t row0 = ((s + v) * a.Hkv + g) * G;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
@@ -346,80 +474,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
 #pragma unroll
                 for (int e = 0; e < E / 2; ++e) o[e] = acc[hh][e];
             }
+            pend = s;
         }
-    }
-}
-
-// One warp per (sequence, query head) merges its segments' records: the sequence's steps
-// [SO, SO + n) met workers f = SO / Lw .. l = (SO + n - 1) / Lw, and worker v left record
-// (s + v) * H_kv + g.  The maximum and the rescaled sum over the records with the lanes
-// striding them, then the weighted accumulators with each lane owning EV = D/32 dims
-// (vector loads, four records in flight).
-template <int EV>
-__global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a)
-{
-    using VT = typename FVec<EV>::T;  // EV floats
-    pdl_wait();
-    if (a.hdr->verdict != kVerdictOk) return;
-    const unsigned lane = threadIdx.x & 31;
-    const uint64_t pairs = a.num_seqs * a.Hq, D = a.D, G = a.G;
-    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
-    const uint64_t S_steps = a.hdr->total_units;
-    const uint64_t Lw = S_steps ? (S_steps + a.workers - 1) / a.workers : 1;
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-    for (uint64_t w = (uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < pairs;
-         w += warps) {
-        const uint64_t s = w / a.Hq, qh = w - s * a.Hq, g = qh / G, hh = qh - g * G;
-        const uint64_t so = a.units_off[s], n = a.units_off[s + 1] - so;
-        float acc[EV];
-#pragma unroll
-        for (int e = 0; e < EV; ++e) acc[e] = 0.0f;
-        if (n > 0) {
-            const uint64_t f = so / Lw, nr = (so + n - 1) / Lw - f + 1;
-            // record j of this (sequence, query head): row ((s + f + j) * H_kv + g) * G + hh
-            const uint64_t row0 = ((s + f) * a.Hkv + g) * G + hh, stride = (uint64_t)a.Hkv * G;
-            float M = -INFINITY;
-            for (uint64_t j = lane; j < nr; j += 32) M = fmaxf(M, ml[row0 + j * stride].x);
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float L = 0.0f;
-            for (uint64_t j = lane; j < nr; j += 32) {
-                const float2 v = ml[row0 + j * stride];
-                L += v.y * exp2f(v.x - M);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            const float inv = 1.0f / L;
-            uint64_t j = 0;
-            for (; j + 4 <= nr; j += 4) {
-                VT v[4];
-                float wt[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t row = row0 + (j + k) * stride;
-                    v[k] = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
-                    wt[k] = ml[row].x;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float x = exp2f(wt[k] - M);
-                    const float* f4 = reinterpret_cast<const float*>(&v[k]);
-#pragma unroll
-                    for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f4[e], acc[e]);
-                }
-            }
-            for (; j < nr; ++j) {
-                const uint64_t row = row0 + j * stride;
-                const VT v = *reinterpret_cast<const VT*>(a.part_acc + row * D + lane * EV);
-                const float x = exp2f(ml[row].x - M);
-                const float* f4 = reinterpret_cast<const float*>(&v);
-#pragma unroll
-                for (int e = 0; e < EV; ++e) acc[e] = fmaf(x, f4[e], acc[e]);
-            }
-#pragma unroll
-            for (int e = 0; e < EV; ++e) acc[e] *= inv;
-        }
-        *reinterpret_cast<VT*>(a.out + w * D + lane * EV) = *reinterpret_cast<const VT*>(acc);
+        settle();
     }
 }
 
@@ -436,14 +493,8 @@ int launch_g(const AttnArgs& a, cudaStream_t st)
     AttnArgs b = a;
     const uint64_t ctas = std::min<uint64_t>((uint64_t)sms * per_sm, HP_ATTN_MAX_CTAS);
     b.workers = ctas * b.R;
-    if (launch_dependent(attn_kernel<IndexT, BF16, G, E>, (unsigned)ctas, kThreads, smem, st,
-                         b) != cudaSuccess)
-        return HP_ERR_CUDA;
-    uint64_t g2 = (a.num_seqs * a.Hq + 7) / 8;
-    const uint64_t cap = (uint64_t)sms * 8;
-    g2 = g2 == 0 ? 1 : (g2 < cap ? g2 : cap);
-    auto comb = E == 2 ? combine_kernel<2> : (E == 4 ? combine_kernel<4> : combine_kernel<8>);
-    return launch_dependent(comb, (unsigned)g2, 256, 0, st, b) == cudaSuccess
+    return launch_dependent(attn_kernel<IndexT, BF16, G, E>, (unsigned)ctas, kThreads, smem, st,
+                            b) == cudaSuccess
                ? HP_OK
                : HP_ERR_CUDA;
 }

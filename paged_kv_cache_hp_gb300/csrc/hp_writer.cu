@@ -8,8 +8,9 @@
 //                page holds, min(page_size, len_s - j*page_size) or 0; atomicMax into a
 //                per-page count, so a page shared by several sequences keeps what the
 //                longest of them uses (Prefix Sharing).
-//   zero_kernel  one warp per entry: the first entry naming a page claims it (bit 31 of
-//                its count) and zeroes the page's slots from that count to the end.
+//   zero_kernel  one thread per entry: the first entry naming a page claims it (bit 31
+//                of its count); the warp then zeroes, page by page, the slots from the
+//                count to the end of each page its lanes claimed that has any.
 // Pages no slice names are never touched.
 //
 // The decode-step append ("Block-Paged Layout -- Hurray Format Specification", Element
@@ -69,21 +70,32 @@ __global__ void __launch_bounds__(256) zero_kernel(const PlanArgs a, unsigned* l
     const unsigned lane = threadIdx.x & 31;
     const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
     const bool wide = row_bytes % 16 == 0;
-    for (uint64_t k = (uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-         k < a.table_len; k += warps) {
-        const uint64_t page = table[k];
-        unsigned old = 0;
-        if (lane == 0) old = atomicOr(live + page, kClaimed);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old & kClaimed) continue;  // another entry of this page zeroes it
-        const uint64_t from = (page * P + (old & ~kClaimed)) * row_bytes;
-        const uint64_t to = (page + 1) * P * row_bytes;
-        if (wide) {
-            uint4* d = reinterpret_cast<uint4*>(pool + from);
-            const uint64_t n = (to - from) / 16;
-            for (uint64_t v = lane; v < n; v += 32) d[v] = make_uint4(0, 0, 0, 0);
-        } else {
-            for (uint64_t b = from + lane; b < to; b += 32) pool[b] = 0;
+    // one entry per lane: the first entry naming a page claims it; the warp then zeroes
+    // the tails of the pages its lanes claimed that have unused slots, one page at a time
+    for (uint64_t base = ((uint64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * 32;
+         base < a.table_len; base += warps * 32) {
+        const uint64_t k = base + lane;
+        uint64_t page = 0;
+        unsigned old = kClaimed;
+        if (k < a.table_len) {
+            page = table[k];
+            old = atomicOr(live + page, kClaimed);
+        }
+        unsigned todo = __ballot_sync(0xffffffffu, !(old & kClaimed) && old < P);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const uint64_t pg = __shfl_sync(0xffffffffu, page, src);
+            const unsigned used = __shfl_sync(0xffffffffu, old, src);
+            const uint64_t from = (pg * P + used) * row_bytes;
+            const uint64_t to = (pg + 1) * P * row_bytes;
+            if (wide) {
+                uint4* d = reinterpret_cast<uint4*>(pool + from);
+                const uint64_t n = (to - from) / 16;
+                for (uint64_t v = lane; v < n; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+            } else {
+                for (uint64_t x = from + lane; x < to; x += 32) pool[x] = 0;
+            }
         }
     }
 }
@@ -183,7 +195,7 @@ int launch_t(const PlanArgs& a, unsigned* live, uint64_t row_bytes, void* pool,
     const int sms = current_sms(&dev);
     if (sms == 0) return HP_ERR_CUDA;
     const uint64_t cap = (uint64_t)sms * 8;
-    uint64_t g1 = (a.table_len + 255) / 256, g2 = (a.table_len + 7) / 8;
+    uint64_t g1 = (a.table_len + 255) / 256, g2 = (a.table_len + 255) / 256;
     g1 = g1 < cap ? g1 : cap;
     g2 = g2 < cap ? g2 : cap;
     if (launch_dependent(live_kernel<IndexT>, (unsigned)g1, 256, 0, st, a, live) != cudaSuccess)
