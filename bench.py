@@ -491,6 +491,18 @@ def lane_only(dev, hp, inputs, peak, reps):
     assert int(status.item()) == 0
     res = rate_entry(2 * lw.lanes * lw.n * lw.width * 2 + lw.pages * 8, ms, peak)
     res.update(op="lane_gather", lanes=lw.lanes, rows=lw.n)
+    # the same 4 KiB runs (every lane's pages, in the snapshot's order) gathered by torch's
+    # index_select over the pool seen as 4 KiB rows: the access pattern's own rate on this
+    # GPU, for reading the fraction above
+    used = -(-lw.n // lw.page_tokens)
+    pg = torch.from_numpy(lw.table[:used].astype(np.int64)).to(dev)
+    lane_ids = torch.arange(lw.batch * lw.kv_heads, device=dev)
+    idx = (pg[None, :] * (lw.batch * lw.kv_heads) + lane_ids[:, None]).reshape(-1)
+    rows = lpool.view(-1, lw.page_tokens * lw.width)
+    dst = torch.empty((idx.numel(), rows.shape[1]), dtype=rows.dtype, device=dev)
+    ms_t = median_ms(lambda: torch.index_select(rows, 0, idx, out=dst), stream, reps)
+    res["torch_index_select_same_runs"] = rate_entry(2 * dst.numel() * 2 + idx.numel() * 8,
+                                                     ms_t, peak)
     return res
 
 
@@ -581,6 +593,43 @@ def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, r
     return res
 
 
+def dequant_measurements(dev, hp, inputs, entry, med_ms):
+    """The dequantising gathers on the quantized_pool batch (int8 codes -> bf16): per-slot
+    scales, then the other schemes of [HF] Per-scheme composition with zero points."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+    w = inputs.config("quantized_pool")
+    st = GatherStep(w, dev, hp, inputs)
+    T = w.total_tokens
+    spans = int((-(-w.lens.astype(np.int64) // w.page_size)).sum())
+    b = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
+    st.plan(stream)
+    ms = med_ms(lambda: st.copy(stream), n=10)
+    out["quantized_pool_dequant_gather"] = entry(b, ms)
+    st.check_status()
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.scales_seed + 1)
+    for name, tag, axis, count in (("per_tensor", 0x01, 0, 1),
+                                   ("per_channel_heads", 0x02, 1, w.num_heads),
+                                   ("per_channel_head_dim", 0x02, 2, w.head_dim),
+                                   ("per_slot_affine", 0x03, 0, w.num_pages * w.page_size)):
+        sc = torch.rand(count, generator=g, device=dev) * 0.049 + 0.001
+        zp = torch.randint(-20, 21, (count,), generator=g, device=dev,
+                           dtype=torch.int8).view(torch.uint8)
+        q = hp.quant_desc(tag, sc, zp, axis=axis, block_size=w.page_size if tag == 3 else 0)
+        ms = med_ms(lambda: hp.hp_gather_dequant_q_planned(st.desc, q, st.out, st.ws, st.status),
+                    n=5)
+        # b counts a 4-byte scale per row; per-slot zero points add one byte per row, the
+        # other schemes' parameters are a few hundred bytes read from cache
+        nbytes = b + T if tag == 3 else b - 4 * T
+        out["quantized_pool_dequant_" + name + "_zp"] = entry(nbytes, ms)
+        st.check_status()
+    del st
+    release_device_memory()
+    return out
+
+
 def ops_measurements(dev, hp, inputs, peak, reps=20):
     """The other rows of the path at their own configurations (bytes as in
     gather_bytes; medians over reps, inputs larger than L2 except where noted)."""
@@ -666,36 +715,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     st.check_status()
     del st
 
-    # int8 pool, per-slot scales -> bf16
-    w = inputs.config("quantized_pool")
-    st = GatherStep(w, dev, hp, inputs)
-    T = w.total_tokens
-    spans = int((-(-w.lens.astype(np.int64) // w.page_size)).sum())
-    b = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
-    st.plan(stream)
-    ms = med_ms(lambda: st.copy(stream), n=10)
-    out["quantized_pool_dequant_gather"] = entry(b, ms)
-    st.check_status()
-    # the other schemes of [HF] Per-scheme composition on the same pool, with zero points
-    g = torch.Generator(device=dev)
-    g.manual_seed(w.scales_seed + 1)
-    for name, tag, axis, count in (("per_tensor", 0x01, 0, 1),
-                                   ("per_channel_heads", 0x02, 1, w.num_heads),
-                                   ("per_channel_head_dim", 0x02, 2, w.head_dim),
-                                   ("per_slot_affine", 0x03, 0, w.num_pages * w.page_size)):
-        sc = torch.rand(count, generator=g, device=dev) * 0.049 + 0.001
-        zp = torch.randint(-20, 21, (count,), generator=g, device=dev,
-                           dtype=torch.int8).view(torch.uint8)
-        q = hp.quant_desc(tag, sc, zp, axis=axis, block_size=w.page_size if tag == 3 else 0)
-        ms = med_ms(lambda: hp.hp_gather_dequant_q_planned(st.desc, q, st.out, st.ws, st.status),
-                    n=5)
-        # b counts a 4-byte scale per row; per-slot zero points add one byte per row, the
-        # other schemes' parameters are a few hundred bytes read from cache
-        nbytes = b + T if tag == 3 else b - 4 * T
-        out["quantized_pool_dequant_" + name + "_zp"] = entry(nbytes, ms)
-        st.check_status()
-    del st
-    release_device_memory()
+    out.update(dequant_measurements(dev, hp, inputs, entry, med_ms))
 
     # decode step: append one row per sequence, then gather the grown batch
     w = inputs.config("decode_append")
@@ -807,6 +827,8 @@ def main():
                     help="time only the two cache layout conversions (kernel-internal "
                          "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
                          "and print their line")
+    ap.add_argument("--dequant", action="store_true",
+                    help="only the dequantising gathers (every scheme) on quantized_pool")
     ap.add_argument("--lane", action="store_true",
                     help="time only the per-lane snapshot gather (256 lanes of the "
                          "lane_synthetic layout) and print its line")
@@ -821,6 +843,17 @@ def main():
         build.build()
         hp.lib()
         print(json.dumps(lane_only("cuda", hp, inputs, peak_hbm()[0], args.steps)))
+        return
+    if args.dequant:
+        import torch
+        from paged_kv_cache_hp_gb300 import build, hp, inputs
+        build.build()
+        hp.lib()
+        peak = peak_hbm()[0]
+        stream = torch.cuda.current_stream()
+        print(json.dumps(dequant_measurements(
+            "cuda", hp, inputs, lambda b, ms, **kw: rate_entry(b, ms, peak, **kw),
+            lambda fn, n=args.steps: median_ms(fn, stream, n))))
         return
     if args.decode_step:
         import torch
