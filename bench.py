@@ -438,8 +438,9 @@ def median_ms(fn, stream, n=20, warm=3, between=None):
     for _ in range(n):
         if between is not None:
             between()
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(200000)
+        if hasattr(torch.cuda, "_sleep"):
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(200000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
