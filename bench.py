@@ -767,6 +767,14 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     ms = med_ms(lambda: hp.hp_copy_pages(pool, w.num_pages, page_bytes, 0, sd, dd, 20000,
                                          status), n=10)
     out["copy_pages_cow"] = entry(2 * 20000 * page_bytes + 2 * 20000 * 4, ms)
+    # the same 20,000 source pages gathered into a contiguous buffer by torch's
+    # index_select (random 32 KiB reads, sequential writes): the pattern's rate at this size
+    pages = pool.view(w.num_pages, page_bytes)
+    tmp = torch.empty((20000, page_bytes), dtype=torch.uint8, device=dev)
+    sl = sd.long()
+    ms = med_ms(lambda: torch.index_select(pages, 0, sl, out=tmp), n=10)
+    out["copy_pages_cow_torch_index_select_same_pages"] = entry(2 * 20000 * page_bytes, ms)
+    del tmp
     rc, nsc = hp.hp_zero_tails_scratch_bytes(d_g)
     scratch = torch.empty(nsc, dtype=torch.uint8, device=dev)
     out["zero_tails_step"] = step_us(lambda: hp.hp_zero_tails(d_g, ws, scratch, status))
