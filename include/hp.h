@@ -387,8 +387,9 @@ int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t nu
  * has the pool's element type (HP_F16 or HP_BF16); out (device, fp32, same shape) gets 0
  * for a sequence with no tokens.  Arithmetic is fp32.  Supported: head_dim 64, 128 or
  * 256, num_q_heads / num_heads in {1, 2, 4, 8}, page_size <= 2^26 (HP_ERR_ARG otherwise).
- * The descriptor is validated as hp_plan does (unless HP_PERMISSIVE is set, in which
- * case the caller vouches for it; an attention reader cannot skip rows).
+ * The descriptor is always validated as hp_plan validates a strict one: HP_PERMISSIVE
+ * is ignored, because an attention reader cannot skip the rows it could not read -- a
+ * descriptor that fails a rule gets that rule's code in *d_status and no output.
  */
 int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const void* q,
                         uint32_t num_q_heads, float scale, float* out, void* workspace,

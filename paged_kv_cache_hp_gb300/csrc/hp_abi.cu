@@ -664,9 +664,13 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
                                uint32_t num_q_heads, float scale, float* out, void* workspace,
                                uint64_t workspace_bytes, int* d_status, void* stream)
 {
-    int rc = check_desc(k_desc);
+    if (!k_desc) return HP_ERR_NULL;
+    // always validated: a reader that cannot skip rows takes no descriptor on trust
+    hp_paged_desc dv = *k_desc;
+    dv.flags &= ~HP_PERMISSIVE;
+    int rc = check_desc(&dv);
     if (rc) return rc;
-    const hp_paged_desc* d = k_desc;
+    const hp_paged_desc* d = &dv;
     if (d->dtype != HP_F16 && d->dtype != HP_BF16) return HP_ERR_DTYPE;
     if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return HP_ERR_ARG;
     if (num_q_heads == 0 || num_q_heads % d->num_heads) return HP_ERR_ARG;

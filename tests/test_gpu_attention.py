@@ -176,3 +176,31 @@ def test_attention_mostly_empty_batch(hp, oracle):
                                8, scale)
     _check(got, want, _vmax_read(od, vpool.cpu().numpy(), "f16"))
     assert (got[lens == 0] == 0).all()
+
+
+@pytest.mark.parametrize("fault", ["page_id", "len"])
+def test_attention_validates_permissive_descriptors(hp, oracle, fault):
+    """HP_PERMISSIVE does not reach decode attention: a block-table entry naming a page
+    outside the pool, or a token count beyond the slice, is rejected by the validation
+    (the rule's code in the status word) and nothing is read or written."""
+    import torch
+    w = inputs.decode_gather(seed=12, num_pages=200, page_size=16, num_heads=2, head_dim=64,
+                             num_seqs=4, len_lo=20, len_hi=300, dtype="bf16")
+    pool = inputs.device_pool(w, "cuda")  # drawn from the well-formed batch
+    table, lens = w.table.copy(), w.lens.copy()
+    if fault == "page_id":
+        table[int(w.seq_ptr[2])] = w.num_pages + 7
+    else:
+        lens[1] = (int(w.seq_ptr[2]) - int(w.seq_ptr[1])) * 16 + 1
+    w = inputs.Workload(**{**w.__dict__, "table": table, "lens": lens})
+    b = Batch(w, pool=pool, flags=hp.PERMISSIVE)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, 4)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    q = torch.zeros((w.num_seqs, 4, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((w.num_seqs, 4, 64), float("nan"), dtype=torch.float32, device="cuda")
+    rc = hp.hp_attention_decode(b.desc, b.pool, q, 4, 0.125, out, ws, b.status)
+    torch.cuda.synchronize()
+    assert hp.status_name(rc) == "HP_OK"
+    want = "HP_ERR_PAGE_ID" if fault == "page_id" else "HP_ERR_LEN"
+    assert hp.status_name(b.status_value()) == want
+    assert torch.isnan(out).all()
