@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
     const uint64_t lo = b * per + umin(b, rem);
     const uint64_t hi = lo + per + (b < rem ? 1 : 0);
 
-    if (WARP_UNITS) {
+    if constexpr (WARP_UNITS) {
         // Each warp resolves 32 units at a time (one per lane) and copies them one after
         // the other, descriptors handed over by shuffle: no CTA-wide barrier, so one
         // warp's resolution overlaps the other warps' copies.
@@ -386,35 +386,34 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const CopyArgs a)
                 copy_run_warp<VEC>(a.src + us, a.dst + ud, rows * a.row_bytes / VEC);
             }
         }
-        return;
-    }
-
-    for (uint64_t u0 = lo; u0 < hi; u0 += kThreads) {
-        const uint64_t u = u0 + threadIdx.x;
-        if (u < hi) {
-            const Unit r = resolve<MODE, IndexT>(a, u);
-            s_src[threadIdx.x] = r.src;
-            s_dst[threadIdx.x] = r.dst;
-            s_scale[threadIdx.x] = r.scale;
-            s_rows[threadIdx.x] = r.rows;
-        }
-        __syncthreads();
-        const int nb = (int)umin(kThreads, hi - u0);
-        for (int i = 0; i < nb; ++i) {
-            const unsigned rows = s_rows[i];
-            if (rows == 0) continue;
-            if (MODE == kDequant) {
-                if (VEC == 16)
-                    dequant_run8<Q>(a, a.src + s_src[i], a.dst + s_dst[i], s_scale[i],
-                                    (uint32_t)(rows * a.row_elems / 8));
-                else
-                    dequant_run1<Q>(a, a.src + s_src[i], a.dst + s_dst[i], s_scale[i],
-                                    rows * a.row_elems);
-            } else {
-                copy_run<VEC>(a.src + s_src[i], a.dst + s_dst[i], rows * a.row_bytes / VEC);
+    } else {
+        for (uint64_t u0 = lo; u0 < hi; u0 += kThreads) {
+            const uint64_t u = u0 + threadIdx.x;
+            if (u < hi) {
+                const Unit r = resolve<MODE, IndexT>(a, u);
+                s_src[threadIdx.x] = r.src;
+                s_dst[threadIdx.x] = r.dst;
+                s_scale[threadIdx.x] = r.scale;
+                s_rows[threadIdx.x] = r.rows;
             }
+            __syncthreads();
+            const int nb = (int)umin(kThreads, hi - u0);
+            for (int i = 0; i < nb; ++i) {
+                const unsigned rows = s_rows[i];
+                if (rows == 0) continue;
+                if (MODE == kDequant) {
+                    if (VEC == 16)
+                        dequant_run8<Q>(a, a.src + s_src[i], a.dst + s_dst[i], s_scale[i],
+                                        (uint32_t)(rows * a.row_elems / 8));
+                    else
+                        dequant_run1<Q>(a, a.src + s_src[i], a.dst + s_dst[i], s_scale[i],
+                                        rows * a.row_elems);
+                } else {
+                    copy_run<VEC>(a.src + s_src[i], a.dst + s_dst[i], rows * a.row_bytes / VEC);
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
 }
 
