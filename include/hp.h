@@ -2,15 +2,23 @@
  * hp.h -- C ABI of the block-paged KV-cache library (libhp.so) for GB300 (sm_103a).
  *
  * The library implements the data path of the block-paged layout defined in
- * "Block-Paged Layout -- Hurray Format Specification" (cited below as [HF]) and
- * of the per-lane page layout in "Keep token order across cache pages"
- * (practical-ch20-paged-kv-layout, cited as [CH]):
+ * "Block-Paged Layout -- Hurray Format Specification" (cited below as [HF]), of the
+ * per-lane page layout in "Keep token order across cache pages"
+ * (practical-ch20-paged-kv-layout, cited as [CH]) and of the block-table reader and
+ * copy-on-write of "Visualize PagedAttention block layout" (cited as [VA]):
  *
  *   - a planner/validator for a block-paged descriptor,
  *   - a gather of a ragged batch into the logical [total_tokens, H, D] tensor,
  *   - the inverse scatter that appends new K/V rows into their pages,
- *   - a dequantising gather of an int8 pool with per-page-slot fp32 scales,
- *   - gather and append for the [N, B, H_kv, P, d] per-lane layout.
+ *   - a dequantising gather of an 8-bit pool with per-page-slot fp32 scales, and
+ *     under the other schemes of [HF] Per-scheme composition (per tensor, per
+ *     channel, per block, with or without zero points),
+ *   - gather and append for the [N, B, H_kv, P, d] per-lane layout,
+ *   - the writer side: a batched page copy (copy-on-write) and the zeroing of the
+ *     slots no sequence reads,
+ *   - decode attention that reads K and V through the block table,
+ *   - conversions between a kernel-internal cache layout and the interchange layout,
+ *     and between a padded block table and the descriptor's slices.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -130,7 +138,8 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  *
  *   page_pool    device, [num_pages, page_size, num_heads, head_dim] elements of
  *                `dtype`, row-major; num_pages*page_size*num_heads*head_dim*width
- *                bytes ([HF] invariant (4)).  Written only by hp_scatter_append.
+ *                bytes ([HF] invariant (4)).  Written only by hp_scatter_append and
+ *                hp_zero_tails (hp_copy_pages takes its pool as an argument of its own).
  *   block_table  device, table_len entries of the index type: physical page IDs,
  *                the per-sequence slices concatenated.  May be NULL iff
  *                table_len == 0 ([HF] Buffer Table, empty batch).
