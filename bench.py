@@ -598,8 +598,18 @@ def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, r
                                                aws, status), n=reps)
     assert int(status.item()) == 0, hp.status_name(int(status.item()))
     kv_bytes = 2 * w.total_tokens * w.row_bytes
-    res = entry(kv_bytes + qd.numel() * 2 + ao.numel() * 4, ms,
+    nbytes = kv_bytes + qd.numel() * 2 + ao.numel() * 4
+    res = entry(nbytes, ms,
                 note="K and V rows read once; %d query heads, GQA %d" % (Hq, Hq // w.num_heads))
+    # the per-layer cost when one plan serves every layer of a decode step: the planned
+    # call alone (attention kernel only)
+    assert hp.hp_attention_plan(d_k, Hq, aws, status) == 0
+    ms_p = med_ms(lambda: hp.hp_attention_decode_planned(d_k, vpool, qd, Hq,
+                                                         1 / np.sqrt(w.head_dim), ao, aws,
+                                                         status), n=reps)
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
+    res["planned_call"] = entry(nbytes, ms_p, note="hp_attention_decode_planned after one "
+                                "hp_attention_plan (per layer of a decode step)")
     del vpool, aws
     release_device_memory()
     return res

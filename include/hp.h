@@ -404,6 +404,25 @@ int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const v
                         uint32_t num_q_heads, float scale, float* out, void* workspace,
                         uint64_t workspace_bytes, int* d_status, void* stream);
 
+/*
+ * The two halves of hp_attention_decode, for a block table shared by several calls (the
+ * layers of one decode step read their K/V pools through the same table, offsets and
+ * counts).  ASYNC hp_attention_plan validates k_desc (always; see above), stores each
+ * sequence's step counts in `workspace` and zeroes its segment counts.  ASYNC
+ * hp_attention_decode_planned then runs the attention kernel alone; any number of
+ * planned calls may follow one plan on the same stream, each with its own K pool (the
+ * descriptor's page_pool), V pool, q, scale and out, provided the descriptor's table,
+ * offsets, counts and geometry and num_q_heads are those of the plan.  A planned call
+ * after a plan that failed writes nothing.  The host checks of hp_attention_decode
+ * apply to both; neither stores HP_OK over an earlier error in *d_status.
+ */
+int hp_attention_plan(const hp_paged_desc* k_desc, uint32_t num_q_heads, void* workspace,
+                      uint64_t workspace_bytes, int* d_status, void* stream);
+int hp_attention_decode_planned(const hp_paged_desc* k_desc, const void* v_pool, const void* q,
+                                uint32_t num_q_heads, float scale, float* out,
+                                const void* workspace, uint64_t workspace_bytes, int* d_status,
+                                void* stream);
+
 /* --------------------------------------------------------- layout conversions */
 /*
  * ASYNC.  [HF] Framework Compliance: a producer whose cache sits in a kernel-internal

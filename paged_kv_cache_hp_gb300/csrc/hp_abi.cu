@@ -660,42 +660,74 @@ HP_API int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint
     return attention_ws(k_desc, num_q_heads, bytes);
 }
 
-HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const void* q,
-                               uint32_t num_q_heads, float scale, float* out, void* workspace,
-                               uint64_t workspace_bytes, int* d_status, void* stream)
+namespace {
+
+// Host checks shared by the attention entry points, on a strict copy of the descriptor:
+// an attention reader always validates (it cannot skip rows it could not read).
+struct AttnPrep {
+    hp_paged_desc d;
+    u64 G;
+    char* part;          // the records, after the plan's workspace
+    unsigned* seg_done;  // one count per (sequence, K/V head), after the records
+};
+
+int attention_prepare(const hp_paged_desc* k_desc, uint32_t num_q_heads, const void* workspace,
+                      uint64_t workspace_bytes, AttnPrep* p)
 {
     if (!k_desc) return HP_ERR_NULL;
-    // always validated: a reader that cannot skip rows takes no descriptor on trust
-    hp_paged_desc dv = *k_desc;
-    dv.flags &= ~HP_PERMISSIVE;
-    int rc = check_desc(&dv);
+    p->d = *k_desc;
+    p->d.flags &= ~HP_PERMISSIVE;
+    const hp_paged_desc* d = &p->d;
+    int rc = check_desc(d);
     if (rc) return rc;
-    const hp_paged_desc* d = &dv;
     if (d->dtype != HP_F16 && d->dtype != HP_BF16) return HP_ERR_DTYPE;
     if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return HP_ERR_ARG;
     if (num_q_heads == 0 || num_q_heads % d->num_heads) return HP_ERR_ARG;
-    const u64 G = num_q_heads / d->num_heads;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return HP_ERR_ARG;
+    p->G = num_q_heads / d->num_heads;
+    if (p->G != 1 && p->G != 2 && p->G != 4 && p->G != 8) return HP_ERR_ARG;
     if (d->page_size > (1u << 26)) return HP_ERR_ARG;  // offsets in a 32-page window fit 32 bits
-    if (d->num_seqs && (!q || !out)) return HP_ERR_NULL;
-    if (d->num_pages && !v_pool) return HP_ERR_NULL;
-    if (misaligned(v_pool, 64) || misaligned(q, 16) || misaligned(out, 16)) return HP_ERR_ALIGN;
     u64 need = 0;
     rc = attention_ws(d, num_q_heads, &need);
     if (rc) return rc;
     if (!workspace || misaligned(workspace, 256) || workspace_bytes < need) return HP_ERR_WORKSPACE;
     u64 plan_bytes = 0;
     ws_bytes(d, &plan_bytes);
-    hp::PlanArgs pa = plan_args(d, workspace, d_status);
-    pa.step_tokens = attn_step_tokens(G, d->head_dim);
-    char* part = static_cast<char*>(workspace) + plan_bytes;
-    const u64 part_bytes = attn_records(d) * G * (d->head_dim + 2) * 4;
-    unsigned* seg_done = reinterpret_cast<unsigned*>(part + part_bytes);
-    if (d->num_seqs && cudaMemsetAsync(seg_done, 0, 4 * d->num_seqs * d->num_heads,
+    p->part = static_cast<char*>(const_cast<void*>(workspace)) + plan_bytes;
+    p->seg_done = reinterpret_cast<unsigned*>(p->part + attn_records(d) * p->G * (d->head_dim + 2) * 4);
+    return HP_OK;
+}
+
+}  // namespace
+
+HP_API int hp_attention_plan(const hp_paged_desc* k_desc, uint32_t num_q_heads, void* workspace,
+                             uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    AttnPrep p;
+    int rc = attention_prepare(k_desc, num_q_heads, workspace, workspace_bytes, &p);
+    if (rc) return rc;
+    const hp_paged_desc* d = &p.d;
+    if (d->num_seqs && cudaMemsetAsync(p.seg_done, 0, 4 * d->num_seqs * d->num_heads,
                                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return HP_ERR_CUDA;
-    rc = hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
-    if (rc || d->num_seqs == 0) return rc;
+    hp::PlanArgs pa = plan_args(d, workspace, d_status);
+    pa.step_tokens = attn_step_tokens(p.G, d->head_dim);
+    return hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
+}
+
+HP_API int hp_attention_decode_planned(const hp_paged_desc* k_desc, const void* v_pool,
+                                       const void* q, uint32_t num_q_heads, float scale,
+                                       float* out, const void* workspace,
+                                       uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    AttnPrep p;
+    int rc = attention_prepare(k_desc, num_q_heads, workspace, workspace_bytes, &p);
+    if (rc) return rc;
+    const hp_paged_desc* d = &p.d;
+    if (d->num_seqs && (!q || !out)) return HP_ERR_NULL;
+    if (d->num_pages && !v_pool) return HP_ERR_NULL;
+    if (misaligned(v_pool, 64) || misaligned(q, 16) || misaligned(out, 16)) return HP_ERR_ALIGN;
+    if (d->num_seqs == 0) return HP_OK;
+    const hp::WsView ws = hp::ws_view(const_cast<void*>(workspace), d->num_seqs);
     hp::AttnArgs a{};
     a.k_pool = d->page_pool;
     a.v_pool = v_pool;
@@ -710,19 +742,37 @@ HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, 
     a.Hkv = (uint32_t)d->num_heads;
     a.Hq = num_q_heads;
     a.D = (uint32_t)d->head_dim;
-    a.G = (uint32_t)G;
+    a.G = (uint32_t)p.G;
     hp::invariant_divisor(d->page_size, &a.p_m, &a.p_l);
     a.R = attn_ranges_per_cta(d->num_heads);
     a.scale = scale;
-    a.hdr = pa.ws.hdr;
-    a.units_off = pa.ws.units_off;
-    a.part_acc = reinterpret_cast<float*>(part);
-    a.part_ml = a.part_acc + attn_records(d) * G * d->head_dim;
-    a.seg_done = seg_done;
+    a.hdr = ws.hdr;
+    a.units_off = ws.units_off;
+    a.part_acc = reinterpret_cast<float*>(p.part);
+    a.part_ml = a.part_acc + attn_records(d) * p.G * d->head_dim;
+    a.seg_done = p.seg_done;
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
     a.d_status = d_status;
     return hp::launch_attention(d->index_type == HP_IDX_U64, a, stream);
+}
+
+HP_API int hp_attention_decode(const hp_paged_desc* k_desc, const void* v_pool, const void* q,
+                               uint32_t num_q_heads, float scale, float* out, void* workspace,
+                               uint64_t workspace_bytes, int* d_status, void* stream)
+{
+    AttnPrep p;
+    int rc = attention_prepare(k_desc, num_q_heads, workspace, workspace_bytes, &p);
+    if (rc) return rc;
+    const hp_paged_desc* d = &p.d;
+    // every host check of the launch before anything is enqueued
+    if (d->num_seqs && (!q || !out)) return HP_ERR_NULL;
+    if (d->num_pages && !v_pool) return HP_ERR_NULL;
+    if (misaligned(v_pool, 64) || misaligned(q, 16) || misaligned(out, 16)) return HP_ERR_ALIGN;
+    rc = hp_attention_plan(k_desc, num_q_heads, workspace, workspace_bytes, d_status, stream);
+    if (rc) return rc;
+    return hp_attention_decode_planned(k_desc, v_pool, q, num_q_heads, scale, out, workspace,
+                                       workspace_bytes, d_status, stream);
 }
 
 namespace {

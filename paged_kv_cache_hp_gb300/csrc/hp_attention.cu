@@ -33,7 +33,8 @@
 //                   segment merges the records into the result, so no second kernel and
 //                   no pass over the sequences follow.
 // Records: acc [records, G, D] and (max, sum) [records, G] in the workspace after the
-// plan, then one count per (sequence, K/V head), zeroed before the launch.
+// plan, then one count per (sequence, K/V head): zeroed by the plan, and set back to zero
+// by the warp that merges, so planned calls can follow one another on one workspace.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -323,6 +324,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 && E >= 4) ? 1 : 2) attn_ker
                 merge_segments<G, E>(a, ((pend + f) * a.Hkv + g) * G, nr,
                                      a.out + (pend * a.Hq + (uint64_t)g * G) * D + lane * E,
                                      lane);
+                // back to zero for the next call on this workspace (no other warp of
+                // this launch touches the count any more)
+                if (lane == 0) a.seg_done[pend * a.Hkv + g] = 0u;
             }
             pend = ~0ull;
         };

@@ -26,7 +26,8 @@ struct AttnArgs {
     const unsigned long long* units_off;  // steps per sequence, prefix
     float* part_acc;          // [records, G, D]: each segment's weighted value sums
     float* part_ml;           // [records, G, 2]: its score maximum and weight sum
-    unsigned* seg_done;       // [num_seqs, Hkv]: segments finished, zero at launch
+    unsigned* seg_done;       // [num_seqs, Hkv]: segments finished; zero at launch and
+                              // again when the launch ends
     float* out;               // [num_seqs, Hq, D] fp32
     int elem_bf16;            // element type: bf16 (1) or f16 (0)
     int* d_status;

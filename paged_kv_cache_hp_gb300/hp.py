@@ -91,6 +91,9 @@ def lib():
                 "hp_attention_decode_workspace_bytes": (i, [D, ctypes.c_uint32, pu64]),
                 "hp_attention_decode": (i, [D, vp, vp, ctypes.c_uint32, ctypes.c_float, vp, vp,
                                             u64, vp, vp]),
+                "hp_attention_plan": (i, [D, ctypes.c_uint32, vp, u64, vp, vp]),
+                "hp_attention_decode_planned": (i, [D, vp, vp, ctypes.c_uint32, ctypes.c_float,
+                                                    vp, vp, u64, vp, vp]),
                 "hp_from_kernel_layout": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32,
                                               vp]),
                 "hp_to_kernel_layout": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32,
@@ -289,6 +292,18 @@ def hp_attention_decode(desc, v_pool, q, num_q_heads, scale, out, workspace, d_s
     return lib().hp_attention_decode(desc.ref, _p(v_pool), _p(q), num_q_heads, float(scale),
                                      _p(out), _p(workspace), _wsn(workspace), _p(d_status),
                                      _stream(stream))
+
+
+def hp_attention_plan(desc, num_q_heads, workspace, d_status=None, stream=None):
+    return lib().hp_attention_plan(desc.ref, num_q_heads, _p(workspace), _wsn(workspace),
+                                   _p(d_status), _stream(stream))
+
+
+def hp_attention_decode_planned(desc, v_pool, q, num_q_heads, scale, out, workspace,
+                                d_status=None, stream=None):
+    return lib().hp_attention_decode_planned(desc.ref, _p(v_pool), _p(q), num_q_heads,
+                                             float(scale), _p(out), _p(workspace),
+                                             _wsn(workspace), _p(d_status), _stream(stream))
 
 
 def hp_from_kernel_layout(src, dst, num_blocks, block_size, num_heads, head_dim, x, dtype,

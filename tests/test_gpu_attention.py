@@ -204,3 +204,62 @@ def test_attention_validates_permissive_descriptors(hp, oracle, fault):
     want = "HP_ERR_PAGE_ID" if fault == "page_id" else "HP_ERR_LEN"
     assert hp.status_name(b.status_value()) == want
     assert torch.isnan(out).all()
+
+
+def test_planned_attention_over_layers(hp, oracle):
+    """One hp_attention_plan, then planned calls for three "layers" (their own K and V
+    pools and queries through the same table): each equals the one-call result bit for
+    bit, so the segment counts are back at zero after every planned call."""
+    import torch
+    w = inputs.decode_gather(seed=31, num_pages=3000, page_size=16, num_heads=4, head_dim=128,
+                             num_seqs=6, len_lo=0, len_hi=2500, dtype="bf16")
+    Hq = 16
+    b = Batch(w)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, Hq)
+    ws_plan = torch.full((nws,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws_one = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    layers = []
+    for layer in range(3):
+        kl = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 500 + layer}), "cuda")
+        vl = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 600 + layer}), "cuda")
+        g = torch.Generator(device="cuda")
+        g.manual_seed(700 + layer)
+        ql = torch.randn((w.num_seqs, Hq, 128), generator=g, device="cuda").to(torch.bfloat16)
+        layers.append((kl, vl, ql))
+    assert hp.hp_attention_plan(b.desc, Hq, ws_plan, b.status) == 0
+    for kl, vl, ql in layers:
+        dl = hp.PagedDesc(kl, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages, page_size=16,
+                          num_heads=4, head_dim=128, dtype="bf16", index_type=b.it)
+        got = torch.full((w.num_seqs, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        want = torch.full_like(got, float("nan"))
+        assert hp.hp_attention_decode_planned(dl, vl, ql, Hq, 0.09, got, ws_plan, b.status) == 0
+        assert hp.hp_attention_decode(dl, vl, ql, Hq, 0.09, want, ws_one, b.status) == 0
+        torch.cuda.synchronize()
+        assert b.status_value() == 0
+        assert torch.equal(got.view(torch.int32), want.view(torch.int32))
+    # and the last layer against the oracle
+    od = oracle.Desc(kl.cpu().numpy(), w.table, w.seq_ptr, w.lens, num_pages=w.num_pages,
+                     page_size=16, num_heads=4, head_dim=128, dtype="bf16", index_type=b.it)
+    vh = vl.cpu().numpy()
+    wantd = od.attention_decode(vh, ql.view(torch.int16).cpu().numpy().view(np.uint16), Hq, 0.09)
+    _check(got.cpu().numpy(), wantd, _vmax_read(od, vh, "bf16"))
+
+
+def test_planned_attention_after_a_failed_plan_writes_nothing(hp, oracle):
+    import torch
+    w = inputs.decode_gather(seed=32, num_pages=200, page_size=16, num_heads=2, head_dim=64,
+                             num_seqs=3, len_lo=20, len_hi=300, dtype="bf16")
+    pool = inputs.device_pool(w, "cuda")
+    table = w.table.copy()
+    table[0] = w.num_pages
+    w = inputs.Workload(**{**w.__dict__, "table": table})
+    b = Batch(w, pool=pool)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, 4)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    q = torch.zeros((w.num_seqs, 4, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((w.num_seqs, 4, 64), float("nan"), dtype=torch.float32, device="cuda")
+    assert hp.hp_attention_plan(b.desc, 4, ws, b.status) == 0
+    assert hp.hp_attention_decode_planned(b.desc, pool, q, 4, 0.125, out, ws, b.status) == 0
+    torch.cuda.synchronize()
+    assert hp.status_name(b.status_value()) == "HP_ERR_PAGE_ID"
+    assert torch.isnan(out).all()
