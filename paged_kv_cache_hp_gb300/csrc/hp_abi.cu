@@ -9,6 +9,7 @@
 // the constructor of "Keep token order across cache pages" (PagedKvLayout::new).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <vector>
 
@@ -140,6 +141,24 @@ hp::CopyArgs copy_args(const hp_paged_desc* d, const void* ws, int* d_status)
     return a;
 }
 
+// True for memory that is not device memory of a GPU: pinned host memory (page-locked and
+// mapped, e.g. Grace memory holding an offloaded pool) or pageable host memory.  Kernels
+// reach it with ordinary loads and stores over the host link; the TMA copy engine is kept
+// to device memory, so an operation touching host memory takes the register engine.
+bool host_resident(const void* p)
+{
+    if (!p) return false;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return true;  // unknown: not a device allocation the TMA engine may assume
+    }
+    return at.type != cudaMemoryTypeDevice;
+}
+
+// Units of at most 8 KiB keep an operation on the register engine (one warp per unit).
+constexpr u64 kRegisterEngineUnit = 8192;
+
 int sync_verdict(const void* ws, u64* first_bad, void* stream)
 {
     unsigned long long key = 0;
@@ -230,6 +249,8 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
         return hp::launch_copy(hp::kDequant, d->index_type == HP_IDX_U64, a, vec, stream);
     }
     vec = pick_vec(a.row_bytes, d->page_pool, out);
+    if (host_resident(d->page_pool) || host_resident(out))
+        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     return hp::launch_copy(hp::kGather, d->index_type == HP_IDX_U64, a, vec, stream);
 }
 
@@ -296,6 +317,8 @@ int append_planned(const hp_paged_desc* d, const void* new_rows, const void* new
     a.dst = static_cast<char*>(const_cast<void*>(d->page_pool));
     if (!a.src) a.src = reinterpret_cast<const char*>(d->page_pool);  // no rows: never read
     const int vec = pick_vec(a.row_bytes, a.src, d->page_pool);
+    if (host_resident(d->page_pool) || host_resident(new_rows))
+        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     return hp::launch_copy(hp::kAppend, d->index_type == HP_IDX_U64, a, vec, stream);
 }
 
@@ -583,7 +606,8 @@ HP_API int hp_copy_pages(void* page_pool, uint64_t num_pages, uint64_t page_byte
     a.src = static_cast<const char*>(page_pool);
     a.dst = static_cast<char*>(page_pool);
     a.row_bytes = page_bytes;
-    a.unit_bytes = page_bytes;
+    a.unit_bytes = host_resident(page_pool) ? std::min<u64>(page_bytes, kRegisterEngineUnit)
+                                            : page_bytes;
     a.d_status = d_status;
     return hp::launch_copy(hp::kCopyPages, index_type == HP_IDX_U64, a,
                            pick_vec(page_bytes, page_pool, page_pool), stream);
@@ -937,6 +961,8 @@ HP_API int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capa
     a.dst = static_cast<char*>(out);
     a.row_bytes = rb;
     a.unit_bytes = page_tokens * rb;
+    if (host_resident(pool) || host_resident(out))
+        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     a.d_status = d_status;
     return hp::launch_copy(hp::kLaneGather, 1, a, pick_vec(rb, pool, out), stream);
 }
@@ -968,6 +994,8 @@ HP_API int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity,
     a.dst = static_cast<char*>(pool);
     a.row_bytes = rb;
     a.unit_bytes = page_tokens * rb;
+    if (host_resident(pool) || host_resident(new_rows))
+        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     a.d_status = d_status;
     return hp::launch_copy(hp::kLaneAppend, 1, a, pick_vec(rb, new_rows, pool), stream);
 }

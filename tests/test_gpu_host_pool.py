@@ -1,0 +1,89 @@
+"""GPU parity of the operations on a page pool (or an output) in page-locked host memory:
+the kernels read and write it in place over the host link (the register copy engine; the
+TMA engine is kept to device memory).  Bit-exact against the oracle, like every copy."""
+import numpy as np
+import pytest
+
+from helpers import Batch, index_tensor
+from paged_kv_cache_hp_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _pinned_copy(t):
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
+@pytest.mark.parametrize("out_on_host", [False, True])
+@pytest.mark.parametrize("name", ["decode_gather", "prefix_sharing"])
+def test_gather_from_a_host_pool(hp, oracle, name, out_on_host):
+    """128 KiB (decode_gather) and 32 KiB (prefix_sharing) page runs, which a device pool
+    sends through the TMA engine; the output in device or in host memory."""
+    import torch
+    w = inputs.config(name, "small")
+    dev = Batch(w)
+    host_pool = _pinned_copy(dev.pool)
+    b = Batch(w, pool=host_pool)
+    T = w.total_tokens
+    if out_on_host:
+        out = torch.full((T * w.row_bytes,), 0xEE, dtype=torch.uint8, pin_memory=True)
+    else:
+        out = torch.full((T * w.row_bytes,), 0xEE, dtype=torch.uint8, device="cuda")
+    assert hp.hp_gather(b.desc, out, T, b.ws, b.status) == 0
+    torch.cuda.synchronize()
+    assert hp.status_name(b.status_value()) == "HP_OK"
+    want, written, fault = dev.oracle_desc().gather()
+    assert fault == "OK" and written.all()
+    assert np.array_equal(out.cpu().numpy().reshape(want.shape), want)
+
+
+def test_bulk_append_into_a_host_pool_then_gather(hp, oracle):
+    """Prefill-style append of every row into empty slices of a host-resident pool, then
+    the gather back: the rows come back, and no other byte of the pool changed."""
+    import torch
+    w = inputs.decode_gather(seed=78, num_pages=300, num_heads=8, head_dim=128, num_seqs=5,
+                             len_lo=1, len_hi=300, dtype="bf16")
+    T = w.total_tokens
+    pool = _pinned_copy(inputs.device_pool(w, "cuda"))
+    before = pool.numpy().copy()
+    rows = np.random.default_rng(2).integers(0, 256, (T, w.row_bytes), dtype=np.uint8)
+    new = torch.from_numpy(rows.reshape(-1)).to("cuda")
+    new_ptr = index_tensor(np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))])
+                           .astype(np.uint32), "cuda")
+    zeros = np.zeros(w.num_seqs, dtype=np.uint32)
+    a = Batch(w, pool=pool, lens=zeros)
+    assert hp.hp_scatter_append(a.desc, new, new_ptr, T, a.ws, a.status) == 0
+    torch.cuda.synchronize()
+    assert a.status_value() == 0
+    # the oracle's append on a copy of the pool as it was gives the same bytes
+    want_pool = before.copy()
+    o = a.oracle_desc(pool_host=want_pool, lens=zeros)
+    np_host = np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))]).astype(np.uint32)
+    assert o.scatter_append(rows, np_host) == "OK"
+    assert np.array_equal(pool.numpy(), want_pool)
+    g = Batch(w, pool=pool)
+    out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device="cuda")
+    assert hp.hp_gather(g.desc, out, T, g.ws, g.status) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().reshape(T, -1), rows)
+
+
+def test_copy_pages_in_a_host_pool(hp, oracle):
+    import torch
+    pages, page_bytes = 64, 32768
+    rng = np.random.default_rng(5)
+    host = rng.integers(0, 256, pages * page_bytes, dtype=np.uint8)
+    pool = torch.from_numpy(host.copy()).pin_memory()
+    src = rng.choice(32, 20, replace=False).astype(np.uint32)
+    dst = (32 + rng.choice(32, 20, replace=False)).astype(np.uint32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = hp.hp_copy_pages(pool, pages, page_bytes, 0, index_tensor(src, "cuda"),
+                          index_tensor(dst, "cuda"), 20, st)
+    torch.cuda.synchronize()
+    assert rc == 0 and st.item() == 0
+    want = host.reshape(pages, page_bytes).copy()
+    want[dst] = want[src]
+    assert np.array_equal(pool.numpy().reshape(pages, page_bytes), want)
