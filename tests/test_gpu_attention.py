@@ -206,14 +206,16 @@ def test_attention_validates_permissive_descriptors(hp, oracle, fault):
     assert torch.isnan(out).all()
 
 
-def test_planned_attention_over_layers(hp, oracle):
+@pytest.mark.parametrize("dtype,Hkv,G,D", [("bf16", 4, 4, 128), ("f16", 2, 8, 256),
+                                           ("bf16", 8, 1, 64), ("f16", 12, 2, 128)])
+def test_planned_attention_over_layers(hp, oracle, dtype, Hkv, G, D):
     """One hp_attention_plan, then planned calls for three "layers" (their own K and V
     pools and queries through the same table): each equals the one-call result bit for
     bit, so the segment counts are back at zero after every planned call."""
     import torch
-    w = inputs.decode_gather(seed=31, num_pages=3000, page_size=16, num_heads=4, head_dim=128,
-                             num_seqs=6, len_lo=0, len_hi=2500, dtype="bf16")
-    Hq = 16
+    w = inputs.decode_gather(seed=31 + D + G, num_pages=3000, page_size=16, num_heads=Hkv,
+                             head_dim=D, num_seqs=6, len_lo=0, len_hi=2500, dtype=dtype)
+    Hq = Hkv * G
     b = Batch(w)
     rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, Hq)
     ws_plan = torch.full((nws,), 0xFF, dtype=torch.uint8, device="cuda")
@@ -224,13 +226,14 @@ def test_planned_attention_over_layers(hp, oracle):
         vl = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 600 + layer}), "cuda")
         g = torch.Generator(device="cuda")
         g.manual_seed(700 + layer)
-        ql = torch.randn((w.num_seqs, Hq, 128), generator=g, device="cuda").to(torch.bfloat16)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+        ql = torch.randn((w.num_seqs, Hq, D), generator=g, device="cuda").to(tdt)
         layers.append((kl, vl, ql))
     assert hp.hp_attention_plan(b.desc, Hq, ws_plan, b.status) == 0
     for kl, vl, ql in layers:
         dl = hp.PagedDesc(kl, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages, page_size=16,
-                          num_heads=4, head_dim=128, dtype="bf16", index_type=b.it)
-        got = torch.full((w.num_seqs, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+                          num_heads=Hkv, head_dim=D, dtype=dtype, index_type=b.it)
+        got = torch.full((w.num_seqs, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
         want = torch.full_like(got, float("nan"))
         assert hp.hp_attention_decode_planned(dl, vl, ql, Hq, 0.09, got, ws_plan, b.status) == 0
         assert hp.hp_attention_decode(dl, vl, ql, Hq, 0.09, want, ws_one, b.status) == 0
@@ -239,10 +242,10 @@ def test_planned_attention_over_layers(hp, oracle):
         assert torch.equal(got.view(torch.int32), want.view(torch.int32))
     # and the last layer against the oracle
     od = oracle.Desc(kl.cpu().numpy(), w.table, w.seq_ptr, w.lens, num_pages=w.num_pages,
-                     page_size=16, num_heads=4, head_dim=128, dtype="bf16", index_type=b.it)
+                     page_size=16, num_heads=Hkv, head_dim=D, dtype=dtype, index_type=b.it)
     vh = vl.cpu().numpy()
     wantd = od.attention_decode(vh, ql.view(torch.int16).cpu().numpy().view(np.uint16), Hq, 0.09)
-    _check(got.cpu().numpy(), wantd, _vmax_read(od, vh, "bf16"))
+    _check(got.cpu().numpy(), wantd, _vmax_read(od, vh, dtype))
 
 
 def test_planned_attention_after_a_failed_plan_writes_nothing(hp, oracle):
