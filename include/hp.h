@@ -26,7 +26,7 @@
  *   hp_status_string() names it.  Nothing aborts or prints.
  * - Pointers named d_* or described as "device" point to GPU memory of the
  *   current CUDA device; pointers described as "host" point to CPU memory.
- *   The page pool and the output of the gathers (not the dequantising ones), the
+ *   The page pool and the output of the gathers (dequantising ones included), the
  *   pool and new rows of the appends, the pool of hp_copy_pages and the buffers of
  *   the lane operations may instead be page-locked host memory (from the CUDA host
  *   allocator or cudaHostRegister, mapped): those operations then read and write it

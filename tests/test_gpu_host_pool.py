@@ -87,3 +87,57 @@ def test_copy_pages_in_a_host_pool(hp, oracle):
     want = host.reshape(pages, page_bytes).copy()
     want[dst] = want[src]
     assert np.array_equal(pool.numpy().reshape(pages, page_bytes), want)
+
+
+@pytest.mark.parametrize("out_on_host", [False, True])
+def test_dequant_gather_from_a_host_pool(hp, oracle, out_on_host):
+    """The dequantising gather (int8 codes x per-slot scales -> bf16) on a pool in
+    page-locked host memory, the output in device or host memory: the same bits as the
+    oracle's single rounding."""
+    import torch
+    w = inputs.config("quantized_pool", "small")
+    dev = Batch(w)
+    b = Batch(w, pool=_pinned_copy(dev.pool))
+    T = w.total_tokens
+    n = T * w.num_heads * w.head_dim
+    kw = dict(pin_memory=True) if out_on_host else dict(device="cuda")
+    out = torch.full((n,), -1, dtype=torch.int16, **kw)
+    assert hp.hp_gather_dequant(b.desc, out, T, b.ws, b.status) == 0
+    torch.cuda.synchronize()
+    assert b.status_value() == 0
+    want, written, fault = dev.oracle_desc().gather_dequant()
+    assert fault == "OK" and written.all()
+    got = out.cpu().numpy().view(np.uint16).reshape(want.shape)
+    assert np.array_equal(got, want)
+
+
+def test_lane_gather_and_append_on_a_host_pool(hp, oracle):
+    """[N, B, H_kv, P, d] lane layout with 16 KiB (lane, page) runs, which a device pool
+    sends through the TMA engine, in page-locked host memory: snapshot, then append."""
+    import torch
+    rng = np.random.default_rng(9)
+    C, P, B, H, W = 1000, 64, 2, 3, 128
+    N = -(-C // P)
+    T = rng.permutation(N).astype(np.uint64)
+    pool = rng.integers(0, 256, (N, B, H, P, W * 2), dtype=np.uint8)
+    hpool = torch.from_numpy(pool.copy()).pin_memory()
+    dT = torch.from_numpy(T.view(np.int64).copy()).to("cuda")
+    st = torch.full((1,), 9, dtype=torch.int32, device="cuda")
+    n = 777
+    out = torch.full((B * H * n * W * 2,), 0xEE, dtype=torch.uint8, pin_memory=True)
+    assert hp.hp_lane_gather(hpool, dT, C, P, B, H, W, "bf16", n, out, st) == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    pool_t = pool.view(np.uint16).reshape(N, B, H, P, W)
+    want = oracle.lane_gather(pool_t, C, P, T, B, H, W, n)
+    assert np.array_equal(out.numpy(), np.ascontiguousarray(want).view(np.uint8).reshape(-1))
+    m = 150
+    new = rng.integers(0, 256, (B, H, m, W * 2), dtype=np.uint8)
+    hnew = torch.from_numpy(new.copy()).pin_memory()
+    assert hp.hp_lane_append(hpool, dT, C, P, B, H, W, "bf16", n, m, hnew, st) == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    host = pool_t.copy()
+    assert oracle.lane_append(host, C, P, T, B, H, W, n,
+                              new.view(np.uint16).reshape(B, H, m, W)) == "OK"
+    assert np.array_equal(hpool.numpy().reshape(-1), host.view(np.uint8).reshape(-1))
