@@ -11,7 +11,7 @@ case; measured on GB300: 1e-8 to 3e-8 of max|V|, 2e-6 with a peaked softmax).  T
 import numpy as np
 import pytest
 
-from helpers import Batch, index_tensor, sub_batch
+from helpers import Batch, sub_batch
 from paged_kv_cache_hp_gb300 import inputs
 
 pytestmark = pytest.mark.gpu

@@ -7,7 +7,7 @@ also count elements that differ at all and expect none.
 import numpy as np
 import pytest
 
-from helpers import Batch, index_tensor, sub_batch
+from helpers import Batch, sub_batch
 from paged_kv_cache_hp_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
