@@ -12,10 +12,13 @@ def test_f16_and_bf16_conversions(oracle):
     finite = np.isfinite(f16)
     assert np.array_equal(got[finite], f16[finite])
     assert np.array_equal(np.isnan(got), np.isnan(f16)) and np.array_equal(np.isinf(got), np.isinf(f16))
-    bf = (codes.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # signalling NaN codes become quiet NaNs
+        bf = (codes.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     gotb = np.array([oracle.lib().or_bf16_to_double(int(c)) for c in codes[::7]])
     fin = np.isfinite(bf[::7])
     assert np.array_equal(gotb[fin], bf[::7][fin])
+    assert np.array_equal(np.isnan(gotb), np.isnan(bf[::7]))
+    assert np.array_equal(np.isinf(gotb), np.isinf(bf[::7]))
 
 
 def _batch(rng, dtype, S=3, N=12, P=4, H=2, D=8, lens=None):
