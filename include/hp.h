@@ -234,8 +234,10 @@ int hp_plan(const hp_paged_desc* desc, uint64_t out_tokens, void* workspace,
 int hp_gather(const hp_paged_desc* desc, void* out, uint64_t out_tokens, void* workspace,
               uint64_t workspace_bytes, int* d_status, void* stream);
 
-/* ASYNC.  The copy step of hp_gather, for a workspace hp_plan filled with the same
- * descriptor earlier on the same stream.  Does nothing if that plan failed. */
+/* ASYNC.  The copy step of hp_gather, for a workspace hp_plan filled earlier on the same
+ * stream with the same descriptor -- or one that differs only in page_pool (the plan
+ * reads no page, so one plan serves the pools of every layer that shares the table,
+ * offsets and counts).  Does nothing if that plan failed. */
 int hp_gather_planned(const hp_paged_desc* desc, void* out, const void* workspace,
                       int* d_status, void* stream);
 
@@ -337,7 +339,8 @@ int hp_append_plan(const hp_paged_desc* desc, const void* new_ptr, uint64_t tota
                    void* workspace, uint64_t workspace_bytes, int* d_status, void* stream);
 
 /* ASYNC.  The copy step of hp_scatter_append, after hp_append_plan (with the same
- * new_ptr and total_new) on the same stream. */
+ * new_ptr and total_new, and a descriptor that differs at most in page_pool) on the same
+ * stream; one plan serves every layer's pool.  Does nothing if that plan failed. */
 int hp_scatter_append_planned(const hp_paged_desc* desc, const void* new_rows,
                               const void* new_ptr, uint64_t total_new, const void* workspace,
                               int* d_status, void* stream);
