@@ -278,3 +278,30 @@ def test_permissive_decode_step_skips_unwritable_rows(hp, oracle, fault):
                                                 pool=inputs.device_pool(w, "cuda"))
     assert code == fault and st == "HP_ERR_" + fault
     assert np.array_equal(got, want_pool)
+
+
+def test_one_append_plan_serves_the_pools_of_several_layers(hp, oracle):
+    """hp_append_plan once (a decode step: one row per sequence), then the planned append
+    into two pools (a layer's K and V) through descriptors that differ only in
+    page_pool: each pool matches the oracle's append into it."""
+    import torch
+    w = inputs.config("decode_append", "small")
+    b = Batch(w, lens=w.lens_before)
+    np_dev = index_tensor(w.new_ptr, "cuda")
+    assert hp.hp_append_plan(b.desc, np_dev, w.total_new, b.ws, b.status) == 0
+    for layer in range(2):
+        pl = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 950 + layer}),
+                                "cuda")
+        host = pl.cpu().numpy().copy()
+        rows = np.random.default_rng(layer).integers(0, 256, (w.total_new, w.row_bytes),
+                                                     dtype=np.uint8)
+        dl = hp.PagedDesc(pl, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages,
+                          page_size=w.page_size, num_heads=w.num_heads, head_dim=w.head_dim,
+                          dtype=w.dtype, index_type=b.it)
+        new = torch.from_numpy(rows.reshape(-1).copy()).to("cuda")
+        assert hp.hp_scatter_append_planned(dl, new, np_dev, w.total_new, b.ws, b.status) == 0
+        torch.cuda.synchronize()
+        assert b.status_value() == 0
+        o = b.oracle_desc(pool_host=host, lens=w.lens_before)
+        assert o.scatter_append(rows, w.new_ptr) == "OK"
+        assert np.array_equal(pl.cpu().numpy(), host)

@@ -356,3 +356,24 @@ def test_one_launch_gather_random_verdicts_and_rows(hp, oracle):
             assert (key >> 58, key & ((1 << 58) - 1)) == (ranks[code], first)
             assert (buf.cpu().numpy() == 0xEE).all()
     assert {"OK", "SEQ_PTR_START", "SEQ_PTR_ORDER", "SEQ_PTR_END", "PAGE_ID", "LEN"} <= seen
+
+
+def test_one_plan_serves_the_pools_of_several_layers(hp, oracle):
+    """hp_plan once, then hp_gather_planned through descriptors that differ only in
+    page_pool (one pool per layer): each output equals that pool's one-call gather."""
+    import torch
+    w = inputs.config("decode_gather", "small")
+    b = Batch(w)
+    assert hp.hp_plan(b.desc, w.total_tokens, b.ws, b.status) == 0
+    for layer in range(3):
+        pl = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 900 + layer}),
+                                "cuda")
+        dl = hp.PagedDesc(pl, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages,
+                          page_size=w.page_size, num_heads=w.num_heads, head_dim=w.head_dim,
+                          dtype=w.dtype, index_type=b.it)
+        got = torch.empty(w.total_tokens * w.row_bytes, dtype=torch.uint8, device="cuda")
+        assert hp.hp_gather_planned(dl, got, b.ws, b.status) == 0
+        torch.cuda.synchronize()
+        assert b.status_value() == 0
+        want = b.oracle_desc(pool_host=pl.cpu().numpy()).gather()[0]
+        assert np.array_equal(got.cpu().numpy().reshape(want.shape), want)
