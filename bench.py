@@ -696,6 +696,57 @@ def dequant_measurements(dev, hp, inputs, entry, med_ms):
     return out
 
 
+def decode_step_layers(dev, hp, inputs, entry, med_ms, layers=4, Hq=32):
+    """A decode step of a `layers`-layer model on the 32-sequence decode-append batch:
+    one append plan and one attention plan serve every layer, and each layer appends its
+    new K and V rows and runs attention through the shared block table.  Bytes: each
+    layer's K and V rows read once by attention, plus its appended rows (read + written)."""
+    import torch
+    w = inputs.config("decode_append", "mid")
+    kw = dict(num_pages=w.num_pages, page_size=w.page_size, num_heads=w.num_heads,
+              head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+    table, sp = idx_tensor(w.table, dev), idx_tensor(w.seq_ptr, dev)
+    before, after = idx_tensor(w.lens_before, dev), idx_tensor(w.lens, dev)
+    new_ptr = idx_tensor(w.new_ptr, dev)
+    new = inputs.device_new_rows(w, dev)
+    pools = []
+    for l in range(layers):
+        kp = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 2000 + 2 * l}), dev)
+        vp = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 2001 + 2 * l}), dev)
+        pools.append((kp, vp, hp.PagedDesc(kp, table, sp, before, **kw),
+                      hp.PagedDesc(vp, table, sp, before, **kw),
+                      hp.PagedDesc(kp, table, sp, after, **kw)))
+    g = torch.Generator(device=dev)
+    g.manual_seed(21)
+    q = torch.randn((w.num_seqs, Hq, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty((w.num_seqs, Hq, w.head_dim), dtype=torch.float32, device=dev)
+    d_before, d_after = pools[0][2], pools[0][4]
+    ws_a = hp.workspace_for(d_before, dev)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(d_after, Hq)
+    ws_t = torch.zeros(nws, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1 / np.sqrt(w.head_dim)
+
+    def step():
+        hp.hp_append_plan(d_before, new_ptr, w.total_new, ws_a, status)
+        for kp, vp, dk, dv, _ in pools:
+            hp.hp_scatter_append_planned(dk, new, new_ptr, w.total_new, ws_a, status)
+            hp.hp_scatter_append_planned(dv, new, new_ptr, w.total_new, ws_a, status)
+        hp.hp_attention_plan(d_after, Hq, ws_t, status)
+        for kp, vp, _, _, dka in pools:
+            hp.hp_attention_decode_planned(dka, vp, q, Hq, scale, out, ws_t, status)
+
+    ms = med_ms(step, n=10)
+    assert int(status.item()) == 0, hp.status_name(int(status.item()))
+    nbytes = layers * (2 * w.total_tokens * w.row_bytes + q.numel() * 2 + out.numel() * 4 +
+                       2 * 2 * w.total_new * w.row_bytes)
+    res = entry(nbytes, ms, note="%d layers of %d sequences: per step 1 append plan, %d "
+                "planned appends, 1 attention plan, %d planned attention calls" %
+                (layers, w.num_seqs, 2 * layers, layers))
+    del pools
+    return res
+
+
 def ops_measurements(dev, hp, inputs, peak, reps=20):
     """The other rows of the path at their own configurations (bytes as in
     gather_bytes; medians over reps, inputs larger than L2 except where noted)."""
@@ -850,6 +901,9 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     release_device_memory()
     out["decode_attention"] = attention_measurement(dev, hp, inputs, w, d_g, peak, entry, med_ms)
     del pool, new
+    release_device_memory()
+
+    out["decode_step_4_layers"] = decode_step_layers(dev, hp, inputs, entry, med_ms)
     release_device_memory()
 
     # kernel-internal [nb, H, D/x, bs, x] -> interchange [nb, bs, H, D], decode-gather pool
