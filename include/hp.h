@@ -27,12 +27,13 @@
  * - Pointers named d_* or described as "device" point to GPU memory of the
  *   current CUDA device; pointers described as "host" point to CPU memory.
  *   The page pool and the output of the gathers (dequantising ones included), the
- *   pool and new rows of the appends, the pool of hp_copy_pages and the buffers of
- *   the lane operations may instead be page-locked host memory (from the CUDA host
- *   allocator or cudaHostRegister, mapped): those operations then read and write it
- *   in place over the host link, on the register copy engine (checked per call
- *   with cudaPointerGetAttributes).  Index buffers, workspaces, status words and
- *   the other operations' buffers are device memory.
+ *   pool and new rows of the appends, the pool of hp_copy_pages, the buffers of the
+ *   lane operations and the K and V pools of decode attention may instead be
+ *   page-locked host memory (from the CUDA host allocator or cudaHostRegister,
+ *   mapped): those operations then read and write it in place over the host link
+ *   (the copies on the register engine, checked per call with
+ *   cudaPointerGetAttributes).  Index buffers, workspaces, status words and the
+ *   other operations' buffers are device memory.
  *   The caller owns every buffer.  The library allocates no device memory; the
  *   only state it keeps between calls is a per-device cache of launch facts (SM
  *   count, resident CTAs per kernel), filled on first use.  It is safe to call from

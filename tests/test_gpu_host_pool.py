@@ -141,3 +141,29 @@ def test_lane_gather_and_append_on_a_host_pool(hp, oracle):
     assert oracle.lane_append(host, C, P, T, B, H, W, n,
                               new.view(np.uint16).reshape(B, H, m, W)) == "OK"
     assert np.array_equal(hpool.numpy().reshape(-1), host.view(np.uint8).reshape(-1))
+
+
+def test_decode_attention_on_host_resident_k_and_v(hp, oracle):
+    """K and V pools in page-locked host memory (an offloaded cache): the kernel's cp.async
+    loads read them over the host link; the result is bit for bit the one from device
+    pools."""
+    import torch
+    w = inputs.decode_gather(seed=61, num_pages=400, page_size=16, num_heads=2, head_dim=128,
+                             num_seqs=4, len_lo=1, len_hi=1500, dtype="bf16")
+    b = Batch(w)
+    vdev = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 62}), "cuda")
+    khost, vhost = _pinned_copy(b.pool), _pinned_copy(vdev)
+    dh = hp.PagedDesc(khost, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages, page_size=16,
+                      num_heads=2, head_dim=128, dtype="bf16", index_type=b.it)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(63)
+    q = torch.randn((w.num_seqs, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+    rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, 8)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    want = torch.full((w.num_seqs, 8, 128), float("nan"), dtype=torch.float32, device="cuda")
+    got = torch.full_like(want, float("nan"))
+    assert hp.hp_attention_decode(b.desc, vdev, q, 8, 0.09, want, ws, b.status) == 0
+    assert hp.hp_attention_decode(dh, vhost, q, 8, 0.09, got, ws, b.status) == 0
+    torch.cuda.synchronize()
+    assert b.status_value() == 0
+    assert torch.equal(got.view(torch.int32), want.view(torch.int32))
