@@ -510,22 +510,29 @@ def rate_entry(bytes_, ms, peak, **kw):
     return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
 
 
-def attention_only(scale, dev, hp, inputs, peak, reps):
+def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False):
     """Decode attention alone on the decode-append batch at `scale` ("full": 256 sequences
     of 1K-32K tokens; "mid": 32 of them, about 2.5 GB on the device, the profiler's case;
-    "short": 2048 sequences of 16-1024 tokens)."""
+    "short": 2048 sequences of 16-1024 tokens); host_kv: K and V in page-locked host
+    memory."""
     import torch
     w = inputs.config("decode_append", scale)
     pool = inputs.device_pool(w, dev)
+    hk = None
+    if host_kv:
+        hk = torch.empty(pool.shape, dtype=pool.dtype, pin_memory=True)
+        hk.copy_(pool)
+        pool = hk
     d_k = hp.PagedDesc(pool, idx_tensor(w.table, dev), idx_tensor(w.seq_ptr, dev),
                        idx_tensor(w.lens, dev), num_pages=w.num_pages, page_size=w.page_size,
                        num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype, index_type=0)
     stream = torch.cuda.current_stream()
     res = attention_measurement(dev, hp, inputs, w, d_k, peak,
                                 lambda b, ms, **kw: rate_entry(b, ms, peak, **kw),
-                                lambda fn, n: median_ms(fn, stream, n), reps=reps)
+                                lambda fn, n: median_ms(fn, stream, n), reps=reps, host_kv=hk)
     res.update(op="decode_attention", workload=w.name, num_seqs=w.num_seqs,
-               total_tokens=w.total_tokens, num_heads=w.num_heads, head_dim=w.head_dim)
+               total_tokens=w.total_tokens, num_heads=w.num_heads, head_dim=w.head_dim,
+               kv_memory="page-locked host" if host_kv else "device")
     return res
 
 
@@ -624,12 +631,19 @@ def transpose_only(dev, hp, peak, reps, nb=10000, bsz=16, H=32, D=128, x=8):
     return res
 
 
-def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, reps=10):
+def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, reps=10,
+                          host_kv=None):
     """hp_attention_decode over batch w (K pool and descriptor d_k; a V pool of the same
-    geometry is drawn here): Hq query heads, bytes = K and V rows once + q + out."""
+    geometry is drawn here): Hq query heads, bytes = K and V rows once + q + out.
+    host_kv: a page-locked host copy of the K pool; then d_k reads it and V is copied to
+    page-locked host memory too (an offloaded cache read over the host link)."""
     import torch
     wv = inputs.Workload(**{**w.__dict__, "pool_seed": w.pool_seed + 77})
     vpool = inputs.device_pool(wv, dev)
+    if host_kv is not None:
+        vh = torch.empty(vpool.shape, dtype=vpool.dtype, pin_memory=True)
+        vh.copy_(vpool)
+        vpool = vh
     gq = torch.Generator(device=dev)
     gq.manual_seed(11)
     qd = torch.randn((w.num_seqs, Hq, w.head_dim), generator=gq, device=dev).to(torch.bfloat16)
@@ -951,6 +965,8 @@ def main():
     ap.add_argument("--attention", choices=["full", "mid", "short"],
                     help="time only hp_attention_decode on the decode-append batch at this "
                          "scale (warm-up calls, then --steps timed calls) and print its line")
+    ap.add_argument("--host-kv", action="store_true",
+                    help="with --attention: K and V pools in page-locked host memory")
     ap.add_argument("--transpose", action="store_true",
                     help="time only the two cache layout conversions (kernel-internal "
                          "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
@@ -1003,7 +1019,7 @@ def main():
         build.build()
         hp.lib()
         print(json.dumps(attention_only(args.attention, "cuda", hp, inputs, peak_hbm()[0],
-                                        args.steps)))
+                                        args.steps, host_kv=args.host_kv)))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
