@@ -965,6 +965,9 @@ def main():
     ap.add_argument("--attention", choices=["full", "mid", "short"],
                     help="time only hp_attention_decode on the decode-append batch at this "
                          "scale (warm-up calls, then --steps timed calls) and print its line")
+    ap.add_argument("--decode-layers", action="store_true",
+                    help="only the 4-layer decode step through the planned calls (32 "
+                         "sequences) and print its line")
     ap.add_argument("--host-kv", action="store_true",
                     help="with --attention: K and V pools in page-locked host memory")
     ap.add_argument("--transpose", action="store_true",
@@ -987,6 +990,17 @@ def main():
         build.build()
         hp.lib()
         print(json.dumps(lane_only("cuda", hp, inputs, peak_hbm()[0], args.steps)))
+        return
+    if args.decode_layers:
+        import torch
+        from paged_kv_cache_hp_gb300 import build, hp, inputs
+        build.build()
+        hp.lib()
+        peak = peak_hbm()[0]
+        stream = torch.cuda.current_stream()
+        print(json.dumps(decode_step_layers(
+            "cuda", hp, inputs, lambda b, ms, **kw: rate_entry(b, ms, peak, **kw),
+            lambda fn, n=10: median_ms(fn, stream, n))))
         return
     if args.dequant:
         import torch
