@@ -350,7 +350,8 @@ def e2e_gather_in_place(w, dev, hp, inputs, steps, host):
         d_idx = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_idx]
         desc = hp.PagedDesc(h_pool, d_idx[0], d_idx[1], d_idx[2], num_pages=w.num_pages,
                             page_size=w.page_size, num_heads=w.num_heads,
-                            head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+                            head_dim=w.head_dim, dtype=w.dtype, index_type=0,
+                            flags=hp.HOST_MEMORY)
         sets.append(dict(idx=d_idx, desc=desc, ws=hp.workspace_for(desc, dev),
                          status=torch.zeros(1, dtype=torch.int32, device=dev),
                          h_out=host["outs"][i]))

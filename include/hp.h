@@ -30,10 +30,11 @@
  *   pool and new rows of the appends, the pool of hp_copy_pages, the buffers of the
  *   lane operations and the K and V pools of decode attention may instead be
  *   page-locked host memory (from the CUDA host allocator or cudaHostRegister,
- *   mapped): those operations then read and write it in place over the host link
- *   (the copies on the register engine, checked per call with
- *   cudaPointerGetAttributes).  Index buffers, workspaces, status words and the
- *   other operations' buffers are device memory.
+ *   mapped): those operations then read and write it in place over the host link.
+ *   The caller says so with HP_HOST_MEMORY (the copies then take the register
+ *   engine); the library never asks the runtime where a pointer lives.  Index
+ *   buffers, workspaces, status words and the other operations' buffers are device
+ *   memory.
  *   The caller owns every buffer.  The library allocates no device memory; the
  *   only state it keeps between calls is a per-device cache of launch facts (SM
  *   count, resident CTAs per kernel), filled on first use.  It is safe to call from
@@ -132,6 +133,15 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
 #define HP_PERMISSIVE 0x1u /* [HF] Storage Invariants: a reader in permissive mode does not
                               reject descriptors that violate invariants (1)-(3)          */
 #define HP_HAS_QUANT 0x2u  /* [HF] Buffer Table: quantisation parameters present          */
+/* Memory placement (no counterpart in the pages, which describe device buffers): the page
+ * pool, the output or the new rows of the call may lie in page-locked host memory that
+ * the GPU reaches directly (cudaHostAlloc'd or cudaHostRegister'ed memory, e.g. a pool
+ * offloaded to Grace memory).  The copy then runs on the register engine, with ordinary
+ * loads and stores over the host link.  Without the flag every buffer must be device
+ * memory: the library asks the runtime nothing about a pointer, and its TMA engine is for
+ * device memory only.  In the descriptor's `flags`, and in the `flags` argument of
+ * hp_copy_pages, hp_lane_gather and hp_lane_append. */
+#define HP_HOST_MEMORY 0x4u
 /* Test hook for the bounded waits (no counterpart in the pages): the TMA copy engine sets
  * up the first load of each of its CTAs but never issues it, so the wait for it runs out
  * (after about 2 s), the call stores HP_ERR_TIMEOUT in *d_status and returns without
@@ -169,7 +179,8 @@ typedef struct hp_paged_desc {
     uint32_t rank;
     uint32_t paged_axis;
     uint32_t has_shard;
-    uint32_t flags;        /* HP_PERMISSIVE | HP_HAS_QUANT (| HP_TEST_STALL in tests) */
+    uint32_t flags;        /* HP_PERMISSIVE | HP_HAS_QUANT | HP_HOST_MEMORY
+                              (| HP_TEST_STALL in tests) */
     uint32_t dtype;        /* hp_dtype */
     uint32_t index_type;   /* hp_index_type */
     uint64_t num_pages;
@@ -328,7 +339,10 @@ int hp_gather_dequant_q_planned(const hp_paged_desc* desc, const hp_quant_desc* 
  * vector path.  With HP_PERMISSIVE the caller vouches for the descriptor: nothing is
  * validated up front, a row whose logical page lies outside its slice or the table is
  * skipped with HP_ERR_LEN in *d_status, one naming a page outside the pool with
- * HP_ERR_PAGE_ID.  An append of fewer than num_seqs*page_size rows (a decode step)
+ * HP_ERR_PAGE_ID; a sequence whose pair new_ptr[s] .. new_ptr[s+1] runs backwards or
+ * ends past total_new appends nothing (HP_ERR_NEW_PTR_ORDER / HP_ERR_NEW_PTR_END), so
+ * no row outside the total_new rows of `new_rows` is ever read, in either mode.  An
+ * append of fewer than num_seqs*page_size rows (a decode step)
  * runs as one kernel with one warp per sequence (after the plan when validated).
  */
 int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, const void* new_ptr,
@@ -360,11 +374,12 @@ int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, uint64_t 
  * arrays of num_pairs entries of `index_type` (HP_IDX_U32 / HP_IDX_U64).  A pair naming a
  * page >= num_pages copies nothing and stores HP_ERR_PAGE_ID in *d_status.  Destination
  * pages must differ from each other and from every source page (the result is otherwise
- * unspecified).  page_pool must be 64-byte aligned.
+ * unspecified).  page_pool must be 64-byte aligned.  flags: 0, or HP_HOST_MEMORY when
+ * page_pool is page-locked host memory.
  */
 int hp_copy_pages(void* page_pool, uint64_t num_pages, uint64_t page_bytes, uint32_t index_type,
                   const void* src_pages, const void* dst_pages, uint64_t num_pairs,
-                  int* d_status, void* stream);
+                  uint32_t flags, int* d_status, void* stream);
 
 /* Bytes of scratch hp_zero_tails needs for `desc`: one 32-bit word per page. */
 int hp_zero_tails_scratch_bytes(const hp_paged_desc* desc, uint64_t* bytes);
@@ -506,21 +521,24 @@ int hp_lane_validate(uint64_t capacity, uint64_t page_tokens, const uint64_t* ta
  * p%P)*d + f, for the n live positions p < n.  Requires n <= capacity
  * (HP_ERR_LENGTH).  The table is not validated here (hp_lane_validate does
  * that once); an entry >= N skips its rows and stores HP_ERR_PHYSICAL_PAGE in
- * *d_status.
+ * *d_status.  flags: 0, or HP_HOST_MEMORY when pool or out is page-locked host memory.
  */
 int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capacity,
                    uint64_t page_tokens, uint64_t batch, uint64_t kv_heads, uint64_t width,
-                   uint32_t dtype, uint64_t n, void* out, int* d_status, void* stream);
+                   uint32_t dtype, uint64_t n, void* out, uint32_t flags, int* d_status,
+                   void* stream);
 
 /*
  * ASYNC.  Append m rows per lane at positions n..n+m-1 (a decode step appends
  * one): element (b, h, i, f) of `new_rows` (device, [B, H_kv, m, d]) is written
  * to pool scalar ((table[p/P]*B*H_kv + b*H_kv + h)*P + p%P)*d + f with p = n+i.
- * Requires n + m <= capacity (HP_ERR_LENGTH, nothing written).
+ * Requires n + m <= capacity (HP_ERR_LENGTH, nothing written).  flags: 0, or
+ * HP_HOST_MEMORY when pool or new_rows is page-locked host memory.
  */
 int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity, uint64_t page_tokens,
                    uint64_t batch, uint64_t kv_heads, uint64_t width, uint32_t dtype,
-                   uint64_t n, uint64_t m, const void* new_rows, int* d_status, void* stream);
+                   uint64_t n, uint64_t m, const void* new_rows, uint32_t flags, int* d_status,
+                   void* stream);
 
 /* ---------------------------------------------------- no-allocation variant */
 /*
@@ -539,7 +557,10 @@ int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity, uint64_
  *   checked; use hp_gather with your own workspace for larger batches.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, which may also load the library's device code on that
- *   device); make that first call before any stream capture.
+ *   device) and keeps it for the life of the process; make that first call before any
+ *   stream capture.  Because the address is kept, resetting a device
+ *   (cudaDeviceReset) after its first call is not supported: the device code may load
+ *   elsewhere in the new context, and later calls would write through the stale address.
  * - All calls on a device share the one array.  Two calls whose work overlaps on the
  *   GPU (different streams, or different host threads, without ordering between them)
  *   race on it and may produce wrong output; order them, e.g. on one stream.  A call

@@ -92,7 +92,7 @@ def lib():
             L.or_gather_dequant.restype = i32
             L.or_gather_dequant.argtypes = [P(OrDesc), vp, vp]
             L.or_scatter_append.restype = i32
-            L.or_scatter_append.argtypes = [P(OrDesc), vp, vp]
+            L.or_scatter_append.argtypes = [P(OrDesc), vp, vp, u64]
             L.or_bf16_rne.restype = ctypes.c_uint16
             L.or_bf16_rne.argtypes = [ctypes.c_double]
             L.or_lane_new.restype = i32
@@ -305,11 +305,16 @@ class Desc:
                                   float(scale), _ptr(out))
         return out
 
-    def scatter_append(self, new_rows, new_ptr):
-        """Writes into self.pool in place; returns the fault name."""
+    def scatter_append(self, new_rows, new_ptr, total_new=None):
+        """Writes into self.pool in place; returns the fault name.  total_new is the
+        number of rows new_rows holds (by default, its byte size over one row's)."""
         npt = np.ascontiguousarray(new_ptr, dtype=self.seq_ptr.dtype)
         nr = np.ascontiguousarray(new_rows)
-        return code_name(lib().or_scatter_append(ctypes.byref(self.c), _ptr(nr), _ptr(npt)))
+        if total_new is None:
+            row_bytes = self.c.num_heads * self.c.head_dim * self.es
+            total_new = nr.nbytes // row_bytes if row_bytes else 0
+        return code_name(lib().or_scatter_append(ctypes.byref(self.c), _ptr(nr), _ptr(npt),
+                                                 int(total_new)))
 
 
 def bf16_rne(x: float) -> int:

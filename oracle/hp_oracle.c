@@ -485,17 +485,24 @@ int or_validate_append(const or_desc* d, const void* new_ptr, uint64_t total_new
  * t = seq_lens[s] + i, written through the same Element Lookup as the gather
  * ([HF] Element Lookup, applied as a store).  Sequences are visited in
  * increasing s, rows in increasing i.  A lookup that fails (permissive mode
- * only) writes nothing for that row; the first failure's code is returned. */
-int or_scatter_append(const or_desc* d, const void* new_rows, const void* new_ptr)
+ * only) writes nothing for that row.  The input holds total_new rows and no row
+ * outside it is read: a sequence whose pair new_ptr[s] .. new_ptr[s+1] runs
+ * backwards (NEW_PTR_ORDER) or past total_new (NEW_PTR_END) contributes no rows
+ * (permissive mode only; a validated append has neither).  The first failure's
+ * code is returned. */
+int or_scatter_append(const or_desc* d, const void* new_rows, const void* new_ptr,
+                      uint64_t total_new)
 {
     const uint64_t es = or_elem_size(d->dtype);
     const uint64_t H = d->num_heads, D = d->head_dim;
     int first_fault = OR_OK;
     for (uint64_t s = 0; s < d->num_seqs; ++s) {
-        const uint64_t base = ix(d, new_ptr, s);
-        const uint64_t n = ix(d, new_ptr, s + 1) - base;
-        if (ix(d, new_ptr, s + 1) < base) continue;
-        for (uint64_t i = 0; i < n; ++i) {
+        const uint64_t base = ix(d, new_ptr, s), end = ix(d, new_ptr, s + 1);
+        if (end < base || end > total_new) {
+            if (first_fault == OR_OK) first_fault = end < base ? OR_NEW_PTR_ORDER : OR_NEW_PTR_END;
+            continue;
+        }
+        for (uint64_t i = 0; i < end - base; ++i) {
             const uint64_t t = ix(d, d->seq_lens, s) + i;
             uint64_t flat;
             int c = lookup_flat(d, s, t, 0, 0, &flat, 0, 0);

@@ -141,20 +141,11 @@ hp::CopyArgs copy_args(const hp_paged_desc* d, const void* ws, int* d_status)
     return a;
 }
 
-// True for memory that is not device memory of a GPU: pinned host memory (page-locked and
-// mapped, e.g. Grace memory holding an offloaded pool) or pageable host memory.  Kernels
-// reach it with ordinary loads and stores over the host link; the TMA copy engine is kept
-// to device memory, so an operation touching host memory takes the register engine.
-bool host_resident(const void* p)
-{
-    if (!p) return false;
-    cudaPointerAttributes at{};
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return true;  // unknown: not a device allocation the TMA engine may assume
-    }
-    return at.type != cudaMemoryTypeDevice;
-}
+// HP_HOST_MEMORY: the caller's buffers may be page-locked host memory (e.g. Grace memory
+// holding an offloaded pool).  Kernels reach it with ordinary loads and stores over the
+// host link; the TMA copy engine is kept to device memory, so such an operation takes the
+// register engine.  The caller declares it; no runtime query runs per call.
+inline bool host_memory(uint32_t flags) { return (flags & HP_HOST_MEMORY) != 0; }
 
 // Units of at most 8 KiB keep an operation on the register engine (one warp per unit).
 constexpr u64 kRegisterEngineUnit = 8192;
@@ -249,8 +240,7 @@ int gather_planned(const hp_paged_desc* d, void* out, const void* ws, int* d_sta
         return hp::launch_copy(hp::kDequant, d->index_type == HP_IDX_U64, a, vec, stream);
     }
     vec = pick_vec(a.row_bytes, d->page_pool, out);
-    if (host_resident(d->page_pool) || host_resident(out))
-        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
+    if (host_memory(d->flags)) a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     return hp::launch_copy(hp::kGather, d->index_type == HP_IDX_U64, a, vec, stream);
 }
 
@@ -302,6 +292,7 @@ int append_planned(const hp_paged_desc* d, const void* new_rows, const void* new
     if (!new_ptr) return HP_ERR_NULL;
     hp::CopyArgs a = copy_args(d, ws, d_status);
     a.new_ptr = new_ptr;
+    a.total_new = total_new;
     if ((u128)total_new < (u128)d->num_seqs * d->page_size) {
         // decode-sized: one warp per sequence after the plan's verdict, no unit search
         a.src = static_cast<const char*>(new_rows);
@@ -317,8 +308,7 @@ int append_planned(const hp_paged_desc* d, const void* new_rows, const void* new
     a.dst = static_cast<char*>(const_cast<void*>(d->page_pool));
     if (!a.src) a.src = reinterpret_cast<const char*>(d->page_pool);  // no rows: never read
     const int vec = pick_vec(a.row_bytes, a.src, d->page_pool);
-    if (host_resident(d->page_pool) || host_resident(new_rows))
-        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
+    if (host_memory(d->flags)) a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     return hp::launch_copy(hp::kAppend, d->index_type == HP_IDX_U64, a, vec, stream);
 }
 
@@ -560,6 +550,7 @@ HP_API int hp_scatter_append(const hp_paged_desc* desc, const void* new_rows, co
         hp::CopyArgs a = copy_args(desc, workspace, d_status);
         a.hdr = nullptr;  // no plan to wait for
         a.new_ptr = new_ptr;
+        a.total_new = total_new;  // bounds the rows read: new_ptr is not validated
         a.src = static_cast<const char*>(new_rows);
         a.dst = static_cast<char*>(const_cast<void*>(desc->page_pool));
         if (!a.src) a.src = reinterpret_cast<const char*>(desc->page_pool);  // never read
@@ -586,7 +577,7 @@ HP_API int hp_validate_append(const hp_paged_desc* desc, const void* new_ptr, ui
 
 HP_API int hp_copy_pages(void* page_pool, uint64_t num_pages, uint64_t page_bytes,
                          uint32_t index_type, const void* src_pages, const void* dst_pages,
-                         uint64_t num_pairs, int* d_status, void* stream)
+                         uint64_t num_pairs, uint32_t flags, int* d_status, void* stream)
 {
     if (index_type != HP_IDX_U32 && index_type != HP_IDX_U64) return HP_ERR_INDEX_TYPE;
     if (page_bytes == 0) return HP_ERR_ZERO_DIM;
@@ -606,8 +597,8 @@ HP_API int hp_copy_pages(void* page_pool, uint64_t num_pages, uint64_t page_byte
     a.src = static_cast<const char*>(page_pool);
     a.dst = static_cast<char*>(page_pool);
     a.row_bytes = page_bytes;
-    a.unit_bytes = host_resident(page_pool) ? std::min<u64>(page_bytes, kRegisterEngineUnit)
-                                            : page_bytes;
+    a.unit_bytes = host_memory(flags) ? std::min<u64>(page_bytes, kRegisterEngineUnit)
+                                      : page_bytes;
     a.d_status = d_status;
     return hp::launch_copy(hp::kCopyPages, index_type == HP_IDX_U64, a,
                            pick_vec(page_bytes, page_pool, page_pool), stream);
@@ -938,7 +929,8 @@ HP_API int hp_lane_validate(uint64_t capacity, uint64_t page_tokens, const uint6
 
 HP_API int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capacity,
                           uint64_t page_tokens, uint64_t batch, uint64_t kv_heads, uint64_t width,
-                          uint32_t dtype, uint64_t n, void* out, int* d_status, void* stream)
+                          uint32_t dtype, uint64_t n, void* out, uint32_t flags, int* d_status,
+                          void* stream)
 {
     u64 pages = 0, rb = 0;
     int rc = check_lane(pool, table, capacity, page_tokens, batch, kv_heads, width, dtype, &pages,
@@ -961,8 +953,7 @@ HP_API int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capa
     a.dst = static_cast<char*>(out);
     a.row_bytes = rb;
     a.unit_bytes = page_tokens * rb;
-    if (host_resident(pool) || host_resident(out))
-        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
+    if (host_memory(flags)) a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     a.d_status = d_status;
     return hp::launch_copy(hp::kLaneGather, 1, a, pick_vec(rb, pool, out), stream);
 }
@@ -970,7 +961,7 @@ HP_API int hp_lane_gather(const void* pool, const uint64_t* table, uint64_t capa
 HP_API int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity,
                           uint64_t page_tokens, uint64_t batch, uint64_t kv_heads, uint64_t width,
                           uint32_t dtype, uint64_t n, uint64_t m, const void* new_rows,
-                          int* d_status, void* stream)
+                          uint32_t flags, int* d_status, void* stream)
 {
     u64 pages = 0, rb = 0;
     int rc = check_lane(pool, table, capacity, page_tokens, batch, kv_heads, width, dtype, &pages,
@@ -994,8 +985,7 @@ HP_API int hp_lane_append(void* pool, const uint64_t* table, uint64_t capacity,
     a.dst = static_cast<char*>(pool);
     a.row_bytes = rb;
     a.unit_bytes = page_tokens * rb;
-    if (host_resident(pool) || host_resident(new_rows))
-        a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
+    if (host_memory(flags)) a.unit_bytes = std::min<u64>(a.unit_bytes, kRegisterEngineUnit);
     a.d_status = d_status;
     return hp::launch_copy(hp::kLaneAppend, 1, a, pick_vec(rb, new_rows, pool), stream);
 }

@@ -31,7 +31,9 @@ constexpr int kMaxDevices = 256;
 std::mutex g_lock;
 void* g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device ordinal
 
-// The scratch's device address on the current device, looked up once per device.
+// The scratch's device address on the current device, looked up once per device and kept
+// for the process.  A cudaDeviceReset after the first call would leave it stale (the module
+// may load elsewhere in the new context); the header states that this is not supported.
 int scratch_on_current_device(void** out)
 {
     int dev = 0;

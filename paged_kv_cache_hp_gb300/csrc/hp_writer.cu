@@ -23,7 +23,10 @@
 //                slot (len_s + i) mod P of page block_table[seq_ptr[s] + (len_s + i) / P].
 //                The row loads go out together with the block-table lookup.  A row whose
 //                logical page lies outside the slice or the table is skipped with
-//                HP_ERR_LEN, one naming a page outside the pool with HP_ERR_PAGE_ID.
+//                HP_ERR_LEN, one naming a page outside the pool with HP_ERR_PAGE_ID; a
+//                sequence whose new_ptr pair runs backwards or past total_new (possible
+//                only without a plan) is skipped whole with HP_ERR_NEW_PTR_ORDER or
+//                HP_ERR_NEW_PTR_END, so no input row past total_new is read.
 #include <cuda_runtime.h>
 
 #include "hp_internal.cuh"
@@ -127,7 +130,10 @@ __global__ void __launch_bounds__(256) append_rows_kernel(const CopyArgs a)
          s < a.num_seqs; s += warps) {
         const uint64_t r0 = np[s], r1 = np[s + 1], len = lens[s];
         const uint64_t lo = sp[s], hi = sp[s + 1];
-        if (r1 < r0) continue;
+        if (r1 < r0 || r1 > a.total_new) {  // permissive only: a plan's verdict rules it out
+            report(a.d_status, r1 < r0 ? HP_ERR_NEW_PTR_ORDER : HP_ERR_NEW_PTR_END);
+            continue;  // no row of the input outside [0, total_new) is read
+        }
         for (uint64_t i = 0; i < r1 - r0; ++i) {
             const T* src = reinterpret_cast<const T*>(a.src + (r0 + i) * a.row_bytes);
             T held[kHeld];  // the row's first vectors, loaded before the table lookup lands

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "libhp.so")
 HP_OK = 0
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "u8": 4, "f64": 5}
 IDX_U32, IDX_U64 = 0, 1
-PERMISSIVE, HAS_QUANT, TEST_STALL = 0x1, 0x2, 0x100
+PERMISSIVE, HAS_QUANT, HOST_MEMORY, TEST_STALL = 0x1, 0x2, 0x4, 0x100
 
 _lock = threading.Lock()
 _lib = None
@@ -83,11 +83,12 @@ def lib():
                 "hp_validate_append": (i, [D, vp, u64, vp, u64, pu64, vp]),
                 "hp_lane_validate": (i, [u64, u64, vp, u64, pu64]),
                 "hp_lane_gather": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32, u64,
-                                       vp, vp, vp]),
+                                       vp, ctypes.c_uint32, vp, vp]),
                 "hp_lane_append": (i, [vp, vp, u64, u64, u64, u64, u64, ctypes.c_uint32, u64,
-                                       u64, vp, vp, vp]),
+                                       u64, vp, ctypes.c_uint32, vp, vp]),
                 "hp_gather_noalloc": (i, [D, vp, u64, vp, vp]),
-                "hp_copy_pages": (i, [vp, u64, u64, ctypes.c_uint32, vp, vp, u64, vp, vp]),
+                "hp_copy_pages": (i, [vp, u64, u64, ctypes.c_uint32, vp, vp, u64, ctypes.c_uint32,
+                                      vp, vp]),
                 "hp_attention_decode_workspace_bytes": (i, [D, ctypes.c_uint32, pu64]),
                 "hp_attention_decode": (i, [D, vp, vp, ctypes.c_uint32, ctypes.c_float, vp, vp,
                                             u64, vp, vp]),
@@ -238,17 +239,18 @@ def hp_lane_validate(capacity, page_tokens, table_host):
 
 
 def hp_lane_gather(pool, table, capacity, page_tokens, batch, kv_heads, width, dtype, n, out,
-                   d_status=None, stream=None):
+                   d_status=None, stream=None, flags=0):
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     return lib().hp_lane_gather(_p(pool), _p(table), capacity, page_tokens, batch, kv_heads,
-                                width, dt, n, _p(out), _p(d_status), _stream(stream))
+                                width, dt, n, _p(out), flags, _p(d_status), _stream(stream))
 
 
 def hp_lane_append(pool, table, capacity, page_tokens, batch, kv_heads, width, dtype, n, m,
-                   new_rows, d_status=None, stream=None):
+                   new_rows, d_status=None, stream=None, flags=0):
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     return lib().hp_lane_append(_p(pool), _p(table), capacity, page_tokens, batch, kv_heads,
-                                width, dt, n, m, _p(new_rows), _p(d_status), _stream(stream))
+                                width, dt, n, m, _p(new_rows), flags, _p(d_status),
+                                _stream(stream))
 
 
 def hp_gather_dequant_q(desc, quant, out, out_tokens, workspace, d_status=None, stream=None):
@@ -265,9 +267,9 @@ def hp_gather_dequant_q_planned(desc, quant, out, workspace, d_status=None, stre
 
 
 def hp_copy_pages(pool, num_pages, page_bytes, index_type, src_pages, dst_pages, num_pairs,
-                  d_status=None, stream=None):
+                  d_status=None, stream=None, flags=0):
     return lib().hp_copy_pages(_p(pool), num_pages, page_bytes, index_type, _p(src_pages),
-                               _p(dst_pages), num_pairs, _p(d_status), _stream(stream))
+                               _p(dst_pages), num_pairs, flags, _p(d_status), _stream(stream))
 
 
 def hp_zero_tails_scratch_bytes(desc):

@@ -146,16 +146,16 @@ def test_lane_validate_matches_oracle(hpc, oracle):
 def test_lane_host_checks(hpc):
     L = hpc.lib()
     pool, table, out = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
-    assert hpc.status_name(L.hp_lane_gather(pool, table, 12, 3, 1, 2, 2, 5, 13, out, None, None)) \
+    assert hpc.status_name(L.hp_lane_gather(pool, table, 12, 3, 1, 2, 2, 5, 13, out, 0, None, None)) \
         == "HP_ERR_LENGTH"
-    assert hpc.status_name(L.hp_lane_gather(pool, table, 12, 3, 0, 2, 2, 5, 1, out, None, None)) \
+    assert hpc.status_name(L.hp_lane_gather(pool, table, 12, 3, 0, 2, 2, 5, 1, out, 0, None, None)) \
         == "HP_ERR_ZERO_DIM"
-    assert hpc.status_name(L.hp_lane_gather(pool, table, 12, 3, 1, 2, 2, 9, 1, out, None, None)) \
+    assert hpc.status_name(L.hp_lane_gather(pool, table, 12, 3, 1, 2, 2, 9, 1, out, 0, None, None)) \
         == "HP_ERR_DTYPE"
-    assert hpc.status_name(L.hp_lane_append(pool, table, 12, 3, 1, 2, 2, 5, 7, 6, out, None,
-                                            None)) == "HP_ERR_LENGTH"
+    assert hpc.status_name(L.hp_lane_append(pool, table, 12, 3, 1, 2, 2, 5, 7, 6, out, 0,
+                                            None, None)) == "HP_ERR_LENGTH"
     assert hpc.status_name(L.hp_lane_gather(pool, table, 1 << 62, 1, 1 << 10, 2, 2, 5, 1, out,
-                                            None, None)) == "HP_ERR_LANE_OVERFLOW"
+                                            0, None, None)) == "HP_ERR_LANE_OVERFLOW"
 
 
 @pytest.mark.parametrize("num_seqs,num_heads,G,D", [

@@ -1,6 +1,7 @@
 """GPU parity of the operations on a page pool (or an output) in page-locked host memory:
-the kernels read and write it in place over the host link (the register copy engine; the
-TMA engine is kept to device memory).  Bit-exact against the oracle, like every copy."""
+the kernels read and write it in place over the host link (the caller sets HP_HOST_MEMORY,
+which sends the copies to the register engine; the TMA engine is kept to device memory).
+Bit-exact against the oracle, like every copy."""
 import numpy as np
 import pytest
 
@@ -26,7 +27,7 @@ def test_gather_from_a_host_pool(hp, oracle, name, out_on_host):
     w = inputs.config(name, "small")
     dev = Batch(w)
     host_pool = _pinned_copy(dev.pool)
-    b = Batch(w, pool=host_pool)
+    b = Batch(w, pool=host_pool, flags=hp.HOST_MEMORY)
     T = w.total_tokens
     if out_on_host:
         out = torch.full((T * w.row_bytes,), 0xEE, dtype=torch.uint8, pin_memory=True)
@@ -54,7 +55,7 @@ def test_bulk_append_into_a_host_pool_then_gather(hp, oracle):
     new_ptr = index_tensor(np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))])
                            .astype(np.uint32), "cuda")
     zeros = np.zeros(w.num_seqs, dtype=np.uint32)
-    a = Batch(w, pool=pool, lens=zeros)
+    a = Batch(w, pool=pool, lens=zeros, flags=hp.HOST_MEMORY)
     assert hp.hp_scatter_append(a.desc, new, new_ptr, T, a.ws, a.status) == 0
     torch.cuda.synchronize()
     assert a.status_value() == 0
@@ -64,7 +65,7 @@ def test_bulk_append_into_a_host_pool_then_gather(hp, oracle):
     np_host = np.concatenate([[0], np.cumsum(w.lens.astype(np.int64))]).astype(np.uint32)
     assert o.scatter_append(rows, np_host) == "OK"
     assert np.array_equal(pool.numpy(), want_pool)
-    g = Batch(w, pool=pool)
+    g = Batch(w, pool=pool, flags=hp.HOST_MEMORY)
     out = torch.empty(T * w.row_bytes, dtype=torch.uint8, device="cuda")
     assert hp.hp_gather(g.desc, out, T, g.ws, g.status) == 0
     torch.cuda.synchronize()
@@ -81,7 +82,7 @@ def test_copy_pages_in_a_host_pool(hp, oracle):
     dst = (32 + rng.choice(32, 20, replace=False)).astype(np.uint32)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = hp.hp_copy_pages(pool, pages, page_bytes, 0, index_tensor(src, "cuda"),
-                          index_tensor(dst, "cuda"), 20, st)
+                          index_tensor(dst, "cuda"), 20, st, flags=hp.HOST_MEMORY)
     torch.cuda.synchronize()
     assert rc == 0 and st.item() == 0
     want = host.reshape(pages, page_bytes).copy()
@@ -97,7 +98,7 @@ def test_dequant_gather_from_a_host_pool(hp, oracle, out_on_host):
     import torch
     w = inputs.config("quantized_pool", "small")
     dev = Batch(w)
-    b = Batch(w, pool=_pinned_copy(dev.pool))
+    b = Batch(w, pool=_pinned_copy(dev.pool), flags=hp.HOST_MEMORY)
     T = w.total_tokens
     n = T * w.num_heads * w.head_dim
     kw = dict(pin_memory=True) if out_on_host else dict(device="cuda")
@@ -125,7 +126,8 @@ def test_lane_gather_and_append_on_a_host_pool(hp, oracle):
     st = torch.full((1,), 9, dtype=torch.int32, device="cuda")
     n = 777
     out = torch.full((B * H * n * W * 2,), 0xEE, dtype=torch.uint8, pin_memory=True)
-    assert hp.hp_lane_gather(hpool, dT, C, P, B, H, W, "bf16", n, out, st) == 0
+    assert hp.hp_lane_gather(hpool, dT, C, P, B, H, W, "bf16", n, out, st,
+                             flags=hp.HOST_MEMORY) == 0
     torch.cuda.synchronize()
     assert st.item() == 0
     pool_t = pool.view(np.uint16).reshape(N, B, H, P, W)
@@ -134,7 +136,8 @@ def test_lane_gather_and_append_on_a_host_pool(hp, oracle):
     m = 150
     new = rng.integers(0, 256, (B, H, m, W * 2), dtype=np.uint8)
     hnew = torch.from_numpy(new.copy()).pin_memory()
-    assert hp.hp_lane_append(hpool, dT, C, P, B, H, W, "bf16", n, m, hnew, st) == 0
+    assert hp.hp_lane_append(hpool, dT, C, P, B, H, W, "bf16", n, m, hnew, st,
+                             flags=hp.HOST_MEMORY) == 0
     torch.cuda.synchronize()
     assert st.item() == 0
     host = pool_t.copy()

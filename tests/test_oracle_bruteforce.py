@@ -86,6 +86,55 @@ def test_append_matches_ndarray_indexing(oracle, seed):
 
 
 @pytest.mark.parametrize("seed", range(20))
+def test_permissive_append_reads_no_row_past_total_new(oracle, seed):
+    """A permissive append whose new_ptr runs backwards or past total_new: those
+    sequences contribute no rows (the first such pair's code is returned), the others
+    land as numpy indexing puts them, and no input row at or past total_new is read (the
+    input buffer is cut to exactly total_new rows, so a read past it would take bytes
+    from a guard that the reference never writes)."""
+    rng = np.random.default_rng(300 + seed)
+    S, P, H, D, N, full, table, seq_ptr = random_batch(rng, alias=False)
+    if S < 2:
+        return
+    before = [int(rng.integers(0, n + 1)) for n in full]
+    new_n = [f - b for f, b in zip(full, before)]
+    new_ptr = np.concatenate([[0], np.cumsum(new_n)]).astype(np.int64)
+    total_new = int(new_ptr[-1])
+    starts = [s for s in range(S) if new_ptr[s] > 0]
+    if seed % 2 == 0 or not starts:  # the last pair ends past total_new
+        new_ptr[S] = total_new + 1 + int(rng.integers(0, 3))
+    else:  # one pair runs backwards
+        bad = starts[int(rng.integers(0, len(starts)))]
+        new_ptr[bad + 1] = new_ptr[bad] - 1
+    pool = rng.integers(0, 256, (N, P, H, D, 2), dtype=np.uint8)
+    ref = pool.copy()
+    guard = np.full((total_new + 8, H, D, 2), 0xEE, dtype=np.uint8)
+    guard[:total_new] = rng.integers(0, 256, (total_new, H, D, 2), dtype=np.uint8)
+    new = guard[:total_new]
+    desc = oracle.Desc(pool, table if table else None, seq_ptr, before, num_pages=N, page_size=P,
+                       num_heads=H, head_dim=D, dtype="f16", index_type=1, flags=1)
+    code = desc.scatter_append(new, new_ptr, total_new)
+    skipped = set()
+    first = "OK"
+    for s in range(S):
+        a, b = int(new_ptr[s]), int(new_ptr[s + 1])
+        if b < a or b > total_new:
+            skipped.add(s)
+            if first == "OK":
+                first = "NEW_PTR_ORDER" if b < a else "NEW_PTR_END"
+            continue
+        for i in range(b - a):
+            t = before[s] + i
+            if t // P >= seq_ptr[s + 1] - seq_ptr[s]:
+                if first == "OK":
+                    first = "LEN"
+                continue
+            ref[table[seq_ptr[s] + t // P], t % P] = new[a + i]
+    assert code == first and skipped
+    assert np.array_equal(pool, ref)
+
+
+@pytest.mark.parametrize("seed", range(20))
 def test_dequant_gather_matches_ndarray_indexing(oracle, seed):
     import torch
     rng = np.random.default_rng(200 + seed)
