@@ -102,27 +102,33 @@ class BlockAllocator:
 
 
 class RequestState:
-    """One request's block table: ceil(prompt/bs) blocks at admission, one more
-    block each time the token count passes a block boundary."""
+    """A request's share of the cache: its token count and, in logical order, the
+    physical blocks holding those tokens.  The invariant kept is that the table has
+    exactly ceil(num_tokens / block_size) blocks: admission sizes it for the prompt,
+    and a token that opens a new block draws one more from the allocator (the trace of
+    "Visualizing the layout": a 4-block request grows to 4 + 1 blocks when its 10 new
+    tokens cross one boundary).  Releasing hands every block back, first to last."""
 
     def __init__(self, request_id, prompt_len: int, allocator: BlockAllocator):
         self.request_id = request_id
-        self.num_tokens = prompt_len
-        self.block_table = []
         self.allocator = allocator
-        bs = allocator.block_size
-        for _ in range((prompt_len + bs - 1) // bs):
-            self.block_table.append(allocator.allocate())
+        self.block_table = []
+        self.num_tokens = 0
+        self._grow_to(prompt_len)
 
-    def append_token(self) -> None:
-        self.num_tokens += 1
-        if self.num_tokens % self.allocator.block_size == 1 and self.num_tokens > 1:
+    def _grow_to(self, tokens: int) -> None:
+        self.num_tokens = tokens
+        bs = self.allocator.block_size
+        while len(self.block_table) * bs < tokens:
             self.block_table.append(self.allocator.allocate())
 
+    def append_token(self) -> None:
+        self._grow_to(self.num_tokens + 1)
+
     def release(self) -> None:
-        for block_id in self.block_table:
+        held, self.block_table = self.block_table, []
+        for block_id in held:
             self.allocator.free(block_id)
-        self.block_table = []
 
 
 # --------------------------------------------------------------------------- workloads

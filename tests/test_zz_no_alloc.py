@@ -4,8 +4,8 @@ Some callers have no way to allocate device memory -- a plugin inside a framewor
 owns the device's memory budget, or a latency-critical loop that must not call
 cudaMalloc/cudaFree.  hp_gather_noalloc serves them with a workspace array the library
 carries in its own device memory.  These tests call it through the C ABI and check that
-its output equals hp_gather's (bit for bit, the gather's bar) on consecutive calls that
-share that array.  This file is collected last on purpose.
+its output equals hp_gather's and the CPU oracle's gather (bit for bit, the gather's bar)
+on consecutive calls that share that array.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -39,11 +39,15 @@ def test_noalloc_equals_gather_on_consecutive_calls(hp, oracle):
     for name in ("prefix_sharing", "decode_gather", "prefix_sharing"):
         w = inputs.config(name, "small")
         b = Batch(w)
+        want, written, fault = b.oracle_desc().gather()
+        assert fault == "OK" and written.all()
         ref, out = _both(hp, b, w.total_tokens)
         assert np.array_equal(out.cpu().numpy(), ref.cpu().numpy())
+        assert np.array_equal(out.cpu().numpy().reshape(want.shape), want)
         # and once more on the same batch
         ref2, out2 = _both(hp, b, w.total_tokens)
         assert np.array_equal(out2.cpu().numpy(), ref.cpu().numpy())
+        assert np.array_equal(out2.cpu().numpy().reshape(want.shape), want)
 
 
 def test_noalloc_at_its_sequence_limit(hp, oracle):
@@ -55,6 +59,8 @@ def test_noalloc_at_its_sequence_limit(hp, oracle):
     b = Batch(w)
     ref, out = _both(hp, b, w.total_tokens)
     assert np.array_equal(out.cpu().numpy(), ref.cpu().numpy())
+    want = b.oracle_desc().gather()[0]
+    assert np.array_equal(out.cpu().numpy().reshape(want.shape), want)
     big = hp.HpPagedDesc()
     ctypes.memmove(ctypes.byref(big), b.desc.ref, ctypes.sizeof(big))
     big.num_seqs = MAX_SEQS + 1
