@@ -128,3 +128,29 @@ def test_lane_recipes():
     s = inputs.lane_synthetic()
     assert sorted(s.table.tolist()) == list(range(s.pages))
     assert 0 < s.n <= s.capacity
+
+
+def test_whole_output_comparison_catches_one_wrong_byte(oracle):
+    """The group-by-group comparison the full-size GPU tests use: on a small batch, rows
+    built by numpy's own indexing pass, and the same rows with one byte changed (in any
+    group) fail, naming the first bad row."""
+    from helpers import compare_whole_gather, sequence_groups
+    w = inputs.config("decode_gather", "small")
+    pool = inputs.host_pool(w)
+    P = w.page_size
+    rows = []
+    for s in range(w.num_seqs):
+        lo = int(w.seq_ptr[s])
+        for t in range(int(w.lens[s])):
+            rows.append(pool[int(w.table[lo + t // P]), t % P])
+    want = np.stack(rows)
+    groups = sequence_groups(w.lens, 300)
+    assert len(groups) > 2 and groups[-1][3] == len(want)
+    assert compare_whole_gather(oracle, w, pool, w.lens, lambda a, b: want[a:b],
+                                group_tokens=300) == len(want)
+    for bad_row in (0, len(want) // 2, len(want) - 1):
+        wrong = want.copy()
+        wrong[bad_row, 5] ^= 1
+        with pytest.raises(AssertionError, match="first at row %d" % bad_row):
+            compare_whole_gather(oracle, w, pool, w.lens, lambda a, b: wrong[a:b],
+                                 group_tokens=300)
