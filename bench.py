@@ -1,17 +1,21 @@
 #!/usr/bin/env python
 """Benchmark of the block-paged KV-cache hot path on GB300.
 
-One step = one pass of the path over the decode-sized gather batch (fp16 pool of
-10000 pages x 16 slots x 32 heads x 128 dims, 64 sequences of U[512, 4096] tokens,
-uint32 block tables from a shuffled free list): hp_plan (device validation of the
-descriptor + ragged prefix sums) then hp_gather_planned (the page-span copy), both
-through the C ABI.  The metric is effective HBM GB/s (algorithmic bytes read and
-written per step / step time).
+One step = one pass of the path over the decode-step batch (bf16 GQA pool of 300,000
+pages x 16 slots x 8 K/V heads x 128 dims, 256 sequences of U[1024, 32768] tokens,
+uint32 block tables from a shuffled free list), all through the C ABI:
+hp_scatter_append of one new row per sequence at its token count (validated on the
+device: plan, table check, one warp per sequence), then hp_plan (device validation of
+the grown batch + ragged prefix sums) and hp_gather_planned (the page-span copy of all
+4.37M tokens).  The metric is effective HBM GB/s (algorithmic bytes read and written
+per step / step time).
 
-Printed: one JSON line (rank 0) with the headline value, the roofline of the copy
-kernel, the CPU oracle timed on a bounded sample, an end-to-end figure through host
-buffers, and per-operation measurements of the other rows of the path (append,
-prefix sharing, dequantising gather, per-lane layout).
+Printed: one JSON line (rank 0) with the headline value, the roofline of the gather's
+copy kernel, the CPU oracle timed on the same step, an end-to-end figure through pinned
+host buffers, and per-operation measurements: the other benchmark configurations (tiny
+prefix gather, decode-sized gather, prefix sharing, int8 dequantising gather), each with
+its roofline fraction, DRAM traffic record and CPU oracle baseline, and the other rows of
+the path (append, schemes, lane layout, writer side, attention, layout conversions).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 Under torchrun each rank runs its own replica of the batch on its own GPU (no
@@ -58,10 +62,18 @@ def source_hash(paths):
     return m.hexdigest()[:16]
 
 
+# Workloads whose DRAM traffic record comes from a smaller capture of the same kernel on
+# the same length distribution (the full size is above the profiler's size rule): the
+# record's bytes per unit (page span) times this launch's units.
+TRAFFIC_FROM = {"gather_decode_append": "gather_decode_append_mid",
+                "gather_quantized_pool": "gather_quantized_pool_mid"}
+
+
 def recorded_traffic(kernel_key, units_now):
     """DRAM bytes per launch from a committed ncu summary, scaled to this launch's
     units, or None when the summary is absent or the kernel source changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    kernel_key = TRAFFIC_FROM.get(kernel_key, kernel_key)
     try:
         with open(path) as f:
             rec = json.load(f)[kernel_key]
@@ -152,6 +164,31 @@ def validate_bytes(w):
     return len(w.table) * ib + (2 * w.num_seqs + 1) * ib
 
 
+def dequant_bytes(w, lens=None):
+    """Algorithmic bytes of one dequantising gather: per row the int8 codes read, the bf16
+    row written and its 4-byte scale; 8 bytes of block table per page span."""
+    lens = (w.lens if lens is None else lens).astype(np.int64)
+    T = int(lens.sum())
+    spans = int((-(-lens // w.page_size)).sum())
+    return T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8, spans
+
+
+def append_bytes(w):
+    """Algorithmic bytes of the decode-step append: every new row read and written once,
+    one block-table entry per row, the new_ptr offsets."""
+    ib = 4 if w.index_dtype == np.uint32 else 8
+    return 2 * w.total_new * w.row_bytes + w.total_new * ib + (w.num_seqs + 1) * ib
+
+
+def unique_gather_bytes(w):
+    """The bytes a gather must move from and to DRAM at least: each physical page's live
+    rows once however many sequences read them (the prefix pages of a shared prompt
+    once), the output rows, the block table."""
+    ib = 4 if w.index_dtype == np.uint32 else 8
+    lens = w.lens.astype(np.int64)
+    return (int(w.live_slots().sum()) + int(lens.sum())) * w.row_bytes + len(w.table) * ib
+
+
 def max_over_ranks(x, dist, device):
     """The largest value of x over all ranks (x itself without a process group)."""
     if dist is None:
@@ -192,6 +229,9 @@ class GatherStep:
         self.out = torch.empty(ob, dtype=torch.uint8, device=dev)
         self.status = torch.full((1,), -12345, dtype=torch.int32, device=dev)
 
+    launches = 3  # plan, table check, copy
+    kernel = "bulk_kernel<gather> (hp_gather_planned)"
+
     def plan(self, stream):
         rc = self.hp.hp_plan(self.desc, self.T, self.ws, self.status, stream=stream)
         assert rc == 0, self.hp.status_name(rc)
@@ -201,18 +241,74 @@ class GatherStep:
         rc = f(self.desc, self.out, self.ws, self.status, stream=stream)
         assert rc == 0, self.hp.status_name(rc)
 
+    def run(self, stream):
+        self.plan(stream)
+        self.copy(stream)
+
     def check_status(self):
         st = int(self.status.item())
         assert st == 0, self.hp.status_name(st)
 
 
+class DecodeAppendStep:
+    """Resident device buffers of the decode-step batch and the three C-ABI calls of one
+    step: hp_scatter_append of one new row per sequence at its count (validated: plan,
+    table check, row kernel), then hp_plan and hp_gather_planned of the grown batch.  The
+    counts are not advanced between steps, so every step appends the same rows at the same
+    slots and gathers the same tokens: identical work each time."""
+
+    launches = 6  # append plan, table check, row kernel; gather plan, table check, copy
+    kernel = "bulk_kernel<gather> (hp_gather_planned)"
+
+    def __init__(self, w, dev, hp, inputs):
+        import torch
+        self.w, self.hp = w, hp
+        self.pool = inputs.device_pool(w, dev)
+        self.table = idx_tensor(w.table, dev)
+        self.seq_ptr = idx_tensor(w.seq_ptr, dev)
+        self.before = idx_tensor(w.lens_before, dev)
+        self.after = idx_tensor(w.lens, dev)
+        self.new_ptr = idx_tensor(w.new_ptr, dev)
+        self.new = inputs.device_new_rows(w, dev)
+        kw = dict(num_pages=w.num_pages, page_size=w.page_size, num_heads=w.num_heads,
+                  head_dim=w.head_dim, dtype=w.dtype,
+                  index_type=0 if w.index_dtype == np.uint32 else 1)
+        self.d_app = hp.PagedDesc(self.pool, self.table, self.seq_ptr, self.before, **kw)
+        self.desc = hp.PagedDesc(self.pool, self.table, self.seq_ptr, self.after, **kw)
+        self.ws_a = hp.workspace_for(self.d_app, dev)
+        self.ws = hp.workspace_for(self.desc, dev)
+        self.T = w.total_tokens
+        self.out = torch.empty(self.T * w.row_bytes, dtype=torch.uint8, device=dev)
+        self.st_a = torch.full((1,), -12345, dtype=torch.int32, device=dev)
+        self.status = torch.full((1,), -12345, dtype=torch.int32, device=dev)
+
+    def append(self, stream):
+        rc = self.hp.hp_scatter_append(self.d_app, self.new, self.new_ptr, self.w.total_new,
+                                       self.ws_a, self.st_a, stream=stream)
+        assert rc == 0, self.hp.status_name(rc)
+
+    def copy(self, stream):
+        rc = self.hp.hp_gather_planned(self.desc, self.out, self.ws, self.status, stream=stream)
+        assert rc == 0, self.hp.status_name(rc)
+
+    def run(self, stream):
+        self.append(stream)
+        rc = self.hp.hp_plan(self.desc, self.T, self.ws, self.status, stream=stream)
+        assert rc == 0, self.hp.status_name(rc)
+        self.copy(stream)
+
+    def check_status(self):
+        for t in (self.st_a, self.status):
+            st = int(t.item())
+            assert st == 0, self.hp.status_name(st)
+
+
 def time_steps(step, steps, warmup, stream, dist=None):
-    """Warm-up, then `steps` timed steps (plan + copy, nothing between them) bracketed
-    by barrier + synchronize.  Returns (per-step ms list, wall seconds)."""
+    """Warm-up, then `steps` timed steps (all of a step's calls, nothing between them)
+    bracketed by barrier + synchronize.  Returns (per-step ms list, wall seconds)."""
     import torch
     for _ in range(warmup):
-        step.plan(stream)
-        step.copy(stream)
+        step.run(stream)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
@@ -222,8 +318,7 @@ def time_steps(step, steps, warmup, stream, dist=None):
     t0 = time.perf_counter()
     for e0, e1 in ev:
         e0.record(stream)
-        step.plan(stream)
-        step.copy(stream)
+        step.run(stream)
         e1.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -249,64 +344,93 @@ def time_copy_kernel(step, launches, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def _pinned_index(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    v = a.view(np.int32) if a.dtype == np.uint32 else a.astype(np.uint64).view(np.int64)
+    return torch.from_numpy(v.copy()).pin_memory()
+
+
 def e2e_host_buffers(w, dev, inputs):
-    """The end-to-end measurement's pinned host buffers: the pool (filled from the seeded
-    device pool) and two output buffers, shared by every e2e_gather call."""
+    """Pinned host buffers of an end-to-end measurement, shared by its runs: the pool
+    (filled from the seeded device pool, as it is before any append), the index buffers,
+    the new rows of a decode step, and two output buffers."""
     import torch
     pool_dev = inputs.device_pool(w, dev)
     h_pool = torch.empty(pool_dev.shape, dtype=torch.uint8, pin_memory=True)
     h_pool.copy_(pool_dev)
     del pool_dev
     n = w.total_tokens * w.row_bytes
-    return dict(pool=h_pool, outs=[torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    host = dict(pool=h_pool, outs=[torch.empty(n, dtype=torch.uint8, pin_memory=True)
                                    for _ in range(2)])
+    if w.new_ptr is not None:
+        host["idx"] = [_pinned_index(a) for a in (w.table, w.seq_ptr, w.lens_before, w.lens,
+                                                  w.new_ptr)]
+        host["new"] = torch.from_numpy(inputs.host_new_rows(w).reshape(-1).copy()).pin_memory()
+    else:
+        host["idx"] = [_pinned_index(a) for a in (w.table, w.seq_ptr, w.lens)]
+    return host
 
 
-def e2e_gather(w, dev, hp, inputs, steps, upload_pool=True, host=None):
-    """The same step through host buffers: every step uploads the pool and index buffers
-    from pinned host memory, gathers through the C ABI and downloads the gathered tensor
-    to pinned host memory.  Steps are pipelined over two device buffer sets and three
-    streams (upload, gather, download), so step k+1's upload overlaps step k's download;
-    a buffer set is reused only after the gather that read it and the download that read
-    its output have finished.  upload_pool=False keeps the pool resident on the device
-    (uploaded once, before the timed steps) and uploads only the index buffers."""
+def e2e_steps(w, dev, hp, steps, host, upload_pool=True):
+    """The step through host buffers: every step uploads its inputs from pinned host
+    memory (the pool unless upload_pool is False, the index buffers, a decode step's new
+    rows), runs the step's C-ABI calls (a decode step: hp_scatter_append, hp_plan,
+    hp_gather_planned; a gather: hp_gather) and downloads the gathered tensor to pinned
+    host memory.  Steps are pipelined over two device buffer sets and three streams
+    (upload, compute, download), so step k+1's upload overlaps step k's download; a buffer
+    set is reused only after the step that read it and the download of its output are
+    done.  Returns (ms per step, h2d bytes, d2h bytes)."""
     import torch
-    if host is None:
-        host = e2e_host_buffers(w, dev, inputs)
-    h_pool = host["pool"]
-    host_idx = [torch.from_numpy(np.ascontiguousarray(a).view(np.int32).copy()).pin_memory()
-                for a in (w.table, w.seq_ptr, w.lens)]
+    h_pool, host_idx, h_new = host["pool"], host["idx"], host.get("new")
+    decode = h_new is not None
     T = w.total_tokens
+    it = 0 if w.index_dtype == np.uint32 else 1
+    kw = dict(num_pages=w.num_pages, page_size=w.page_size, num_heads=w.num_heads,
+              head_dim=w.head_dim, dtype=w.dtype, index_type=it)
     sets = []
     for i in range(2):
         d_pool = torch.empty(h_pool.shape, dtype=torch.uint8, device=dev)
         d_idx = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_idx]
-        desc = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[2], num_pages=w.num_pages,
-                            page_size=w.page_size, num_heads=w.num_heads,
-                            head_dim=w.head_dim, dtype=w.dtype, index_type=0)
-        sets.append(dict(pool=d_pool, idx=d_idx, desc=desc, ws=hp.workspace_for(desc, dev),
-                         status=torch.zeros(1, dtype=torch.int32, device=dev),
-                         out=torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev),
-                         h_out=host["outs"][i],
-                         gathered=None, downloaded=None))
+        b = dict(pool=d_pool, idx=d_idx, status=torch.zeros(1, dtype=torch.int32, device=dev),
+                 st_a=torch.zeros(1, dtype=torch.int32, device=dev),
+                 out=torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev),
+                 h_out=host["outs"][i], gathered=None, downloaded=None)
+        if decode:
+            b["new"] = torch.empty(h_new.shape, dtype=h_new.dtype, device=dev)
+            b["d_app"] = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[2], **kw)
+            b["desc"] = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[3], **kw)
+            b["ws_a"] = hp.workspace_for(b["d_app"], dev)
+        else:
+            b["desc"] = hp.PagedDesc(d_pool, d_idx[0], d_idx[1], d_idx[2], **kw)
+        b["ws"] = hp.workspace_for(b["desc"], dev)
+        sets.append(b)
     up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
     def one(k, first=False):
         b = sets[k % 2]
         with torch.cuda.stream(up):
             if b["gathered"] is not None:
-                up.wait_event(b["gathered"])  # the last gather through this set is done
+                up.wait_event(b["gathered"])  # the last step through this set is done
             if upload_pool or first:
                 b["pool"].copy_(h_pool, non_blocking=True)
             for d, h in zip(b["idx"], host_idx):
                 d.copy_(h, non_blocking=True)
+            if decode:
+                b["new"].copy_(h_new, non_blocking=True)
             uploaded = torch.cuda.Event()
             uploaded.record(up)
         comp.wait_event(uploaded)
         if b["downloaded"] is not None:
             comp.wait_event(b["downloaded"])  # its output buffer has been read back
-        rc = hp.hp_gather(b["desc"], b["out"], T, b["ws"], b["status"], stream=comp)
-        assert rc == 0
+        if decode:
+            assert hp.hp_scatter_append(b["d_app"], b["new"], b["idx"][4], w.total_new,
+                                        b["ws_a"], b["st_a"], stream=comp) == 0
+            assert hp.hp_plan(b["desc"], T, b["ws"], b["status"], stream=comp) == 0
+            assert hp.hp_gather_planned(b["desc"], b["out"], b["ws"], b["status"],
+                                        stream=comp) == 0
+        else:
+            assert hp.hp_gather(b["desc"], b["out"], T, b["ws"], b["status"], stream=comp) == 0
         b["gathered"] = torch.cuda.Event()
         b["gathered"].record(comp)
         down.wait_event(b["gathered"])
@@ -326,131 +450,127 @@ def e2e_gather(w, dev, hp, inputs, steps, upload_pool=True, host=None):
     main.wait_stream(down)
     e1.record(main)
     torch.cuda.synchronize()
-    assert all(int(b["status"].item()) == 0 for b in sets)
+    assert all(int(b["status"].item()) == 0 and int(b["st_a"].item()) == 0 for b in sets)
     ms = e0.elapsed_time(e1) / steps
     h2d = (h_pool.numel() if upload_pool else 0) + sum(h.numel() * h.element_size()
                                                        for h in host_idx)
+    if decode:
+        h2d += h_new.numel()
     return ms, h2d, T * w.row_bytes
 
 
-def e2e_gather_in_place(w, dev, hp, inputs, steps, host):
-    """The same steps with the pool left in pinned host memory and the output written
-    straight into pinned host memory: every step uploads only its index buffers, and the
-    gather reads the live pages over the host link and writes the rows back over it (the
-    library routes host-resident memory to its register copy engine).  Two index and
-    output buffer sets alternate, as in e2e_gather."""
+def e2e_measurement(w, dev, hp, inputs, step_bytes, check_out):
+    """Three runs of 8 pipelined steps through pinned host buffers (the host link shows
+    occasional slow stretches, a whole run at about half speed): the median run, every
+    run listed, and the same with the pool resident on the device.  The downloaded rows
+    are compared with the device-resident step's output (check_out)."""
     import torch
-    h_pool = host["pool"]
-    host_idx = [torch.from_numpy(np.ascontiguousarray(a).view(np.int32).copy()).pin_memory()
-                for a in (w.table, w.seq_ptr, w.lens)]
-    T = w.total_tokens
-    stream = torch.cuda.current_stream()
-    sets = []
-    for i in range(2):
-        d_idx = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_idx]
-        desc = hp.PagedDesc(h_pool, d_idx[0], d_idx[1], d_idx[2], num_pages=w.num_pages,
-                            page_size=w.page_size, num_heads=w.num_heads,
-                            head_dim=w.head_dim, dtype=w.dtype, index_type=0,
-                            flags=hp.HOST_MEMORY)
-        sets.append(dict(idx=d_idx, desc=desc, ws=hp.workspace_for(desc, dev),
-                         status=torch.zeros(1, dtype=torch.int32, device=dev),
-                         h_out=host["outs"][i]))
-
-    def one(k):
-        b = sets[k % 2]
-        for d, h in zip(b["idx"], host_idx):
-            d.copy_(h, non_blocking=True)
-        assert hp.hp_gather(b["desc"], b["h_out"], T, b["ws"], b["status"], stream=stream) == 0
-
-    for k in range(2):
-        one(k)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(steps):
-        one(k)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    assert all(int(b["status"].item()) == 0 for b in sets)
-    ms = e0.elapsed_time(e1) / steps
-    live = int((-(-w.lens.astype(np.int64) // w.page_size)).sum())  # spans read
-    h2d = T * w.row_bytes + sum(h.numel() * h.element_size() for h in host_idx)
-    return ms, h2d, T * w.row_bytes, live
+    host = e2e_host_buffers(w, dev, inputs)
+    runs = [e2e_steps(w, dev, hp, 8, host) for _ in range(3)]
+    ms, h2d, d2h = sorted(runs)[1]
+    n = min(1 << 20, check_out.numel())
+    for o in host["outs"]:
+        assert torch.equal(o[:n].to(dev), check_out[:n]), "end-to-end output differs"
+        assert torch.equal(o[-n:].to(dev), check_out[-n:]), "end-to-end output differs"
+    res = {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+           "runs_ms_per_step": [round(r[0], 3) for r in runs],
+           "note": "pinned host buffers; every step uploads the pool, the index buffers%s and "
+                   "downloads the gathered tensor; pipelined over two buffer sets; median of "
+                   "three runs of 8 steps" % (" and the new rows" if w.new_ptr is not None
+                                              else "")}
+    runs = [e2e_steps(w, dev, hp, 8, host, upload_pool=False) for _ in range(3)]
+    ms_r, h2d_r, d2h_r = sorted(runs)[1]
+    res["resident_pool"] = {
+        "value": round(step_bytes / (ms_r * 1e-3) / 1e9, 1), "unit": UNIT,
+        "h2d_bytes_per_step": h2d_r, "d2h_bytes_per_step": d2h_r,
+        "ms_per_step": round(ms_r, 3), "runs_ms_per_step": [round(r[0], 3) for r in runs],
+        "note": "the pool stays on the device (a resident cache); every step uploads its "
+                "index buffers%s and downloads the gathered tensor"
+                % (" and new rows" if w.new_ptr is not None else "")}
+    del host
+    return res
 
 
 # ----------------------------------------------------------------------------- oracle arm
-def _oracle_desc_for(w, host_pool, seqs_upto, tokens_cap, oracle_mod):
-    lens = w.lens.astype(np.int64)[:seqs_upto].copy()
-    if tokens_cap is not None:
-        c = np.cumsum(lens)
-        k = int(np.searchsorted(c, tokens_cap))
-        lens = lens[:k + 1].copy()
-        prev = int(c[k - 1]) if k > 0 else 0
-        lens[-1] = max(1, min(int(lens[-1]), tokens_cap - prev))
-    n = len(lens)
-    sp = w.seq_ptr[:n + 1].astype(w.index_dtype)
-    table = w.table[:int(sp[-1])]
-    d = oracle_mod.Desc(host_pool, table, sp, lens.astype(w.index_dtype), num_pages=w.num_pages,
-                        page_size=w.page_size, num_heads=w.num_heads, head_dim=w.head_dim,
-                        dtype=w.dtype, index_type=0 if w.index_dtype == np.uint32 else 1)
-    return d, lens
+def _prefix_lens(w, tokens_cap):
+    """Token counts of the first tokens_cap tokens of the batch (the whole batch when
+    None): whole sequences, the last one cut short."""
+    lens = w.lens.astype(np.int64).copy()
+    if tokens_cap is None or tokens_cap >= int(lens.sum()):
+        return lens
+    c = np.cumsum(lens)
+    k = int(np.searchsorted(c, tokens_cap))
+    lens = lens[:k + 1].copy()
+    prev = int(c[k - 1]) if k > 0 else 0
+    lens[-1] = max(1, min(int(lens[-1]), tokens_cap - prev))
+    return lens
 
 
-def time_oracle(w, host_pool, oracle_mod, budget_s, max_tokens=None):
-    """Oracle gather on a prefix of the batch sized to take about budget_s seconds."""
-    tokens = 256
-    while True:
-        d, lens = _oracle_desc_for(w, host_pool, w.num_seqs, tokens, oracle_mod)
-        t0 = time.perf_counter()
-        d.gather()
-        dt = time.perf_counter() - t0
-        T = int(lens.sum())
-        if dt >= budget_s * 0.5 or T >= w.total_tokens or (max_tokens and T >= max_tokens):
-            break
-        scale = max(2.0, min(16.0, budget_s / max(dt, 1e-4)))
-        tokens = int(min(w.total_tokens, tokens * scale))
-        if max_tokens:
-            tokens = min(tokens, max_tokens)
-    b, _ = gather_bytes(w, lens)
-    return b / dt / 1e9, dt, T, lens
+def _oracle_sub(w, host_pool, oracle_mod, a, b, lens, scales=None):
+    """An oracle descriptor over sequences a..b-1 (re-based slices), counts `lens`."""
+    sp = (w.seq_ptr[a:b + 1].astype(np.int64) - int(w.seq_ptr[a])).astype(w.index_dtype)
+    table = w.table[int(w.seq_ptr[a]):int(w.seq_ptr[b])]
+    return oracle_mod.Desc(host_pool, table, sp, np.asarray(lens).astype(w.index_dtype),
+                           num_pages=w.num_pages, page_size=w.page_size, num_heads=w.num_heads,
+                           head_dim=w.head_dim, dtype=w.dtype,
+                           index_type=0 if w.index_dtype == np.uint32 else 1, scales=scales,
+                           flags=0 if scales is None else oracle_mod.HAS_QUANT)
 
 
 class OracleThreads:
-    """The oracle gather, as it stands, on nthreads host threads over the first
-    `tokens_cap` tokens of the batch (all of it when None): the sequences are cut into
-    nthreads contiguous groups, each gathered by one call through its own sub-descriptor
-    (ctypes releases the GIL during the call)."""
+    """The oracle's gather (its dequantising gather when `scales` is given), as it stands,
+    on nthreads host threads over the first `tokens_cap` tokens of the batch (all of it
+    when None): the sequences are cut into nthreads contiguous groups, each gathered by
+    one call through its own sub-descriptor (ctypes releases the GIL during the call).
+    For a decode-step batch each step first runs the oracle's append of the new rows
+    (one call, on the calling thread)."""
 
-    def __init__(self, w, host_pool, oracle_mod, nthreads, tokens_cap=None):
+    def __init__(self, w, host_pool, oracle_mod, nthreads, tokens_cap=None, scales=None,
+                 append=False):
         from concurrent.futures import ThreadPoolExecutor
-        _, lens = _oracle_desc_for(w, host_pool, w.num_seqs, tokens_cap, oracle_mod)
-        lens = lens.astype(np.int64)
+        lens = _prefix_lens(w, tokens_cap)
         n = len(lens)
         cuts = np.linspace(0, n, min(nthreads, n) + 1).astype(int)
         self.descs, self.outs = [], []
+        E = w.num_heads * w.head_dim
         for a, b in zip(cuts[:-1], cuts[1:]):
             if b <= a:
                 continue
-            sp = (w.seq_ptr[a:b + 1].astype(np.int64) - int(w.seq_ptr[a])).astype(w.index_dtype)
-            table = w.table[int(w.seq_ptr[a]):int(w.seq_ptr[b])]
-            d = oracle_mod.Desc(host_pool, table, sp, lens[a:b].astype(w.index_dtype),
-                                num_pages=w.num_pages, page_size=w.page_size,
-                                num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype,
-                                index_type=0 if w.index_dtype == np.uint32 else 1)
+            d = _oracle_sub(w, host_pool, oracle_mod, a, b, lens[a:b], scales)
             self.descs.append(d)
-            self.outs.append(np.zeros((d.total_tokens(), w.row_bytes), dtype=np.uint8))
+            T = int(lens[a:b].sum())
+            self.outs.append(np.zeros((T, w.row_bytes), dtype=np.uint8) if scales is None
+                             else np.zeros((T, E), dtype=np.uint16))
+        self.dequant = scales is not None
         self.pool = ThreadPoolExecutor(max(1, len(self.descs)))
         self.tokens = int(lens.sum())
-        self.bytes, _ = gather_bytes(w, lens)
+        self.bytes = (dequant_bytes if self.dequant else gather_bytes)(w, lens)[0]
         self.threads = len(self.descs)
+        self.append = None
+        if append:
+            self.append = (_oracle_sub(w, host_pool, oracle_mod, 0, w.num_seqs, w.lens_before),
+                           inputs_new_rows(w), w.new_ptr)
+            self.bytes += append_bytes(w)
 
     def step(self):
-        faults = list(self.pool.map(lambda i: self.descs[i].gather(self.outs[i])[2],
-                                    range(len(self.descs))))
-        assert all(f == "OK" for f in faults), faults
+        if self.append is not None:
+            d, rows, new_ptr = self.append
+            assert d.scatter_append(rows, new_ptr) == "OK"
+        if self.dequant:
+            f = lambda i: self.descs[i].gather_dequant(self.outs[i])[2]
+        else:
+            f = lambda i: self.descs[i].gather(self.outs[i])[2]
+        faults = list(self.pool.map(f, range(len(self.descs))))
+        assert all(x == "OK" for x in faults), faults
 
     def close(self):
         self.pool.shutdown()
+
+
+def inputs_new_rows(w):
+    from paged_kv_cache_hp_gb300 import inputs
+    return inputs.host_new_rows(w)
 
 
 def host_threads():
@@ -458,15 +578,76 @@ def host_threads():
                else (os.cpu_count() or 1))
 
 
-def time_oracle_threads(w, host_pool, oracle_mod, nthreads):
-    """The threaded oracle gather of the whole batch: (GB/s, seconds, threads used)."""
-    r = OracleThreads(w, host_pool, oracle_mod, nthreads)
-    r.step()  # page in
+def time_oracle_run(w, host_pool, oracle_mod, nthreads, budget_s, scales=None, append=False):
+    """The oracle on nthreads threads over as much of the batch (a prefix of it) as takes
+    about budget_s seconds a step: a probe of 65,536 tokens sets the size.  Returns
+    (GB/s, seconds, tokens, threads used)."""
+    probe = OracleThreads(w, host_pool, oracle_mod, nthreads, tokens_cap=1 << 16, scales=scales)
+    probe.step()
     t0 = time.perf_counter()
-    r.step()
+    probe.step()
+    rate = probe.tokens / max(time.perf_counter() - t0, 1e-6)
+    probe.close()
+    cap = int(rate * budget_s)
+    run = OracleThreads(w, host_pool, oracle_mod, nthreads,
+                        tokens_cap=None if cap >= w.total_tokens else cap, scales=scales,
+                        append=append)
+    run.step()  # page in
+    t0 = time.perf_counter()
+    run.step()
     dt = time.perf_counter() - t0
-    r.close()
-    return r.bytes / dt / 1e9, dt, r.threads
+    run.close()
+    return run.bytes / dt / 1e9, dt, run.tokens, run.threads
+
+
+def cpu_baseline_entry(w, host_pool, oracle_mod, scales=None, append=False, budget_s=8.0,
+                       single_budget_s=6.0):
+    """The oracle as it stands timed on this host: on every host thread (the whole batch
+    when it takes under budget_s, else a prefix), and on one thread (a prefix of about
+    single_budget_s)."""
+    what = "dequantising gather" if scales is not None else "gather"
+    if append:
+        what = "append of the %d new rows + %s" % (w.total_new, what)
+    gbps, dt, tok, used = time_oracle_run(w, host_pool, oracle_mod, host_threads(), budget_s,
+                                          scales, append)
+    g1, dt1, tok1, _ = time_oracle_run(w, host_pool, oracle_mod, 1, single_budget_s, scales,
+                                       append)
+    span = "the whole batch (%d tokens)" % tok if tok >= w.total_tokens else \
+        "the first %d of %d tokens" % (tok, w.total_tokens)
+    span1 = "the whole batch" if tok1 >= w.total_tokens else \
+        "the first %d of %d tokens" % (tok1, w.total_tokens)
+    return {"value": round(gbps, 3), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": "oracle %s of %s on %d threads, one contiguous group of sequences each, "
+                      "%.2f s" % (what, span, used, dt),
+            "single_thread": {"value": round(g1, 3), "cores": 1,
+                              "sample": "oracle %s (one thread) of %s, %.2f s"
+                                        % (what, span1, dt1)}}
+
+
+def host_pool_for(w, dev=None):
+    """The pool's bytes on the host: the seeded device pool copied back when a GPU is
+    present (the bytes every GPU measurement reads); on a host without one, small pools
+    from numpy and large ones zero-filled (a byte copy's time does not depend on the
+    bytes)."""
+    from paged_kv_cache_hp_gb300 import inputs
+    if w.pool_bytes <= (64 << 20):
+        return inputs.host_pool(w).reshape(-1), "seeded"
+    import torch
+    if torch.cuda.is_available():
+        return inputs.device_pool(w, dev or "cuda").cpu().numpy().reshape(-1), "seeded"
+    return np.zeros(w.pool_bytes, dtype=np.uint8), "zero-filled (no GPU on this host)"
+
+
+def host_scales_for(w, dev=None):
+    from paged_kv_cache_hp_gb300 import inputs
+    import torch
+    if w.scales_seed is None:
+        return None
+    n = w.num_pages * w.page_size
+    if n * 4 <= (64 << 20) or not torch.cuda.is_available():
+        return inputs.host_scales(w) if n * 4 <= (64 << 20) else \
+            np.full(n, 0.01, dtype=np.float32)
+    return inputs.device_scales(w, dev or "cuda").cpu().numpy()
 
 
 # ----------------------------------------------------------------------------- ops
@@ -674,20 +855,26 @@ def attention_measurement(dev, hp, inputs, w, d_k, peak, entry, med_ms, Hq=32, r
     return res
 
 
-def dequant_measurements(dev, hp, inputs, entry, med_ms):
+def dequant_measurements(dev, hp, inputs, entry, med_ms, oracle_mod=None):
     """The dequantising gathers on the quantized_pool batch (int8 codes -> bf16): per-slot
-    scales, then the other schemes of [HF] Per-scheme composition with zero points."""
+    scales (the benchmark configuration, with its traffic record and, given the oracle,
+    its CPU baseline), then the other schemes of [HF] Per-scheme composition with zero
+    points."""
     import torch
     out = {}
     stream = torch.cuda.current_stream()
     w = inputs.config("quantized_pool")
     st = GatherStep(w, dev, hp, inputs)
     T = w.total_tokens
-    spans = int((-(-w.lens.astype(np.int64) // w.page_size)).sum())
-    b = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
+    b, spans = dequant_bytes(w)
     st.plan(stream)
     ms = med_ms(lambda: st.copy(stream), n=10)
-    out["quantized_pool_dequant_gather"] = entry(b, ms)
+    e = entry(b, ms, workload=w.name, tokens=T, units=spans, kernel="copy_kernel<dequant>")
+    traffic = recorded_traffic("gather_" + w.name, spans)
+    e["traffic"] = None if traffic is None else int(traffic)
+    if traffic is not None:
+        e["traffic_source"] = traffic_source("gather_" + w.name)
+    out["quantized_pool_dequant_gather"] = e
     st.check_status()
     g = torch.Generator(device=dev)
     g.manual_seed(w.scales_seed + 1)
@@ -706,7 +893,15 @@ def dequant_measurements(dev, hp, inputs, entry, med_ms):
         nbytes = b + T if tag == 3 else b - 4 * T
         out["quantized_pool_dequant_" + name + "_zp"] = entry(nbytes, ms)
         st.check_status()
-    del st
+    if oracle_mod is not None:
+        host_pool = st.pool.cpu().numpy().reshape(-1)
+        scales = st.scales.cpu().numpy()
+        del st
+        release_device_memory()
+        e["cpu_baseline"] = cpu_baseline_entry(w, host_pool, oracle_mod, scales=scales)
+        del host_pool
+    else:
+        del st
     release_device_memory()
     return out
 
@@ -762,7 +957,55 @@ def decode_step_layers(dev, hp, inputs, entry, med_ms, layers=4, Hq=32):
     return res
 
 
-def ops_measurements(dev, hp, inputs, peak, reps=20):
+def config_entry(dev, hp, inputs, w, peak, med_ms, oracle_mod, cold=None, e2e=False):
+    """One benchmark configuration's gather (dequantising for an int8 pool): the copy
+    kernel's median time after one plan and the whole step's (plan, table check, copy),
+    the fraction of the peak, the DRAM traffic record, and the oracle's baseline.  With
+    prefix sharing, also the bytes a gather must move at least (each shared page once)
+    and their fraction: the logical bytes count a shared page once per reader, and those
+    reads after the first come from L2."""
+    import torch
+    stream = torch.cuda.current_stream()
+    st = GatherStep(w, dev, hp, inputs)
+    b, spans = (dequant_bytes if st.dequant else gather_bytes)(w)
+    st.run(stream)
+    ms = med_ms(lambda: st.copy(stream), n=10)
+    ms_step = med_ms(lambda: st.run(stream), n=10)
+    st.check_status()
+    e = rate_entry(b, ms, peak, workload=w.name, tokens=w.total_tokens, units=spans,
+                   kernel="copy_kernel<dequant>" if st.dequant else "bulk_kernel<gather>")
+    e["step"] = rate_entry(b + validate_bytes(w), ms_step, peak,
+                           note="hp_plan + copy (plan, table check, copy kernels)")
+    traffic = recorded_traffic("gather_" + w.name, spans)
+    e["traffic"] = None if traffic is None else int(traffic)
+    if traffic is not None:
+        e["traffic_source"] = traffic_source("gather_" + w.name)
+    if w.name.startswith("prefix_sharing"):
+        ub = unique_gather_bytes(w)
+        e["note"] = "logical bytes: each shared prefix page counted once per sequence"
+        e["unique_bytes"] = ub
+        e["gbps_unique"] = round(ub / (ms * 1e-3) / 1e9, 1)
+        e["frac_unique"] = round(ub / (ms * 1e-3) / 1e9 / peak, 4)
+        if traffic is not None:
+            e["traffic_over_unique"] = round(traffic / ub, 4)
+        if cold is not None:
+            ms_c = med_ms(lambda: st.copy(stream), n=10, between=cold)
+            e["l2_cold"] = rate_entry(b, ms_c, peak, note="L2 scrubbed (256 MB write) before "
+                                      "each call; logical bytes")
+            e["l2_cold"]["frac_unique"] = round(ub / (ms_c * 1e-3) / 1e9 / peak, 4)
+    if e2e and not st.dequant:
+        e["e2e"] = e2e_measurement(w, dev, hp, inputs, b + validate_bytes(w), st.out)
+    if oracle_mod is not None:
+        host_pool = st.pool.cpu().numpy().reshape(-1)
+        scales = st.scales.cpu().numpy() if st.dequant else None
+        del st
+        release_device_memory()
+        e["cpu_baseline"] = cpu_baseline_entry(w, host_pool, oracle_mod, scales=scales)
+        del host_pool
+    return e
+
+
+def ops_measurements(dev, hp, inputs, peak, oracle_mod=None, reps=20):
     """The other rows of the path at their own configurations (bytes as in
     gather_bytes; medians over reps, inputs larger than L2 except where noted)."""
     import torch
@@ -818,7 +1061,7 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     def entry(bytes_, ms, **kw):
         return rate_entry(bytes_, ms, peak, **kw)
 
-    # tiny prefix-sharing gather: latency
+    # tiny prefix-sharing gather (28 tokens): latency
     w = inputs.tiny_prefix_gather()
     st = GatherStep(w, dev, hp, inputs)
     # stream=None: the binding uses torch's current stream, the capture stream inside a graph
@@ -826,6 +1069,16 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     out["tiny_prefix_gather"]["us_per_step_l2_cold"] = round(
         1e3 * med_ms(lambda: (st.plan(stream), st.copy(stream)), between=cold), 2)
     st.check_status()
+    if oracle_mod is not None:
+        d = _oracle_sub(w, inputs.host_pool(w).reshape(-1), oracle_mod, 0, w.num_seqs, w.lens)
+        d.gather()
+        t0 = time.perf_counter()
+        for _ in range(2000):
+            d.gather()
+        out["tiny_prefix_gather"]["cpu_baseline"] = {
+            "us_per_call": round((time.perf_counter() - t0) / 2000 * 1e6, 2), "cores": 1,
+            "kind": "oracle", "sample": "oracle gather of the whole batch, one thread, mean "
+                                        "of 2000 calls (each allocating its output)"}
     # the same gather as one hp_gather call: a small validated batch takes the one-launch
     # path (plan, table check and copy in one kernel)
     out["tiny_prefix_gather_one_call"] = step_us(
@@ -833,21 +1086,18 @@ def ops_measurements(dev, hp, inputs, peak, reps=20):
     st.check_status()
     del st
 
-    # prefix sharing at scale
+    # decode-sized gather (64 sequences, 8 KiB rows) and prefix sharing (128 sequences on
+    # one 2048-token prompt): each configuration with its traffic record and CPU baseline
+    w = inputs.config("decode_gather")
+    out["decode_gather"] = config_entry(dev, hp, inputs, w, peak, med_ms, oracle_mod,
+                                        e2e=True)
+    release_device_memory()
     w = inputs.config("prefix_sharing")
-    st = GatherStep(w, dev, hp, inputs)
-    b, spans = gather_bytes(w)
-    st.plan(stream)
-    ms = med_ms(lambda: st.copy(stream))
-    out["prefix_sharing_gather"] = entry(b, ms, note="logical bytes; the 128 shared pages are "
-                                         "read from L2 after their first use")
-    ms = med_ms(lambda: st.copy(stream), between=cold)
-    out["prefix_sharing_gather_l2_cold"] = entry(
-        b, ms, note="logical bytes, L2 scrubbed (256 MB write) before each call")
-    st.check_status()
-    del st
+    out["prefix_sharing_gather"] = config_entry(dev, hp, inputs, w, peak, med_ms, oracle_mod,
+                                                cold=cold)
+    release_device_memory()
 
-    out.update(dequant_measurements(dev, hp, inputs, entry, med_ms))
+    out.update(dequant_measurements(dev, hp, inputs, entry, med_ms, oracle_mod))
 
     # decode step: append one row per sequence, then gather the grown batch
     w = inputs.config("decode_append")
@@ -959,10 +1209,11 @@ def main():
     ap.add_argument("--no-ops", action="store_true", help="skip the per-operation measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
-    ap.add_argument("--workload", default="decode_gather",
-                    choices=["decode_gather", "decode_append", "prefix_sharing", "quantized_pool",
-                             "quantized_pool_mid"],
-                    help="batch the timed steps gather (default: the decode-sized gather)")
+    ap.add_argument("--workload", default="decode_append",
+                    choices=["decode_append", "decode_append_mid", "decode_gather",
+                             "prefix_sharing", "quantized_pool", "quantized_pool_mid"],
+                    help="batch of the timed steps (default: the decode step, append then "
+                         "gather, at its stated size; *_mid: the profiler's smaller case)")
     ap.add_argument("--attention", choices=["full", "mid", "short"],
                     help="time only hp_attention_decode on the decode-append batch at this "
                          "scale (warm-up calls, then --steps timed calls) and print its line")
@@ -1042,65 +1293,35 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     from paged_kv_cache_hp_gb300 import inputs
-    if args.workload == "quantized_pool_mid":
-        w = inputs.config("quantized_pool", "mid")
-    else:
-        w = inputs.config(args.workload)
+    w = workload(inputs, args.workload)
     T = w.total_tokens
-    step_bytes_copy, spans = gather_bytes(w)
-    if w.scales_seed is not None:  # int8 in, 4-byte scale per row, bf16 out
-        step_bytes_copy = T * (w.num_heads * w.head_dim * 3 + 4) + spans * 8
-    step_bytes = step_bytes_copy + validate_bytes(w)
+    decode = w.new_ptr is not None
+    dequant = w.scales_seed is not None
+    copy_bytes, spans = (dequant_bytes if dequant else gather_bytes)(w)
+    step_bytes = copy_bytes + validate_bytes(w)
+    if decode:  # the append, and its own plan's reads
+        step_bytes += append_bytes(w) + validate_bytes(w)
     config = {"workload": w.name, "num_pages": w.num_pages, "page_size": w.page_size,
               "num_heads": w.num_heads, "head_dim": w.head_dim, "pool_dtype": w.dtype,
               "num_seqs": w.num_seqs, "total_tokens": T,
               "index": "u32" if w.index_dtype == np.uint32 else "u64",
               "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (%.2f GB per step)"
               % (step_bytes / 1e9), "parallelism": "replicas x%d" % args.gpus}
+    if decode:
+        config.update(new_rows_per_step=w.total_new, step=(
+            "hp_scatter_append (validated: plan, table check, one warp per sequence) of one "
+            "new row per sequence at its count, then hp_plan + hp_gather_planned of the "
+            "grown batch; the counts are not advanced between steps (identical work)"),
+            num_pages_note="300,000 pages: the stated 60,000 cannot hold 256 sequences of "
+                           "U[1024, 32768] tokens (about 270,000 pages needed)"
+            if w.name == "decode_append" else None)
+    else:
+        config["step"] = ("hp_plan + hp_gather_dequant_planned" if dequant
+                          else "hp_plan + hp_gather_planned")
 
     if args.impl == "reference":
-        if rank != 0:
-            return
-        import oracle
-        oracle.build()
-        host_pool = inputs.host_pool(w) if w.pool_bytes <= (64 << 20) else None
-        if host_pool is None:
-            import torch
-            host_pool = inputs.device_pool(w, "cpu", force_device_rng=True).numpy() \
-                if not torch.cuda.is_available() else inputs.device_pool(w, "cuda").cpu().numpy()
-        # each step: the threaded oracle over a prefix of the batch sized so that the
-        # whole --steps/--warmup run takes about two minutes of host time
-        per_step = max(0.002, 120.0 / (args.steps + args.warmup))
-        nthr = host_threads()
-        full = OracleThreads(w, host_pool, oracle, nthr)
-        full.step()
-        t0 = time.perf_counter()
-        full.step()
-        dt_full = time.perf_counter() - t0
-        full.close()
-        cap = None if dt_full <= per_step else max(256, int(w.total_tokens * per_step / dt_full))
-        run = OracleThreads(w, host_pool, oracle, nthr, cap)
-        for _ in range(args.warmup):
-            run.step()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            run.step()
-        el = time.perf_counter() - t0
-        run.close()
-        value = run.bytes * args.steps / el / 1e9
-        sample = ("oracle gather of the first %d of %d tokens per step on %d host threads "
-                  "(one contiguous group of sequences each)" % (run.tokens, w.total_tokens,
-                                                                 run.threads))
-        print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 3),
-                          "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-                          "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
-                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                          "dtype": w.dtype, "data": "synthetic", "config": config,
-                          "cpu_baseline": {"value": round(value, 3), "unit": UNIT,
-                                           "cores": run.threads, "kind": "oracle",
-                                           "sample": sample},
-                          "e2e": {"value": round(value, 3), "unit": UNIT,
-                                  "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        if rank == 0:
+            reference_arm(args, w, config, decode)
         return
 
     import torch
@@ -1116,7 +1337,7 @@ def main():
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
-    step = GatherStep(w, dev, hp, inputs)
+    step = DecodeAppendStep(w, dev, hp, inputs) if decode else GatherStep(w, dev, hp, inputs)
     with ClockSampler(local) as clk:
         step_ms, wall = time_steps(step, args.steps, args.warmup, stream, dist)
         copy_ms = time_copy_kernel(step, min(args.steps, 500), stream)
@@ -1124,10 +1345,87 @@ def main():
     value = whole_job_gbps(step_bytes, args.steps, world, total_ms)
     peak, peak_kind = peak_hbm()
     copy_mean = statistics.mean(copy_ms)
-    achieved = step_bytes_copy / (copy_mean * 1e-3) / 1e9
+    achieved = copy_bytes / (copy_mean * 1e-3) / 1e9
+    d2d_gbps = d2d_copy_gbps(T * w.row_bytes, dev, stream)
 
-    # a same-bytes device-to-device copy as the practical ceiling
-    a = torch.empty(T * w.row_bytes, dtype=torch.uint8, device=dev)
+    traffic = recorded_traffic("gather_" + w.name, spans)
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; pool ~N(0,1) drawn on the device)", "config": config,
+        "gpu_launches": step.launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic is None else int(traffic),
+                     "kernel": ("copy_kernel<dequant> (hp_gather_dequant_planned)"
+                                if dequant else step.kernel),
+                     "kernel_timing": "CUDA events around each of %d copy-only launches "
+                                      "after the timed steps" % len(copy_ms),
+                     "peak_kind": peak_kind + " (hbm_gbs, copy)",
+                     "algorithmic_bytes_per_launch": copy_bytes,
+                     "units_per_launch": spans,
+                     "launch_ms_mean": round(copy_mean, 4),
+                     "frac_of_nominal_8000": round(achieved / 8000.0, 4),
+                     "d2d_copy_same_bytes_gbps": round(d2d_gbps, 1)},
+        "clocks": clk.summary(),
+    }
+    if traffic is not None:
+        result["roofline"]["traffic_source"] = traffic_source("gather_" + w.name)
+    if rank == 0 and world == 1 and not args.no_e2e and not dequant:
+        result["e2e"] = e2e_measurement(w, dev, hp, inputs, step_bytes, step.out)
+        release_device_memory()
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        # (for a decode step the pool already holds the new rows; the oracle's append
+        # writes the same rows over them, the same work as on the pool before the step)
+        host_pool = step.pool.cpu().numpy().reshape(-1)
+        scales = step.scales.cpu().numpy() if dequant else None
+        result["cpu_baseline"] = cpu_baseline_entry(w, host_pool, oracle, scales=scales,
+                                                    append=decode)
+        del host_pool
+    if rank == 0 and world == 1 and not args.no_ops:
+        del step
+        release_device_memory()
+        result["ops"] = ops_measurements(dev, hp, inputs, peak,
+                                         None if args.no_cpu else load_oracle())
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def load_oracle():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def workload(inputs, name):
+    if name.endswith("_mid"):
+        return inputs.config(name[:-4], "mid")
+    return inputs.config(name)
+
+
+def traffic_source(key):
+    src = TRAFFIC_FROM.get(key, key)
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f)[src]
+        how = "captured on this workload" if src == key else \
+            "captured on %s, scaled by page spans" % src[len("gather_"):]
+        return "%s, %s" % (rec.get("capture"), how)
+    except Exception:
+        return None
+
+
+def d2d_copy_gbps(nbytes, dev, stream):
+    """A same-bytes device-to-device copy (torch copy_), the practical ceiling."""
+    import torch
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     bb = torch.empty_like(a)
     for _ in range(3):
         bb.copy_(a)
@@ -1138,94 +1436,52 @@ def main():
         bb.copy_(a)
     e1.record(stream)
     torch.cuda.synchronize()
-    d2d_gbps = 2 * a.numel() / (e0.elapsed_time(e1) / 20 * 1e-3) / 1e9
     del a, bb
+    return 2 * nbytes / (e0.elapsed_time(e1) / 20 * 1e-3) / 1e9
 
-    traffic = recorded_traffic("gather_" + w.name, spans)
-    result = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic (seeded; pool ~N(0,1) drawn on the device)", "config": config,
-        "gpu_launches": 3 * args.steps,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None if traffic is None else int(traffic),
-                     "kernel": ("copy_kernel<dequant> (hp_gather_dequant_planned)"
-                                if step.dequant else "bulk_kernel<gather> (hp_gather_planned)"),
-                     "kernel_timing": "CUDA events around each of %d copy-only launches "
-                                      "after the timed steps" % len(copy_ms),
-                     "peak_kind": peak_kind + " (hbm_gbs, copy)",
-                     "algorithmic_bytes_per_launch": step_bytes_copy,
-                     "launch_ms_mean": round(copy_mean, 4),
-                     "frac_of_nominal_8000": round(achieved / 8000.0, 4),
-                     "d2d_copy_same_bytes_gbps": round(d2d_gbps, 1)},
-        "clocks": clk.summary(),
-    }
-    if rank == 0 and world == 1 and not args.no_e2e and args.workload == "decode_gather":
-        # the host link shows occasional slow stretches (a whole run of steps at about
-        # half speed, seen with either kind of pinned memory): three runs of 8 steps, the
-        # median run reported and every run listed
-        host = e2e_host_buffers(w, dev, inputs)
-        runs = [e2e_gather(w, dev, hp, inputs, steps=8, host=host) for _ in range(3)]
-        ms, h2d, d2h = sorted(runs)[1]
-        result["e2e"] = {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
-                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "ms_per_step": round(ms, 3),
-                         "runs_ms_per_step": [round(r[0], 3) for r in runs],
-                         "note": "pinned host buffers; uploads, gathers and downloads "
-                                 "pipelined over two buffer sets; median of three runs of "
-                                 "8 steps"}
-        runs = [e2e_gather(w, dev, hp, inputs, steps=8, upload_pool=False, host=host)
-                for _ in range(3)]
-        ms_r, h2d_r, d2h_r = sorted(runs)[1]
-        for o in host["outs"]:
-            o[:1 << 20].fill_(0xEE)  # so that the check below sees the in-place gather's rows
-        runs_z = [e2e_gather_in_place(w, dev, hp, inputs, steps=8, host=host)
-                  for _ in range(3)]
-        ms_z, h2d_z, d2h_z, _ = sorted(runs_z)[1]
-        # the output must be the gather's: compare one buffer with a device gather
-        check = host["outs"][0][:1 << 20].clone()
-        del host
-        result["e2e"]["resident_pool"] = {
-            "value": round(step_bytes / (ms_r * 1e-3) / 1e9, 1), "unit": UNIT,
-            "h2d_bytes_per_step": h2d_r, "d2h_bytes_per_step": d2h_r,
-            "ms_per_step": round(ms_r, 3),
-            "runs_ms_per_step": [round(r[0], 3) for r in runs],
-            "note": "the pool stays on the device (a resident cache); every step uploads "
-                    "its index buffers and downloads the gathered tensor"}
-        assert torch.equal(check.to(dev), step.out[:1 << 20]), "in-place gather differs"
-        result["e2e"]["pool_in_host_memory"] = {
-            "value": round(step_bytes / (ms_z * 1e-3) / 1e9, 1), "unit": UNIT,
-            "h2d_bytes_per_step": h2d_z, "d2h_bytes_per_step": d2h_z,
-            "ms_per_step": round(ms_z, 3),
-            "runs_ms_per_step": [round(r[0], 3) for r in runs_z],
-            "note": "the pool stays in pinned host memory and the gather writes its rows "
-                    "into pinned host memory: each step uploads its index buffers; the "
-                    "kernel reads the live pages and writes the output over the host link"}
-    if rank == 0 and world == 1 and not args.no_cpu and w.scales_seed is None:
-        import oracle
-        oracle.build()
-        host_pool = step.pool.cpu().numpy()
-        gbps, dt, Ts, lens = time_oracle(w, host_pool, oracle, budget_s=12.0)
-        gbps_mt, dt_mt, used = time_oracle_threads(w, host_pool, oracle, host_threads())
-        result["cpu_baseline"] = {
-            "value": round(gbps_mt, 3), "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": "oracle gather of the whole batch (%d tokens) on %d threads, one "
-                      "contiguous group of sequences each, %.2f s" % (T, used, dt_mt),
-            "single_thread": {"value": round(gbps, 3), "cores": 1,
-                              "sample": "oracle gather (one thread) of the first %d of %d "
-                                        "tokens, %.1f s" % (Ts, T, dt)}}
-    if rank == 0 and world == 1 and not args.no_ops:
-        del step
-        release_device_memory()
-        result["ops"] = ops_measurements(dev, hp, inputs, peak)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(result))
+
+def reference_arm(args, w, config, decode):
+    """The CPU oracle as it stands, on every host thread, each step over a prefix of the
+    batch sized so that the whole --steps/--warmup run takes about two minutes (for a
+    decode step: the oracle's append of the new rows, then the gather of the prefix)."""
+    import oracle
+    oracle.build()
+    host_pool, fill = host_pool_for(w)
+    scales = host_scales_for(w)
+    per_step = max(0.002, 120.0 / (args.steps + args.warmup))
+    nthr = host_threads()
+    probe = OracleThreads(w, host_pool, oracle, nthr, tokens_cap=1 << 16, scales=scales)
+    probe.step()
+    t0 = time.perf_counter()
+    probe.step()
+    rate = probe.tokens / max(time.perf_counter() - t0, 1e-6)
+    probe.close()
+    cap = int(rate * per_step)
+    run = OracleThreads(w, host_pool, oracle, nthr, None if cap >= w.total_tokens else max(256, cap),
+                        scales=scales, append=decode)
+    for _ in range(args.warmup):
+        run.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run.step()
+    el = time.perf_counter() - t0
+    run.close()
+    value = run.bytes * args.steps / el / 1e9
+    what = ("append of the %d new rows, then gather" % w.total_new) if decode else \
+        ("dequantising gather" if scales is not None else "gather")
+    sample = ("oracle %s of the first %d of %d tokens per step on %d host threads (one "
+              "contiguous group of sequences each); pool %s" % (what, run.tokens, w.total_tokens,
+                                                               run.threads, fill))
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 3),
+                      "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                      "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                      "dtype": w.dtype, "data": "synthetic", "config": config,
+                      "cpu_baseline": {"value": round(value, 3), "unit": UNIT,
+                                       "cores": run.threads, "kind": "oracle",
+                                       "sample": sample},
+                      "e2e": {"value": round(value, 3), "unit": UNIT,
+                              "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
 if __name__ == "__main__":

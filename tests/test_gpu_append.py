@@ -305,3 +305,38 @@ def test_one_append_plan_serves_the_pools_of_several_layers(hp, oracle):
         o = b.oracle_desc(pool_host=host, lens=w.lens_before)
         assert o.scatter_append(rows, w.new_ptr) == "OK"
         assert np.array_equal(pl.cpu().numpy(), host)
+
+
+@pytest.mark.parametrize("fault", ["NEW_PTR_END", "NEW_PTR_ORDER"])
+def test_permissive_decode_step_reads_no_row_past_total_new(hp, oracle, fault):
+    """HP_PERMISSIVE with a new_ptr that ends past total_new (or runs backwards): the
+    one-kernel decode path skips that sequence, reports the rule, reads no row outside
+    the total_new rows given, and writes exactly what the oracle writes."""
+    import torch
+    rng = np.random.default_rng(11)
+    w = inputs.decode_gather(seed=71, num_pages=900, page_size=16, num_heads=8, head_dim=128,
+                             num_seqs=20, len_lo=2, len_hi=200, dtype="bf16")
+    full = w.lens.astype(np.int64)
+    before = full - 1
+    if fault == "NEW_PTR_END":  # one row each; the last sequence claims rows past the buffer
+        new_ptr = np.arange(w.num_seqs + 1, dtype=np.int64)
+        total_new = w.num_seqs
+        new_ptr[-1] = total_new + 3
+    else:  # sequence 7's pair is (7, 6): backwards; every other pair holds one row
+        new_ptr = np.concatenate([np.arange(8), np.arange(6, w.num_seqs - 1)]).astype(np.int64)
+        total_new = int(new_ptr[-1])
+    rows = rng.integers(0, 256, (total_new, w.row_bytes), dtype=np.uint8)
+    # the device buffer holds exactly total_new rows, followed by a page of other bytes
+    dev = torch.full(((total_new + 16) * w.row_bytes,), 0xEE, dtype=torch.uint8, device="cuda")
+    dev[:total_new * w.row_bytes] = torch.from_numpy(rows.reshape(-1)).to("cuda")
+    b = Batch(w, flags=1, lens=before.astype(np.uint32))
+    host = b.host_pool().copy()
+    rc = hp.hp_scatter_append(b.desc, dev, index_tensor(new_ptr.astype(np.uint32), "cuda"),
+                              total_new, b.ws, b.status)
+    torch.cuda.synchronize()
+    assert rc == 0
+    o = b.oracle_desc(pool_host=host, lens=before.astype(np.uint32))
+    assert o.scatter_append(rows, new_ptr.astype(np.uint32), total_new) == fault
+    assert hp.status_name(b.status_value()) == "HP_ERR_" + fault
+    got = b.pool.cpu().numpy()
+    assert np.array_equal(got, host)
