@@ -45,9 +45,12 @@ def test_dequant_small_config(hp, oracle):
     assert check_close(got, want) == 0
 
 
-@pytest.mark.parametrize("H,D,P", [(1, 3, 4), (3, 5, 2), (2, 8, 7), (1, 16, 1), (4, 32, 32)])
+@pytest.mark.parametrize("H,D,P", [(1, 3, 4), (3, 5, 2), (2, 8, 7), (1, 16, 1), (4, 32, 32),
+                                   (8, 256, 32), (32, 512, 4), (32, 1024, 2), (3, 48, 5)])
 def test_dequant_shapes(hp, oracle, H, D, P):
-    """Rows that are not a multiple of 16 elements take the element-wise path."""
+    """Rows that are not a multiple of 8 elements take the element-wise path, the others
+    8-code groups; copy units from 3 rows of 3 codes to 64 KiB pages (8 heads of 256 codes
+    x 32 slots, 32 heads of 512 x 4) and rows of 32 KiB."""
     w = inputs.quantized_pool(seed=H * 10 + D + P, num_pages=500, page_size=P, num_heads=H,
                               head_dim=D, num_seqs=5, len_lo=0, len_hi=70,
                               index_dtype=np.uint32 if P % 2 else np.uint64)

@@ -66,10 +66,14 @@ def test_schemes_small(hp, oracle, scheme, asym, dtype):
     assert check_close(got, want) == 0
 
 
-@pytest.mark.parametrize("H,D,P", [(3, 5, 4), (2, 12, 3), (4, 8, 1), (1, 24, 7)])
+@pytest.mark.parametrize("H,D,P", [(3, 5, 4), (2, 12, 3), (4, 8, 1), (1, 24, 7), (3, 16, 4),
+                                   (6, 32, 5), (5, 48, 3), (2, 16, 8), (8, 256, 32)])
 @pytest.mark.parametrize("scheme", list(SCHEMES))
 def test_schemes_shapes(hp, oracle, H, D, P, scheme):
-    """Rows or heads that do not split into groups of 8 take the element-wise path."""
+    """Rows or heads that do not split into groups of 8 take the element-wise path, the
+    others 8-code groups -- with per-channel parameters read once per thread when a row's
+    group count divides the CTA's 256 threads (4 and 256 groups) and per group
+    otherwise (6, 24 and 30 groups)."""
     w = inputs.quantized_pool(seed=H * 100 + D + P, num_pages=400, page_size=P, num_heads=H,
                               head_dim=D, num_seqs=5, len_lo=0, len_hi=60,
                               index_dtype=np.uint32 if P % 2 else np.uint64)

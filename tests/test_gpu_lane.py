@@ -119,3 +119,46 @@ def test_lane_synthetic_full_size_sampled(hp, oracle):
         one = np.ascontiguousarray(host[:, b:b + 1, h:h + 1])
         want = oracle.lane_gather(one, w.capacity, w.page_tokens, w.table, 1, 1, w.width, w.n)
         assert np.array_equal(got[b, h], want[0, 0])
+
+
+@pytest.mark.parametrize("B,H,P,W,dtype", [(3, 3, 16, 128, "bf16"), (1, 5, 8, 128, "f32"),
+                                           (2, 3, 4, 256, "bf16"), (1, 1, 16, 64, "bf16"),
+                                           (5, 7, 32, 32, "bf16"), (2, 2, 2, 512, "bf16"),
+                                           (4, 8, 16, 256, "bf16")])
+def test_lane_gather_run_sizes(hp, oracle, B, H, P, W, dtype):
+    """(lane, page) runs of 2-16 KiB: odd lane counts, live lengths that end in a partial
+    page, one row, the whole capacity; then one page ID outside the pool, whose rows are
+    skipped and reported while every other row still lands."""
+    import torch
+    rng = np.random.default_rng(B * 100 + H * 10 + P)
+    es = inputs.ELEM_BYTES[dtype]
+    C = int(rng.integers(3 * P, 60 * P))
+    N = -(-C // P)
+    T = rng.permutation(N).astype(np.uint64)
+    pool = rng.integers(0, 256, (N, B, H, P, W * es), dtype=np.uint8)
+    dpool = _dev(pool)
+    st = torch.full((1,), 9, dtype=torch.int32, device="cuda")
+    for n in (1, P + 1, C - 1, C, int(rng.integers(1, C + 1))):
+        nbytes = B * H * n * W * es
+        out = torch.full((nbytes + 64,), 0xEE, dtype=torch.uint8, device="cuda")
+        rc = hp.hp_lane_gather(dpool, _dev(T.view(np.int64)), C, P, B, H, W, dtype, n, out, st)
+        torch.cuda.synchronize()
+        assert rc == 0 and st.item() == 0
+        want = oracle.lane_gather(pool, C, P, T, B, H, W * es, n)
+        o = out.cpu().numpy()
+        assert np.array_equal(o[:nbytes], want.reshape(-1)), n
+        assert (o[nbytes:] == 0xEE).all()
+    bad = T.copy()
+    k = int(rng.integers(0, N))
+    bad[k] = N + 3
+    n = C
+    nbytes = B * H * n * W * es
+    out = torch.full((nbytes,), 0xEE, dtype=torch.uint8, device="cuda")
+    rc = hp.hp_lane_gather(dpool, _dev(bad.view(np.int64)), C, P, B, H, W, dtype, n, out, st)
+    torch.cuda.synchronize()
+    assert rc == 0 and hp.status_name(st.item()) == "HP_ERR_PHYSICAL_PAGE"
+    o = out.cpu().numpy().reshape(B * H, n, W * es)
+    good = oracle.lane_gather(pool, C, P, T, B, H, W * es, n).reshape(B * H, n, W * es)
+    rows = np.arange(n) // P == k
+    assert (o[:, rows] == 0xEE).all()
+    assert np.array_equal(o[:, ~rows], good[:, ~rows])
