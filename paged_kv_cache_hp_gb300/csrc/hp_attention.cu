@@ -42,6 +42,7 @@
 #include <algorithm>
 
 #include "hp_attn.cuh"
+#include "hp_attn_merge.cuh"
 #include "hp_internal.cuh"
 #include "hp_resolve.cuh"
 
@@ -100,13 +101,6 @@ __device__ __forceinline__ f2 mul2(f2 a, f2 b)
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ float exp2_approx(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // A 32-bit word of two 16-bit elements as an f2 (element 0 low).
 template <bool BF16>
 __device__ __forceinline__ f2 widen2(unsigned w)
@@ -166,92 +160,6 @@ __device__ __forceinline__ void issue_step(const AttnArgs& a, unsigned char* sta
     for (int m = 0; m < S::NPC; ++m) {
         cp_async16(kd + m * S::LT * 16, ks + m * S::LT * 16, n);
         cp_async16(kd + S::TS * S::ROW + m * S::LT * 16, vs + m * S::LT * 16, n);
-    }
-}
-
-// E floats of a record written earlier in this launch by another warp (L2, not L1).
-template <int E>
-__device__ __forceinline__ void load_dims(const float* p, float (&x)[E])
-{
-    if constexpr (E == 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
-        x[0] = v.x;
-        x[1] = v.y;
-    } else {
-#pragma unroll
-        for (int k = 0; k < E / 4; ++k) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(p) + k);
-            x[4 * k] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
-        }
-    }
-}
-
-// Merges the nr segment records of one (sequence, K/V head) -- record j's query head hh
-// at row row0 + j * H_kv * G + hh -- into the G normalised results at out + hh * D (the
-// lane's E dims).  The maxima and weight sums first: lane l takes head l % G of records
-// l / G, l / G + 32 / G, ... with a running (max, sum), and the lanes of a head merge
-// theirs pairwise; then the weighted accumulators, CH records at a time.
-template <int G, int E>
-__device__ __forceinline__ void merge_segments(const AttnArgs& a, uint64_t row0, uint64_t nr,
-                                            float* out, unsigned lane)
-{
-    constexpr int CH = G >= 8 ? 1 : 8 / G;  // records per pass of the accumulator loop
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-    const uint64_t stride = (uint64_t)a.Hkv * G, D = a.D;
-    float mx = -INFINITY, sm = 0.0f;
-    for (uint64_t j = lane / G; j < nr; j += 32 / G) {
-        const float2 x = __ldcg(ml + row0 + j * stride + lane % G);  // x.x finite
-        const float mn = fmaxf(mx, x.x);
-        sm = sm * exp2_approx(mx - mn) + x.y * exp2_approx(x.x - mn);
-        mx = mn;
-    }
-#pragma unroll
-    for (int o = G; o < 32; o <<= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
-        const float os = __shfl_xor_sync(0xffffffffu, sm, o);
-        const float mn = fmaxf(mx, om);
-        if (mn != -INFINITY) {
-            sm = sm * exp2_approx(mx - mn) + os * exp2_approx(om - mn);
-            mx = mn;
-        }
-    }
-    float M[G], acc[G][E];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        M[hh] = __shfl_sync(0xffffffffu, mx, hh);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[hh][e] = 0.0f;
-    }
-    const float L = sm;  // lane hh < G holds head hh's sum
-    for (uint64_t j = 0; j < nr; j += CH) {
-        float x[CH][G][E], w[CH][G];
-#pragma unroll
-        for (int c = 0; c < CH; ++c)
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const uint64_t row = row0 + (j + c < nr ? j + c : j) * stride + hh;
-                load_dims<E>(a.part_acc + row * D + lane * E, x[c][hh]);
-                w[c][hh] = j + c < nr ? __ldcg(ml + row).x : -INFINITY;
-            }
-#pragma unroll
-        for (int c = 0; c < CH; ++c)
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float wt = exp2_approx(w[c][hh] - M[hh]);  // 0 past the last record
-#pragma unroll
-                for (int e = 0; e < E; ++e) acc[hh][e] = fmaf(wt, x[c][hh][e], acc[hh][e]);
-            }
-    }
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        const float inv = 1.0f / __shfl_sync(0xffffffffu, L, hh);
-        float* o = out + hh * D;
-#pragma unroll
-        for (int e = 0; e < E; e += 2)
-            *reinterpret_cast<float2*>(o + e) = make_float2(acc[hh][e] * inv, acc[hh][e + 1] * inv);
     }
 }
 

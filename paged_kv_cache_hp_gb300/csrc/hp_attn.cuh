@@ -34,5 +34,11 @@ struct AttnArgs {
 };
 int launch_attention(int index_u64, const AttnArgs& a, void* stream);
 
+// Decode attention on the tensor cores (hp_attn_tc.cu): head_dim 128, pages of 8-128 slots,
+// K and V in device memory; a step is attention_tc_step_tokens() tokens.
+bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory);
+uint64_t attention_tc_step_tokens();
+int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream);
+
 
 }  // namespace hp

@@ -21,6 +21,7 @@ HP_OK = 0
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "u8": 4, "f64": 5}
 IDX_U32, IDX_U64 = 0, 1
 PERMISSIVE, HAS_QUANT, HOST_MEMORY, TEST_STALL = 0x1, 0x2, 0x4, 0x100
+ATTN_TENSOR_CORES, ATTN_CUDA_CORES = 0x8, 0x10
 
 _lock = threading.Lock()
 _lib = None

@@ -16,12 +16,24 @@ from paged_kv_cache_hp_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
+KF = 0  # the kernel the current test asks for (HP_ATTN_TENSOR_CORES or HP_ATTN_CUDA_CORES)
+
+
+@pytest.fixture(autouse=True, params=["tensor_cores", "cuda_cores"])
+def attn_kernel(request, hp):
+    """Every test here runs once on each kernel: the tensor-core kernel (where the shape
+    allows it: head_dim 128, pages of 8-128 slots; the others fall back to the CUDA cores)
+    and the CUDA-core kernel."""
+    global KF
+    KF = hp.ATTN_TENSOR_CORES if request.param == "tensor_cores" else hp.ATTN_CUDA_CORES
+    yield request.param
+
 
 def _run(hp, oracle, w, Hq, seed, scale=None):
     import torch
     D = w.head_dim
     scale = 1.0 / np.sqrt(D) if scale is None else scale
-    b = Batch(w)
+    b = Batch(w, flags=KF)
     wv = inputs.Workload(**{**w.__dict__, "pool_seed": w.pool_seed + 77})
     vpool = inputs.device_pool(wv, "cuda")
     rng = np.random.default_rng(seed)
@@ -57,6 +69,8 @@ def _check(got, want, vmax):
     ("bf16", 4, 2, 256, 5, None), ("f16", 3, 8, 128, 3, None), ("bf16", 12, 1, 128, 32, None),
     ("bf16", 2, 8, 256, 16, None), ("f16", 2, 8, 64, 16, None), ("f16", 1, 4, 64, 1, None),
     ("bf16", 8, 4, 128, 16, 1.5),  # peaked softmax: a few tokens carry the weight
+    # the tensor-core kernel's other page sizes (steps of 16, 4, 2 and 1 pages)
+    ("bf16", 2, 8, 128, 8, None), ("f16", 4, 2, 128, 64, None), ("bf16", 1, 1, 128, 128, None),
 ])
 def test_attention_matches_oracle(hp, oracle, dtype, Hkv, G, D, P, scale):
     # lengths up to ~1300 tokens: small pages move the 32-page window many times
@@ -134,7 +148,7 @@ def test_attention_full_size_sampled(hp, oracle):
 def test_attention_rejections(hp, oracle):
     import torch
     w = inputs.config("decode_gather", "small")   # 32 heads of 128, fp16
-    b = Batch(w)
+    b = Batch(w, flags=KF)
     rc, n = hp.hp_attention_decode_workspace_bytes(b.desc, 32)
     ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
     q = torch.zeros((w.num_seqs, 48, 128), dtype=torch.float16, device="cuda")
@@ -193,7 +207,7 @@ def test_attention_validates_permissive_descriptors(hp, oracle, fault):
     else:
         lens[1] = (int(w.seq_ptr[2]) - int(w.seq_ptr[1])) * 16 + 1
     w = inputs.Workload(**{**w.__dict__, "table": table, "lens": lens})
-    b = Batch(w, pool=pool, flags=hp.PERMISSIVE)
+    b = Batch(w, pool=pool, flags=hp.PERMISSIVE | KF)
     rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, 4)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
     q = torch.zeros((w.num_seqs, 4, 64), dtype=torch.bfloat16, device="cuda")
@@ -216,7 +230,7 @@ def test_planned_attention_over_layers(hp, oracle, dtype, Hkv, G, D):
     w = inputs.decode_gather(seed=31 + D + G, num_pages=3000, page_size=16, num_heads=Hkv,
                              head_dim=D, num_seqs=6, len_lo=0, len_hi=2500, dtype=dtype)
     Hq = Hkv * G
-    b = Batch(w)
+    b = Batch(w, flags=KF)
     rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, Hq)
     ws_plan = torch.full((nws,), 0xFF, dtype=torch.uint8, device="cuda")
     ws_one = torch.zeros(nws, dtype=torch.uint8, device="cuda")
@@ -232,7 +246,7 @@ def test_planned_attention_over_layers(hp, oracle, dtype, Hkv, G, D):
     assert hp.hp_attention_plan(b.desc, Hq, ws_plan, b.status) == 0
     for kl, vl, ql in layers:
         dl = hp.PagedDesc(kl, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages, page_size=16,
-                          num_heads=Hkv, head_dim=D, dtype=dtype, index_type=b.it)
+                          num_heads=Hkv, head_dim=D, dtype=dtype, index_type=b.it, flags=KF)
         got = torch.full((w.num_seqs, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
         want = torch.full_like(got, float("nan"))
         assert hp.hp_attention_decode_planned(dl, vl, ql, Hq, 0.09, got, ws_plan, b.status) == 0
@@ -256,7 +270,7 @@ def test_planned_attention_after_a_failed_plan_writes_nothing(hp, oracle):
     table = w.table.copy()
     table[0] = w.num_pages
     w = inputs.Workload(**{**w.__dict__, "table": table})
-    b = Batch(w, pool=pool)
+    b = Batch(w, pool=pool, flags=KF)
     rc, nws = hp.hp_attention_decode_workspace_bytes(b.desc, 4)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
     q = torch.zeros((w.num_seqs, 4, 64), dtype=torch.bfloat16, device="cuda")

@@ -147,17 +147,19 @@ def test_lane_gather_and_append_on_a_host_pool(hp, oracle):
 
 
 def test_decode_attention_on_host_resident_k_and_v(hp, oracle):
-    """K and V pools in page-locked host memory (an offloaded cache): the kernel's cp.async
-    loads read them over the host link; the result is bit for bit the one from device
-    pools."""
+    """K and V pools in page-locked host memory (an offloaded cache, HP_HOST_MEMORY): the
+    CUDA-core kernel's cp.async loads read them over the host link; the result is bit for
+    bit the one the same kernel gives from device pools (HP_HOST_MEMORY set there too, which
+    keeps the call off the tensor-core kernel), and matches the oracle."""
     import torch
     w = inputs.decode_gather(seed=61, num_pages=400, page_size=16, num_heads=2, head_dim=128,
                              num_seqs=4, len_lo=1, len_hi=1500, dtype="bf16")
-    b = Batch(w)
+    b = Batch(w, flags=hp.HOST_MEMORY)
     vdev = inputs.device_pool(inputs.Workload(**{**w.__dict__, "pool_seed": 62}), "cuda")
     khost, vhost = _pinned_copy(b.pool), _pinned_copy(vdev)
     dh = hp.PagedDesc(khost, b.table, b.seq_ptr, b.lens, num_pages=w.num_pages, page_size=16,
-                      num_heads=2, head_dim=128, dtype="bf16", index_type=b.it)
+                      num_heads=2, head_dim=128, dtype="bf16", index_type=b.it,
+                      flags=hp.HOST_MEMORY)
     g = torch.Generator(device="cuda")
     g.manual_seed(63)
     q = torch.randn((w.num_seqs, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
@@ -170,3 +172,8 @@ def test_decode_attention_on_host_resident_k_and_v(hp, oracle):
     torch.cuda.synchronize()
     assert b.status_value() == 0
     assert torch.equal(got.view(torch.int32), want.view(torch.int32))
+    ref = b.oracle_desc().attention_decode(vdev.cpu().numpy(),
+                                           q.view(torch.int16).cpu().numpy().view(np.uint16), 8,
+                                           0.09)
+    vmax = float(vdev.view(torch.bfloat16).float().abs().max())
+    assert np.abs(got.cpu().numpy() - ref).max() <= 1e-4 * vmax + 1e-6
