@@ -692,11 +692,11 @@ def rate_entry(bytes_, ms, peak, **kw):
     return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
 
 
-def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False):
+def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False, kernel="auto"):
     """Decode attention alone on the decode-append batch at `scale` ("full": 256 sequences
     of 1K-32K tokens; "mid": 32 of them, about 2.5 GB on the device, the profiler's case;
     "short": 2048 sequences of 16-1024 tokens); host_kv: K and V in page-locked host
-    memory."""
+    memory (HP_HOST_MEMORY); kernel: "auto" (the library's choice), "tensor" or "cuda"."""
     import torch
     w = inputs.config("decode_append", scale)
     pool = inputs.device_pool(w, dev)
@@ -705,16 +705,20 @@ def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False):
         hk = torch.empty(pool.shape, dtype=pool.dtype, pin_memory=True)
         hk.copy_(pool)
         pool = hk
+    flags = {"auto": 0, "tensor": hp.ATTN_TENSOR_CORES, "cuda": hp.ATTN_CUDA_CORES}[kernel]
+    if host_kv:
+        flags |= hp.HOST_MEMORY
     d_k = hp.PagedDesc(pool, idx_tensor(w.table, dev), idx_tensor(w.seq_ptr, dev),
                        idx_tensor(w.lens, dev), num_pages=w.num_pages, page_size=w.page_size,
-                       num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype, index_type=0)
+                       num_heads=w.num_heads, head_dim=w.head_dim, dtype=w.dtype, index_type=0,
+                       flags=flags)
     stream = torch.cuda.current_stream()
     res = attention_measurement(dev, hp, inputs, w, d_k, peak,
                                 lambda b, ms, **kw: rate_entry(b, ms, peak, **kw),
                                 lambda fn, n: median_ms(fn, stream, n), reps=reps, host_kv=hk)
     res.update(op="decode_attention", workload=w.name, num_seqs=w.num_seqs,
                total_tokens=w.total_tokens, num_heads=w.num_heads, head_dim=w.head_dim,
-               kv_memory="page-locked host" if host_kv else "device")
+               kv_memory="page-locked host" if host_kv else "device", kernel=kernel)
     return res
 
 
@@ -1222,6 +1226,8 @@ def main():
                          "sequences) and print its line")
     ap.add_argument("--host-kv", action="store_true",
                     help="with --attention: K and V pools in page-locked host memory")
+    ap.add_argument("--attention-kernel", default="auto", choices=["auto", "tensor", "cuda"],
+                    help="with --attention: the library's choice of kernel, or force one")
     ap.add_argument("--transpose", action="store_true",
                     help="time only the two cache layout conversions (kernel-internal "
                          "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
@@ -1285,7 +1291,8 @@ def main():
         build.build()
         hp.lib()
         print(json.dumps(attention_only(args.attention, "cuda", hp, inputs, peak_hbm()[0],
-                                        args.steps, host_kv=args.host_kv)))
+                                        args.steps, host_kv=args.host_kv,
+                                        kernel=args.attention_kernel)))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
