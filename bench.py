@@ -1027,10 +1027,15 @@ def ops_measurements(dev, hp, inputs, peak, oracle_mod=None, reps=20):
 
     def step_us(fn, n=300):
         """Steps issued back to back, as a decode loop issues them: (issue-bound) time
-        per step, and the same step captured once in a CUDA graph and replayed."""
-        for _ in range(5):
-            fn()
-        torch.cuda.synchronize()
+        per step, and the same step captured once in a CUDA graph and replayed.  About
+        50 ms of the step first: after the seconds of host work the CPU baselines take, the
+        GPU's clocks need that long to come back up (a 256-row append then replayed in
+        10 us instead of 8.2)."""
+        t_end = time.perf_counter() + 0.05
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                fn()
+            torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(n):
