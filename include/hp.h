@@ -143,13 +143,15 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * hp_copy_pages, hp_lane_gather and hp_lane_append. */
 #define HP_HOST_MEMORY 0x4u
 /* Decode attention's kernel (no counterpart in the pages).  By default the library picks:
- * the tensor-core kernel when the shape allows it (head_dim 128, pages of 8-128 slots,
- * device memory) and the batch has at least HP_ATTN_TC_MIN_STEPS steps of 128 tokens per
- * SM and K/V head (table_len * page_size / 128 / SMs), the CUDA-core kernel otherwise
- * (measured on GB300: the tensor-core kernel is faster on long batches, the CUDA-core one
- * on short ones).  HP_ATTN_TENSOR_CORES asks for the tensor-core kernel wherever the shape
- * allows it, HP_ATTN_CUDA_CORES for the CUDA-core kernel always.  The plan and the planned
- * calls that follow it must carry the same flags. */
+ * the tensor-core kernel when the shape allows it (head_dim 128; 1, 2, 4 or 8 K/V heads;
+ * G = num_q_heads / num_heads in {1, 2, 4, 8} with at most 32 query heads; pages of a
+ * power of two from 8 to 128 / num_heads slots; device memory) and the batch has at least
+ * HP_ATTN_TC_MIN_STEPS steps of 128 (head, token) rows per SM (table_len * page_size *
+ * num_heads / 128 / SMs), the CUDA-core kernel otherwise (measured on GB300: the
+ * tensor-core kernel is as fast or faster from about 150 steps per SM up, the CUDA-core one
+ * on batches of few, short sequences).  HP_ATTN_TENSOR_CORES asks for the tensor-core
+ * kernel wherever the shape allows it, HP_ATTN_CUDA_CORES for the CUDA-core kernel always.
+ * The plan and the planned calls that follow it must carry the same flags. */
 #define HP_ATTN_TENSOR_CORES 0x8u
 #define HP_ATTN_CUDA_CORES 0x10u
 #define HP_ATTN_TC_MIN_STEPS 128
@@ -433,10 +435,11 @@ int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t nu
  * has the pool's element type (HP_F16 or HP_BF16); out (device, fp32, same shape) gets 0
  * for a sequence with no tokens.  Arithmetic is fp32.  Supported: head_dim 64, 128 or
  * 256, num_q_heads / num_heads in {1, 2, 4, 8}, page_size <= 2^26 (HP_ERR_ARG otherwise).
- * With head_dim 128, pages of 8, 16, 32, 64 or 128 slots and both pools in device memory
- * the scores and the weighted value sums may run on the tensor cores (products of the
- * 16-bit inputs accumulated in fp32; the weights as two 16-bit parts, so the result stays
- * within about 2^-16 of max|V| of the fp32 one); otherwise on the CUDA cores in fp32 --
+ * With head_dim 128, 1, 2, 4 or 8 K/V heads, at most 32 query heads, pages of 8 to
+ * 128 / num_heads slots and both pools in device memory the scores and the weighted value
+ * sums may run on the tensor cores (products of the 16-bit inputs accumulated in fp32; the
+ * weights as two 16-bit parts, so the result stays within about 2^-16 of max|V| of the
+ * fp32 one); otherwise on the CUDA cores in fp32 --
  * see HP_ATTN_TENSOR_CORES for the choice.  K and V pools in page-locked host memory need
  * HP_HOST_MEMORY in k_desc's flags (they are then read in place over the host link by the
  * CUDA-core kernel).

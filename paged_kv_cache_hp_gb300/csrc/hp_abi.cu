@@ -647,22 +647,23 @@ u64 attn_step_tokens(u64 G, u64 D)
 }
 uint32_t attn_ranges_per_cta(u64 Hkv) { return Hkv < 8 ? (uint32_t)(8 / Hkv) : 1u; }
 
-// The tensor-core kernel serves head_dim 128 on device-memory pools with pages of 8-128
-// slots (its steps are 128 tokens); by default only batches with enough steps per SM and
-// K/V head to keep its one CTA per SM streaming (measured: it leads on 256 sequences of
-// 1K-32K tokens, the CUDA-core kernel on 32 of them and on 2048 short ones).  The plan and
-// the planned call decide alike, from the descriptor alone.
-bool attn_on_tensor_cores(const hp_paged_desc* d)
+// The tensor-core kernel serves head_dim 128 on device-memory pools with power-of-two K/V
+// head counts up to 8, at most 32 query heads and pages of 8 .. 128 / H_kv slots (its steps
+// are 128 (head, token) rows); by default only batches with at least HP_ATTN_TC_MIN_STEPS
+// such steps per SM.  The plan and the planned call decide alike, from the descriptor and
+// the query heads alone.
+bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
 {
     if (!hp::attention_tc_fits(d->head_dim, d->page_size, d->num_pages,
-                               (d->flags & HP_HOST_MEMORY) != 0) ||
-        (d->flags & HP_ATTN_CUDA_CORES))
-        return false;
+                               (d->flags & HP_HOST_MEMORY) != 0, d->num_heads, G * d->num_heads) ||
+        (d->flags & HP_ATTN_CUDA_CORES) || (u128)d->num_seqs * G * d->num_heads >= (1ull << 31))
+        return false;  // (the query rows are addressed by a 32-bit tensor coordinate)
     if (d->flags & HP_ATTN_TENSOR_CORES) return true;
     int dev = 0;
     const int sms = hp::current_sms(&dev);
     if (sms == 0) return false;
-    const u128 steps = (u128)d->table_len * d->page_size / hp::attention_tc_step_tokens();
+    const u128 steps =
+        (u128)d->table_len * d->page_size / hp::attention_tc_step_tokens(d->num_heads);
     return steps >= (u128)HP_ATTN_TC_MIN_STEPS * (u128)sms;
 }
 
@@ -744,8 +745,8 @@ HP_API int hp_attention_plan(const hp_paged_desc* k_desc, uint32_t num_q_heads, 
                                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return HP_ERR_CUDA;
     hp::PlanArgs pa = plan_args(d, workspace, d_status);
-    pa.step_tokens = attn_on_tensor_cores(d) ? hp::attention_tc_step_tokens()
-                                             : attn_step_tokens(p.G, d->head_dim);
+    pa.step_tokens = attn_on_tensor_cores(d, p.G) ? hp::attention_tc_step_tokens(d->num_heads)
+                                                  : attn_step_tokens(p.G, d->head_dim);
     return hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
 }
 
@@ -789,7 +790,7 @@ HP_API int hp_attention_decode_planned(const hp_paged_desc* k_desc, const void* 
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
     a.d_status = d_status;
-    if (attn_on_tensor_cores(d)) return hp::launch_attention_tc(d->index_type == HP_IDX_U64, a, stream);
+    if (attn_on_tensor_cores(d, p.G)) return hp::launch_attention_tc(d->index_type == HP_IDX_U64, a, stream);
     return hp::launch_attention(d->index_type == HP_IDX_U64, a, stream);
 }
 

@@ -34,10 +34,13 @@ struct AttnArgs {
 };
 int launch_attention(int index_u64, const AttnArgs& a, void* stream);
 
-// Decode attention on the tensor cores (hp_attn_tc.cu): head_dim 128, pages of 8-128 slots,
-// K and V in device memory; a step is attention_tc_step_tokens() tokens.
-bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory);
-uint64_t attention_tc_step_tokens();
+// Decode attention on the tensor cores (hp_attn_tc.cu): head_dim 128, K and V in device
+// memory, H_kv in {1, 2, 4, 8} K/V heads, G in {1, 2, 4, 8} query heads per K/V head with
+// at most 32 query heads, pages of 8 .. 128 / H_kv slots (a power of two); a step is
+// attention_tc_step_tokens(H_kv) = 128 / H_kv tokens of a sequence and all its K/V heads.
+bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory,
+                       uint64_t num_kv_heads, uint64_t num_q_heads);
+uint64_t attention_tc_step_tokens(uint64_t num_kv_heads);
 int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream);
 
 

@@ -1,36 +1,48 @@
 // hp_attn_tc.cu -- decode attention through the block table on the tensor cores (tcgen05),
-// for head_dim 128 and pages of 8-128 slots.
+// for head_dim 128.
 //
 // The same computation as hp_attention.cu ("Visualize PagedAttention block layout", How the
 // attention kernel uses the block table; K(s,t,g) and V(s,t,g) read through the Element
 // Lookup of "Block-Paged Layout -- Hurray Format Specification"): for sequence s and query
 // head qh (K/V head g = qh / G), score_t = scale * q . K(s,t,g) over t < len_s, softmax over
 // t, out = sum_t weight_t V(s,t,g).  The work is split the same way -- steps balanced over
-// workers, segments, records merged by the last segment's finisher -- with a step of 128
-// tokens of one K/V head, and the two contractions of a step on the tensor cores:
-//   S [128 tokens x 16]  = K [128 x 128 dims] . Q^T        (the G query heads, padded to 16)
-//   O^T [128 dims x 16]  = V^T [128 dims x 128 tokens] . P^T
+// workers, one record per segment of a sequence, the records merged by the last segment's
+// finisher -- with a step of TS = 128 / H_kv tokens of a sequence and ALL its K/V heads: the
+// 128 rows of the step's tiles are (head, token) pairs, h * TS + t.  So a step reads whole
+// pages (all heads of its tokens, contiguous in the pool) and a worker's range holds few
+// segments.  The two contractions of a step run on the tensor cores (kind::f16, fp32
+// accumulators in TMEM):
+//   S [128 rows x 32] = K [128 rows x 128 dims] . Q^T     Q: the sequence's Hq <= 32 query
+//                                                         heads (padded to 32); row h * TS + t
+//                                                         keeps the G columns of head h
+//   O_h^T [128 dims x 16] = V_h^T [128 dims x TS] . P_h^T for each K/V head h: its TS rows of
+//                                                         V and its weights (G rows, padded)
 // One CTA per SM, six roles, each running ahead as far as its buffers allow:
-//   warps 0, 7  TMA: per step, the K (warp 0) and V (warp 7) rows of the step's pages (one
-//               head's 128 dims of P tokens per box, two 64-dim boxes per page, 128-byte
-//               swizzled by the tensor map) into rings of 3 stages of 32 KiB, counted on
-//               "k_full"/"v_full"; a K stage comes back once S has read it, a V stage once
-//               O has;
-//   warp 1      tcgen05.mma issue of S (one thread): step j into TMEM buffer j % 2 as soon
-//               as its K stage and the segment's Q are in, committed to "s_full";
-//   warp 6      tcgen05.mma issue of O (one thread): step j from its V stage and weights,
-//               committed to "o_full";
+//   warps 0, 7  TMA: per step, the K (warp 0) and V (warp 7) rows of the step's pages, one
+//               box per (head, page): 64 dims x 1 head x P tokens, 128-byte swizzled by the
+//               tensor map, two per (head, page) for the two 64-dim halves, into rings of 3
+//               stages of 32 KiB counted on "k_full"/"v_full"; warp 0 also brings each
+//               segment's queries (one box per half); a K stage comes back once S has read
+//               it, a V stage once O has;
+//   warp 1      tcgen05.mma issue of S (one thread, 8 products of K = 16), committed to
+//               "s_full";
+//   warp 6      tcgen05.mma issue of the H_kv O products (one thread, 8 slices of 16 rows,
+//               twice each: hi and lo weights), committed to "o_full"; both issuers run
+//               unrolled code with the descriptors precomputed, because a product of M = 128
+//               and N <= 64 keeps the tensor pipe only about 45 cycles (measured on GB300),
+//               less than a loop that rebuilds descriptors takes to issue it;
 //   warps 2-5   softmax and accumulation, one thread per TMEM lane: a step's scores (lane =
-//               token), masked past the sequence, the running maximum per query head (a
-//               cross-warp maximum through shared memory), the weights written as bfloat16
-//               (or half) pairs hi + lo = p (so P.V keeps about 16 significant bits where a
-//               single 16-bit P would keep 8), then the previous step's O (lane = dim) folded
-//               into fp32 registers with the usual online-softmax rescaling.
+//               row = (head, token)), masked past the sequence, the running maximum of each
+//               query head (a shuffle reduction over the head's rows), the weights written as
+//               16-bit pairs hi + lo = p (so P.V keeps about 16 significant bits where one
+//               16-bit P would keep 8), then the previous step's O (lane = dim) folded into
+//               fp32 registers, rescaled only on the steps where some query's maximum rose.
 // Rows of V past the sequence (an unfilled last page, or pages a step does not have) are
 // zeroed in shared memory before their weights (zero) are handed over, so no stale or
 // undefined value reaches the product.  Every wait is bounded (about 2 s); a wait that runs
-// out reports HP_ERR_TIMEOUT, and every role then leaves its loop; the loads and the matrix
-// operations already issued are waited for (bounded) before the TMEM is freed.
+// out reports HP_ERR_TIMEOUT, every role leaves its loop (the softmax threads decide it
+// together at their one barrier per step, so none is left at a barrier), and the loads and
+// matrix operations already issued are waited for (bounded) before the TMEM is freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,17 +61,20 @@ namespace {
 
 using namespace tma;
 
-constexpr int kTok = 128;           // tokens per step
+constexpr int kRows = 128;          // rows of a step's tiles: H_kv heads x TS tokens
 constexpr int kD = 128;             // head_dim
-constexpr int kN = 16;              // query-head columns of the MMAs (G padded)
+constexpr int kNS = 32;             // S columns: the query heads, padded
+constexpr int kNO = 16;             // O columns of one K/V head: its G query heads, padded
+constexpr int kMaxHkv = 8;
 constexpr int kKV = 3;              // K/V stages
-constexpr uint32_t kHalf = kTok * 128;       // one 64-dim half of a K or V tile (16 KiB)
+constexpr uint32_t kHalf = kRows * 128;      // one 64-dim half of a K or V tile (16 KiB)
 constexpr uint32_t kTile = 2 * kHalf;        // one K or V tile (32 KiB)
-constexpr uint32_t kPBuf = 2 * kN * 128;     // one P operand: 16 rows x 128 tokens (4 KiB)
-constexpr uint32_t kQBuf = 2 * kN * 128;     // one Q operand: 16 rows x 128 dims (4 KiB)
+constexpr uint32_t kPBuf = 2 * kNO * 128;    // one P operand: 16 rows x 128 (head, token) cols
+constexpr uint32_t kQBuf = 2 * kNS * 128;    // one Q operand: 32 rows x 128 dims (8 KiB)
 constexpr int kThreadsTc = 8 * 32;
 constexpr int kSoftmax = 128;       // warps 2-5
-constexpr uint32_t kTmemCols = 64;  // S x 2 buffers, O x 2 buffers
+constexpr uint32_t kTmemCols = 512; // S x 2 (64 columns), O x 2 (up to 2 x 8 x 16)
+constexpr uint32_t kOCol = 2 * kNS; // first O column
 
 // shared memory: K ring, V ring, then P (2 steps x hi/lo), then Q (2 segments)
 constexpr uint32_t kOffP = kKV * 2 * kTile;
@@ -77,11 +92,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint
 }
 
 // kind::f16 instruction descriptor: fp32 accumulator, A and B both bf16 (or both f16),
-// A K-major (S) or M-major (O^T), B K-major, N = 16, M = 128.
-__host__ __device__ constexpr uint32_t mma_idesc(bool bf16, bool a_mn_major)
+// A K-major (S) or M-major (O^T), B K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t mma_idesc(bool bf16, bool a_mn_major, uint32_t n)
 {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(kN >> 3) << 17) | ((128u >> 4) << 24);
+           ((a_mn_major ? 1u : 0u) << 15) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
@@ -99,17 +114,87 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// tcgen05.ld of N consecutive TMEM columns of this thread's lane (32x32b shape) into r,
+// not yet waited for; the column is a multiple of N
+template <int N> __device__ __forceinline__ void tmem_issue(uint32_t taddr, uint32_t* r);
+
+template <> __device__ __forceinline__ void tmem_issue<1>(uint32_t taddr, uint32_t* r)
 {
-    uint32_t r[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                 : "=r"(r[0])
                  : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <> __device__ __forceinline__ void tmem_issue<2>(uint32_t taddr, uint32_t* r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(taddr));
+}
+
+template <> __device__ __forceinline__ void tmem_issue<4>(uint32_t taddr, uint32_t* r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+
+template <> __device__ __forceinline__ void tmem_issue<8>(uint32_t taddr, uint32_t* r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+template <> __device__ __forceinline__ void tmem_issue<16>(uint32_t taddr, uint32_t* r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
+
+// waits for this thread's TMEM loads; the registers they fill are operands of the wait, so
+// no use of them is scheduled above it
+template <int N> __device__ __forceinline__ void tmem_wait(uint32_t (&r)[N]);
+
+template <> __device__ __forceinline__ void tmem_wait<1>(uint32_t (&r)[1])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0])::"memory");
+}
+
+template <> __device__ __forceinline__ void tmem_wait<2>(uint32_t (&r)[2])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1])::"memory");
+}
+
+template <> __device__ __forceinline__ void tmem_wait<4>(uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3])::"memory");
+}
+
+template <> __device__ __forceinline__ void tmem_wait<8>(uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])::"memory");
+}
+
+template <> __device__ __forceinline__ void tmem_wait<16>(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
+}
+
+template <> __device__ __forceinline__ void tmem_wait<32>(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+// N consecutive TMEM columns of this thread's lane, waited for
+template <int N> __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N])
+{
+    uint32_t r[N];
+    tmem_issue<N>(taddr, r);
+    tmem_wait<N>(r);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -147,8 +232,9 @@ __device__ __forceinline__ void named_sync(int id, int n)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// true in every one of the n threads at named barrier `id` iff v is true in all of them: the
-// softmax threads take every decision to stop together, so none is left at a barrier
+// true in every one of the n threads at named barrier `id` iff v is true in all (and) / in
+// any (or) of them; the softmax threads take every decision to stop together, so none is
+// left at a barrier
 __device__ __forceinline__ bool named_and(int id, int n, bool v)
 {
     uint32_t r;
@@ -159,57 +245,72 @@ __device__ __forceinline__ bool named_and(int id, int n, bool v)
                  : "memory");
     return r != 0;
 }
+__device__ __forceinline__ bool named_or(int id, int n, bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+                 "barrier.cta.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "r"(id), "r"(n)
+                 : "memory");
+    return r != 0;
+}
 
-// The segments of a worker's step range, in the order every role walks them: for each K/V
-// head g, the sequences whose steps meet [beg, end).
+// The segments of a worker's step range, in the order every role walks them: the sequences
+// whose steps meet [beg, end).
 struct SegWalk {
     const unsigned long long* units_off;
-    uint64_t num_seqs, beg, end, s_first;
-    uint32_t Hkv;
-    uint32_t g = 0;
-    uint64_t s = 0, pos = 0;
-    bool started = false;
-    // next segment: head g, sequence s, steps k0 .. k1 - 1 of it; false at the end
-    __device__ bool next(uint32_t& og, uint64_t& os, uint64_t& k0, uint64_t& k1)
+    uint64_t beg, end, s;
+    uint64_t pos = ~0ull;
+    // next segment: sequence s, steps k0 .. k1 - 1 of it; false at the end
+    __device__ bool next(uint64_t& os, uint64_t& k0, uint64_t& k1)
     {
-        if (!started) {
-            started = true;
-            g = 0;
-            s = s_first;
-            pos = beg;
-        }
-        while (g < Hkv) {
-            if (pos < end) {
-                while (units_off[s + 1] <= pos) ++s;  // skips sequences without steps
-                const uint64_t so = units_off[s];
-                k0 = pos - so;
-                k1 = umin(units_off[s + 1], end) - so;
-                pos = so + k1;
-                og = g;
-                os = s;
-                return true;
-            }
-            ++g;
-            s = s_first;
-            pos = beg;
-        }
-        return false;
+        if (pos == ~0ull) pos = beg;
+        if (pos >= end) return false;
+        while (units_off[s + 1] <= pos) ++s;  // skips sequences without steps
+        const uint64_t so = units_off[s];
+        k0 = pos - so;
+        k1 = umin(units_off[s + 1], end) - so;
+        pos = so + k1;
+        os = s;
+        return true;
     }
 };
 
-template <typename IndexT, bool BF16, int G>
+__device__ __forceinline__ unsigned long long table_at(const void* table, bool u64, uint64_t i)
+{
+    return u64 ? (unsigned long long)static_cast<const unsigned long long*>(table)[i]
+               : (unsigned long long)static_cast<const unsigned int*>(table)[i];
+}
+
+// Run-time shape of a launch, beside AttnArgs.
+struct TcShape {
+    uint32_t hkv;   // K/V heads: 1, 2, 4 or 8
+    uint32_t ts;    // tokens per step: 128 / hkv
+    uint32_t lts;   // log2(ts)
+    uint32_t pps;   // pages per step: ts / page_size
+    uint32_t idx64; // index type: uint64 (1) or uint32 (0)
+    uint32_t bf16;  // element type: bf16 (1) or f16 (0)
+};
+
+template <int G>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+    attn_tc_kernel(const AttnArgs a, const TcShape sh, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq)
 {
+    constexpr int kHeads = (kMaxHkv * G < kNS ? kMaxHkv * G : kNS) / G;  // K/V heads at most
+    constexpr int kAcc = kHeads * G;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long k_full[kKV], v_full[kKV], k_free[kKV], v_free[kKV];
     __shared__ __align__(8) unsigned long long s_full[2], s_free[2], p_full[2], o_full[2],
         o_free[2], q_full[2], q_free[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float red[4][kN];
+    __shared__ float corr_s[2][kNS];  // per step parity: each query head's rescale factor
+    __shared__ float red_s[4][8];     // per-warp maxima or sums when a head's rows span warps
+    __shared__ float ml_s[2][kNS];    // a segment's maxima and weight sums per query head
     __shared__ unsigned merge_done;
+    __shared__ int fail_s[2];         // softmax waits that ran out, by step parity
 
     pdl_wait();  // the plan before this launch is complete
     if (a.hdr->verdict != kVerdictOk) return;
@@ -220,7 +321,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             float4* o = reinterpret_cast<float4*>(a.out + s * a.Hq * a.D);
             for (uint64_t i = lane; i < a.Hq * a.D / 4; i += 32) o[i] = make_float4(0, 0, 0, 0);
         }
-    const uint64_t S_steps = a.hdr->total_units;  // steps of all sequences, one head
+    const uint64_t S_steps = a.hdr->total_units;  // steps of all sequences (all heads each)
     const uint64_t Lw = (S_steps + a.workers - 1) / a.workers;
     const uint64_t v = blockIdx.x;  // worker index (one per CTA)
     const uint64_t beg = umin(v * Lw, S_steps), end = umin(beg + Lw, S_steps);
@@ -246,13 +347,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mbar_init(smem_u32(&q_free[i]), 1);
         }
         abort_flag = 0;
+        fail_s[0] = fail_s[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // the P operands' padding rows (query heads G..15) stay zero for the whole launch
-    for (uint32_t i = threadIdx.x; i < 2 * 2 * kPBuf / 16; i += kThreadsTc)
+    // padding rows stay zero for the whole launch: P rows G..15, Q rows Hq..31
+    for (uint32_t i = threadIdx.x; i < (2 * 2 * kPBuf + 2 * kQBuf) / 16; i += kThreadsTc)
         *reinterpret_cast<uint4*>(smem + kOffP + i * 16) = make_uint4(0, 0, 0, 0);
-    for (uint32_t i = threadIdx.x; i < 2 * kQBuf / 16; i += kThreadsTc)
-        *reinterpret_cast<uint4*>(smem + kOffQ + i * 16) = make_uint4(0, 0, 0, 0);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -265,13 +365,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = tmem_base;
-    const IndexT* table = static_cast<const IndexT*>(a.table);
-    const IndexT* spp = static_cast<const IndexT*>(a.seq_ptr);
-    const IndexT* lensp = static_cast<const IndexT*>(a.lens);
-    const uint32_t P = (uint32_t)a.page_size;
-    const uint32_t ppt = kTok / P;  // pages per step
-    SegWalk walk{a.units_off, a.num_seqs, beg, end, find_seq(a.units_off, a.num_seqs, beg),
-                 a.Hkv};
+    const uint32_t P = (uint32_t)a.page_size, TS = sh.ts, HKV = sh.hkv, PPS = sh.pps;
+    const bool u64 = sh.idx64 != 0, bf16 = sh.bf16 != 0;
+    SegWalk walk{a.units_off, beg, end, find_seq(a.units_off, a.num_seqs, beg)};
     auto failed = [&](bool ok) {
         if (!ok) {
             abort_flag = 1;
@@ -287,24 +383,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         unsigned long long* full = is_k ? k_full : v_full;
         unsigned long long* freed = is_k ? k_free : v_free;
         const uint32_t base = sm0 + (is_k ? 0u : kKV * kTile);
+        const uint32_t lh = lane / PPS, li = lane % PPS;  // this lane's (head, page of the step)
+        const bool active = lane < HKV * PPS;
         uint64_t j = 0, seg = 0;  // steps and segments issued
-        uint32_t g;
         uint64_t s, k0, k1;
         bool stop = false;
-        while (!stop && walk.next(g, s, k0, k1)) {
-            const uint64_t len = lensp[s], tab0 = spp[s];
+        while (!stop && walk.next(s, k0, k1)) {
+            const uint64_t len = table_at(a.lens, u64, s), tab0 = table_at(a.seq_ptr, u64, s);
             if (is_k) {
-                // the segment's G query rows, both 64-dim halves, into Q buffer seg % 2 once
-                // the S of segment seg - 2 have read it (rows G..15 stay zero)
+                // the sequence's query heads, both 64-dim halves, into Q buffer seg % 2 once
+                // the S of segment seg - 2 have read it (rows Hq..31 stay zero)
                 int ok = 1;
                 if (lane == 0) {
                     ok = seg < 2 || mbar_wait(smem_u32(&q_free[seg % 2]), (uint32_t)((seg / 2 - 1) & 1));
                     if (ok) {
                         const uint32_t qb = sm0 + kOffQ + (uint32_t)(seg % 2) * kQBuf;
-                        const int row = (int)(s * a.Hq + (uint64_t)g * G);
-                        mbar_expect_tx(smem_u32(&q_full[seg % 2]), 2 * G * 128);
+                        const int row = (int)(s * a.Hq);
+                        mbar_expect_tx(smem_u32(&q_full[seg % 2]), 2 * a.Hq * 128);
                         tma_2d(qb, &tmq, 0, row, smem_u32(&q_full[seg % 2]));
-                        tma_2d(qb + 2048, &tmq, 64, row, smem_u32(&q_full[seg % 2]));
+                        tma_2d(qb + kNS * 128, &tmq, 64, row, smem_u32(&q_full[seg % 2]));
                     }
                 }
                 if (failed(__shfl_sync(0xffffffffu, ok, 0) != 0)) break;
@@ -312,12 +409,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             }
             for (uint64_t k = k0; k < k1; ++k, ++j) {
                 const uint32_t st = (uint32_t)(j % kKV);
-                // lane i < ppt: the step's page i, if any of its slots holds a live token
-                // (its ID read before the wait for the stage)
-                const uint64_t t0 = k * kTok + (uint64_t)lane * P;
-                const bool live = lane < ppt && t0 < len;
-                const unsigned long long phys = live ? (unsigned long long)table[tab0 + t0 / P] : 0ull;
-                const uint32_t npages = __popc(__ballot_sync(0xffffffffu, live));
+                // the lane's page (its ID read before the wait for the stage), if any of its
+                // slots holds a live token
+                const uint64_t t0 = k * TS + (uint64_t)li * P;
+                const bool live = active && t0 < len;
+                const unsigned long long phys = live ? table_at(a.table, u64, tab0 + k * PPS + li) : 0ull;
+                const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
                 int ok = 1;
                 if (lane == 0 && j >= kKV)
                     ok = mbar_wait(smem_u32(&freed[st]), (uint32_t)((j / kKV - 1) & 1));
@@ -326,13 +423,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     stop = true;
                     break;
                 }
-                if (lane == 0) mbar_expect_tx(smem_u32(&full[st]), npages * P * 256);
+                if (lane == 0) mbar_expect_tx(smem_u32(&full[st]), nlive * P * 256);
                 __syncwarp();
                 if (live) {
-                    const uint32_t dst = base + st * kTile + lane * P * 128;
+                    const uint32_t dst = base + st * kTile + (lh * TS + li * P) * 128;
                     const int row = (int)(phys * P);
-                    tma_3d(dst, map, 0, (int)g, row, smem_u32(&full[st]));
-                    tma_3d(dst + kHalf, map, 64, (int)g, row, smem_u32(&full[st]));
+                    tma_3d(dst, map, 0, (int)lh, row, smem_u32(&full[st]));
+                    tma_3d(dst + kHalf, map, 64, (int)lh, row, smem_u32(&full[st]));
                 }
             }
         }
@@ -346,12 +443,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
     } else if (warp == 1) {
         // --------------------------------------------------- S = K . Q^T (one thread issues)
-        const uint32_t id_s = mma_idesc(BF16, false);
+        const uint32_t id_s = mma_idesc(bf16, false, kNS);
+        // descriptors of K stage 0 and Q buffer 0; the others differ only in the start
+        // address field (addresses >> 4, below 2^14 for all of shared memory)
+        const uint64_t kd0 = sw128_desc(sm0, 16, 1024), qd0 = sw128_desc(sm0 + kOffQ, 16, 1024);
         uint64_t j = 0, seg = 0;
-        uint32_t g;
         uint64_t s, k0, k1;
         bool stop = false;
-        while (!stop && walk.next(g, s, k0, k1)) {
+        while (!stop && walk.next(s, k0, k1)) {
             for (uint64_t k = k0; k < k1; ++k, ++j) {
                 int ok = 1;
                 if (lane == 0) {
@@ -360,14 +459,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                          (j < 2 || mbar_wait(smem_u32(&s_free[j % 2]), (uint32_t)((j / 2 - 1) & 1)));
                     if (ok) {
                         fence_after();
-                        const uint32_t kst = sm0 + (uint32_t)(j % kKV) * kTile;
-                        const uint32_t qb = sm0 + kOffQ + (uint32_t)(seg % 2) * kQBuf;
-                        const uint32_t d = tmem + (uint32_t)(j % 2) * kN;
-                        for (uint32_t h = 0; h < 2; ++h)
-                            for (uint32_t kk = 0; kk < 4; ++kk)
-                                mma_f16(d, sw128_desc(kst + h * kHalf + kk * 32, 16, 1024),
-                                        sw128_desc(qb + h * 2048 + kk * 32, 16, 1024), id_s,
-                                        h | kk);
+                        const uint64_t kd = kd0 + (((uint32_t)(j % kKV) * kTile) >> 4);
+                        const uint64_t qd = qd0 + (((uint32_t)(seg % 2) * kQBuf) >> 4);
+                        const uint32_t d = tmem + (uint32_t)(j % 2) * kNS;
+                        // 8 products of 16 dims: 64-dim half h, 32-byte slice kk of its rows
+#pragma unroll
+                        for (uint32_t u = 0; u < 8; ++u) {
+                            const uint32_t h = u >> 2, kk = u & 3;
+                            mma_f16(d, kd + ((h * kHalf + kk * 32) >> 4),
+                                    qd + ((h * kNS * 128 + kk * 32) >> 4), id_s, u);
+                        }
                         mma_commit(smem_u32(&s_full[j % 2]));
                         mma_commit(smem_u32(&k_free[j % kKV]));  // K of this step is read
                         if (k + 1 == k1) mma_commit(smem_u32(&q_free[seg % 2]));  // and Q
@@ -375,6 +476,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (failed(ok != 0)) {
+                    j += ok != 0;  // issued before another role stopped: waited for below
                     stop = true;
                     break;
                 }
@@ -384,13 +486,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // every S issued has completed before the TMEM goes
         if (lane == 0 && j >= 1) mbar_wait(smem_u32(&s_full[(j - 1) % 2]), (uint32_t)(((j - 1) / 2) & 1));
     } else if (warp == 6) {
-        // ------------------------------------------- O^T = V^T . P^T (one thread issues)
-        const uint32_t id_o = mma_idesc(BF16, true);
+        // ------------------------------ O_h^T = V_h^T . P_h^T for every head (one thread issues)
+        const uint32_t id_o = mma_idesc(bf16, true, kNO);
+        // descriptors of V stage 0 and P buffer 0 (as for S: only the start address moves)
+        const uint64_t vd0 = sw128_desc(sm0 + kKV * kTile, kHalf, 1024);
+        const uint64_t pd0 = sw128_desc(sm0 + kOffP, 16, 1024);
         uint64_t j = 0;
-        uint32_t g;
         uint64_t s, k0, k1;
         bool stop = false;
-        while (!stop && walk.next(g, s, k0, k1)) {
+        while (!stop && walk.next(s, k0, k1)) {
             for (uint64_t k = k0; k < k1; ++k, ++j) {
                 int ok = 1;
                 if (lane == 0) {
@@ -399,15 +503,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                          (j < 2 || mbar_wait(smem_u32(&o_free[j % 2]), (uint32_t)((j / 2 - 1) & 1)));
                     if (ok) {
                         fence_after();
-                        const uint32_t vst = sm0 + kKV * kTile + (uint32_t)(j % kKV) * kTile;
-                        const uint32_t pb = sm0 + kOffP + (uint32_t)(j % 2) * 2 * kPBuf;
-                        const uint32_t d = tmem + 32 + (uint32_t)(j % 2) * kN;
-                        for (uint32_t kk = 0; kk < kTok / 16; ++kk) {
-                            const uint64_t ad = sw128_desc(vst + kk * 2048, kHalf, 1024);
-                            for (uint32_t part = 0; part < 2; ++part) {  // weights hi, then lo
-                                const uint32_t pa = pb + part * kPBuf + (kk >> 2) * 2048 + (kk & 3) * 32;
-                                mma_f16(d, ad, sw128_desc(pa, 16, 1024), id_o, kk | part);
-                            }
+                        const uint64_t vd = vd0 + (((uint32_t)(j % kKV) * kTile) >> 4);
+                        const uint64_t pd = pd0 + (((uint32_t)(j % 2) * 2 * kPBuf) >> 4);
+                        const uint32_t ob = tmem + kOCol + (uint32_t)(j % 2) * HKV * kNO;
+                        // 8 slices of 16 rows (V rows, P columns), each in its head's O: the
+                        // weights' hi part, then their lo part
+#pragma unroll
+                        for (uint32_t u = 0; u < 8; ++u) {
+                            const uint32_t row = u * 16, h = row >> sh.lts;
+                            const uint64_t ad = vd + ((row * 128) >> 4);
+                            const uint64_t bd = pd + (((row >> 6) * 2048 + (row & 63) * 2) >> 4);
+                            mma_f16(ob + h * kNO, ad, bd, id_o, (row & (TS - 1)) != 0);
+                            mma_f16(ob + h * kNO, ad, bd + (kPBuf >> 4), id_o, 1u);
                         }
                         mma_commit(smem_u32(&o_full[j % 2]));
                         mma_commit(smem_u32(&v_free[j % kKV]));  // V of this step is read
@@ -415,6 +522,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (failed(ok != 0)) {
+                    j += ok != 0;  // issued before another role stopped: waited for below
                     stop = true;
                     break;
                 }
@@ -424,94 +532,127 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (lane == 0 && j >= 1) mbar_wait(smem_u32(&o_full[(j - 1) % 2]), (uint32_t)(((j - 1) / 2) & 1));
     } else {
         // ------------------------------------------------------- softmax, accumulation
-        const uint32_t t = threadIdx.x - 64;          // 0..127
-        const uint32_t q4 = warp & 3;                  // this warp's TMEM lane quarter
-        const uint32_t my = q4 * 32 + lane;            // TMEM lane: token (S) or dim (O)
+        const uint32_t t = threadIdx.x - 64;        // 0..127
+        const uint32_t q4 = warp & 3;                // this warp's TMEM lane quarter
+        const uint32_t my = q4 * 32 + lane;          // TMEM lane: row (S, P) or dim (O)
+        const uint32_t rh = my >> sh.lts, rt = my & (TS - 1);  // the row's head and token
         const uint32_t lane_addr = (q4 * 32) << 16;
+        const uint32_t span = TS < 32 ? TS : 32;     // lanes of a warp holding one head's rows
+        const uint32_t hw = TS > 32 ? TS / 32 : 1;   // warps holding one head's rows
         const float qscale = a.scale * 1.4426950408889634f;  // scores in log2 units
-        uint64_t j = 0, seg = 0;
-        uint32_t g;
-        uint64_t s, k0, k1;
-        // a wait of every softmax thread, decided together; on a timeout the launch stops
-        auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-            const bool ok = named_and(2, kSoftmax, mbar_wait(bar, parity));
-            if (!ok && t == 0) {
+        // The softmax threads wait each on its own, and stop together: a wait that runs out
+        // marks fail_s[w % 2] for the window w it falls in -- window w runs from the step
+        // barrier of step w - 1 to that of step w -- and after the step barrier of step w
+        // every thread reads the same mark (nothing writes it until the next window).  A
+        // thread whose wait ran out carries on to that barrier with values it discards.
+        bool ok_w = true;  // this thread's waits since the last step barrier
+        auto wait_one = [&](uint32_t bar, uint32_t parity, uint64_t w) {
+            if (!mbar_wait(bar, parity)) {
+                fail_s[w % 2] = 1;
                 abort_flag = 1;
                 report(a.d_status, HP_ERR_TIMEOUT);
+                ok_w = false;
             }
-            return ok;
         };
-        bool stop = false;
-        float acc[G];
-        while (!stop && walk.next(g, s, k0, k1)) {
-            const uint64_t len = lensp[s];
-            float m[G], m_acc[G];  // running maxima: of the scores, and of acc
+        // x[g] over the rows of this thread's head: the warp's lanes of the head by shuffles,
+        // then (rows spanning warps) the head's warps through red_s
+        auto head_reduce = [&](float (&x)[G], bool is_max) {
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                m[h] = -INFINITY;
-                m_acc[h] = -INFINITY;
-                acc[h] = 0.0f;
+            for (int g = 0; g < G; ++g)
+                for (uint32_t o2 = 1; o2 < span; o2 <<= 1) {
+                    const float y = __shfl_xor_sync(0xffffffffu, x[g], o2);
+                    x[g] = is_max ? fmaxf(x[g], y) : x[g] + y;
+                }
+            if (hw > 1) {
+                if (lane == 0)
+#pragma unroll
+                    for (int g = 0; g < G; ++g) red_s[q4][g] = x[g];
+                named_sync(1, kSoftmax);
+                const uint32_t w0 = (rh * TS) >> 5;  // first TMEM quarter of the head
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float r = red_s[w0][g];
+                    for (uint32_t w2 = 1; w2 < hw; ++w2)
+                        r = is_max ? fmaxf(r, red_s[w0 + w2][g]) : r + red_s[w0 + w2][g];
+                    x[g] = r;
+                }
+                named_sync(1, kSoftmax);  // red_s is rewritten next time
             }
-            float lp[G];  // this thread's share of each head's weight sum
+        };
+        float acc[kAcc];
+        // folds O of step jj into acc, each query head rescaled by its factor of step jj
+        // (every factor is 1 when no maximum rose in that step)
+        auto fold = [&](uint64_t jj, bool rescale, uint64_t w) {
+            wait_one(smem_u32(&o_full[jj % 2]), (uint32_t)((jj / 2) & 1), w);
+            fence_after();
+            const uint32_t ob = tmem + lane_addr + kOCol + (uint32_t)(jj % 2) * HKV * kNO;
+            uint32_t o[kAcc];  // every head's G columns, loaded together, one wait
 #pragma unroll
-            for (int h = 0; h < G; ++h) lp[h] = 0.0f;
-            // folds O of step jj (weights relative to mj) into acc
-            auto fold = [&](uint64_t jj, const float (&mj)[G]) -> bool {
-                if (!wait_all(smem_u32(&o_full[jj % 2]), (uint32_t)((jj / 2) & 1))) return false;
-                fence_after();
-                float o[16];
-                tmem_ld16(tmem + lane_addr + 32 + (uint32_t)(jj % 2) * kN, o);
-                fence_before();
-                mbar_arrive(smem_u32(&o_free[jj % 2]));
+            for (int i = 0; i < kAcc; ++i) o[i] = 0u;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float c = exp2_approx(m_acc[h] - mj[h]);  // 0 while acc is empty
-                    acc[h] = acc[h] * c + o[h];
-                    m_acc[h] = mj[h];
-                }
-                return true;
-            };
-            float m_prev[G];
+            for (int hh = 0; hh < kHeads; ++hh)
+                if ((uint32_t)hh < HKV) tmem_issue<G>(ob + hh * kNO, o + hh * G);
+            tmem_wait<kAcc>(o);
+#pragma unroll
+            for (int i = 0; i < kAcc; ++i) {
+                const float c = rescale ? corr_s[jj % 2][i] : 1.0f;  // (i < Hq when it counts)
+                acc[i] = acc[i] * c + __uint_as_float(o[i]);
+            }
+            fence_before();
+            mbar_arrive(smem_u32(&o_free[jj % 2]));
+        };
+        uint64_t j = 0;
+        uint64_t s, k0, k1;
+        bool stop = false;
+        while (!stop && walk.next(s, k0, k1)) {
+            const uint64_t len = table_at(a.lens, u64, s);
+            float m_run[G], lp[G];  // this row's head: running maxima, this row's weight sums
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                m_run[g] = -INFINITY;
+                lp[g] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < kAcc; ++i) acc[i] = 0.0f;
+            bool up_prev = false;
             for (uint64_t k = k0; k < k1; ++k, ++j) {
-                if (!wait_all(smem_u32(&s_full[j % 2]), (uint32_t)((j / 2) & 1))) {
-                    stop = true;
-                    break;
-                }
+                wait_one(smem_u32(&s_full[j % 2]), (uint32_t)((j / 2) & 1), j);
                 fence_after();
-                float sc[16];
-                tmem_ld16(tmem + lane_addr + (uint32_t)(j % 2) * kN, sc);
+                // the G score columns of this row's head: a warp holds the rows of one head,
+                // or (16-token steps) of two, whose 2G columns it loads together
+                float x[G], mx[G];
+                const uint32_t sbase = tmem + lane_addr + (uint32_t)(j % 2) * kNS;
+                if (TS == 16) {
+                    float sc[2 * G];
+                    tmem_ld<2 * G>(sbase + q4 * 2 * G, sc);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) x[g] = lane < 16 ? sc[g] : sc[G + g];
+                } else {
+                    tmem_ld<G>(sbase + rh * G, x);
+                }
                 fence_before();
                 mbar_arrive(smem_u32(&s_free[j % 2]));
-                const uint64_t tok = k * kTok + my;
-                const bool valid = tok < len;
-                float mx[G];
+                const bool valid = k * TS + rt < len;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    sc[h] = valid ? sc[h] * qscale : -INFINITY;
-                    float x = sc[h];
-#pragma unroll
-                    for (int o2 = 16; o2 >= 1; o2 >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o2));
-                    mx[h] = x;
+                for (int g = 0; g < G; ++g) {
+                    x[g] = valid ? x[g] * qscale : -INFINITY;
+                    mx[g] = x[g];
                 }
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-                    if (lane == (unsigned)h) red[q4][h] = mx[h];  // every lane holds the maxima
-                named_sync(1, kSoftmax);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    m_prev[h] = m[h];
-                    m[h] = fmaxf(m[h], fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h])));
-                }
-                named_sync(1, kSoftmax);  // red is rewritten next step
-                // weights relative to the new maxima, as hi + lo pairs of 16-bit values
+                head_reduce(mx, true);  // the step's maximum of each query head of rh
+                bool up = false;
                 unsigned char* pb = smem + kOffP + (uint32_t)(j % 2) * 2 * kPBuf;
                 const uint32_t pcol = my & 63, patom = (my >> 6) * 2048;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float p = exp2_approx(sc[h] - m[h]);  // 0 past the sequence
-                    lp[h] = lp[h] * exp2_approx(m_prev[h] - m[h]) + p;
+                for (int g = 0; g < G; ++g) {
+                    const float mn = fmaxf(m_run[g], mx[g]);
+                    up |= mn > m_run[g];
+                    const float c = exp2_approx(m_run[g] - mn);  // 0 while nothing is summed
+                    const float p = exp2_approx(x[g] - mn);      // 0 past the sequence
+                    lp[g] = lp[g] * c + p;
+                    if (rt == 0) corr_s[j % 2][rh * G + g] = c;
+                    m_run[g] = mn;
                     unsigned short hi, lo;
-                    if (BF16) {
+                    if (bf16) {
                         const __nv_bfloat16 bh = __float2bfloat16_rn(p);
                         hi = __bfloat16_as_ushort(bh);
                         lo = __bfloat16_as_ushort(__float2bfloat16_rn(p - __bfloat162float(bh)));
@@ -520,84 +661,84 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         hi = __half_as_ushort(hh);
                         lo = __half_as_ushort(__float2half_rn(p - __half2float(hh)));
                     }
-                    const uint32_t off = patom + sw128_off((uint32_t)h, pcol);
+                    const uint32_t off = patom + sw128_off((uint32_t)g, pcol);
                     *reinterpret_cast<unsigned short*>(pb + off) = hi;
                     *reinterpret_cast<unsigned short*>(pb + kPBuf + off) = lo;
                 }
                 // rows of V past the sequence become zeros (their weights are zero, and a
                 // stale or undefined value must not reach the product)
-                if ((k + 1) * kTok > len) {  // the same in every softmax thread
-                    if (!wait_all(smem_u32(&v_full[j % kKV]), (uint32_t)((j / kKV) & 1))) {
-                        stop = true;
-                        break;
-                    }
-                    // rows r0 .. 127 of both halves, 16-byte pieces spread over the threads
-                    // (consecutive threads, consecutive pieces of a row)
-                    const uint32_t r0 = (uint32_t)(len - k * kTok);
-                    unsigned char* vst = smem + (kKV + (uint32_t)(j % kKV)) * kTile;
-                    for (uint32_t x = t; x < (kTok - r0) * 16; x += kSoftmax) {
-                        const uint32_t row = r0 + (x >> 4), piece = x & 15;
-                        *reinterpret_cast<uint4*>(vst + (piece >> 3) * kHalf + row * 128 +
-                                                  (piece & 7) * 16) = make_uint4(0, 0, 0, 0);
+                if ((k + 1) * TS > len) {  // the same in every softmax thread
+                    wait_one(smem_u32(&v_full[j % kKV]), (uint32_t)((j / kKV) & 1), j);
+                    if (!valid) {
+                        unsigned char* vrow = smem + (kKV + (uint32_t)(j % kKV)) * kTile + my * 128;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            *reinterpret_cast<uint4*>(vrow + i * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(vrow + kHalf + i * 16) = make_uint4(0, 0, 0, 0);
+                        }
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(smem_u32(&p_full[j % 2]));
-                // the previous step's O, now that this step's weights are handed over
-                if (k > k0 && !fold(j - 1, m_prev)) {
+                // the step barrier: whether any maximum rose (and the step's factors, now
+                // visible to all), and whether any wait of this window ran out
+                up = named_or(3, kSoftmax, up);
+                ok_w = true;
+                if (*(volatile int*)&fail_s[j % 2]) {
                     stop = true;
                     break;
                 }
+                // the previous step's O, now that this step's weights are handed over
+                if (k > k0) fold(j - 1, up_prev, j + 1);
+                up_prev = up;
             }
-            if (stop || !fold(j - 1, m)) break;
-            // each head's weight sum over the 128 threads
-            float l[G];
+            if (stop) break;
+            fold(j - 1, up_prev, j);
+            if (!named_and(2, kSoftmax, ok_w)) break;  // the segment's last waits
+            // each query head's weight sum over its rows, and its maximum, per head leader
+            head_reduce(lp, false);
+            if (rt == 0)
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float x = lp[h];
-#pragma unroll
-                for (int o2 = 16; o2 >= 1; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2);
-                if (lane == 0) red[q4][h] = x;
-            }
-            named_sync(1, kSoftmax);
-#pragma unroll
-            for (int h = 0; h < G; ++h) l[h] = red[0][h] + red[1][h] + red[2][h] + red[3][h];
+                for (int g = 0; g < G; ++g) {
+                    ml_s[0][rh * G + g] = m_run[g];
+                    ml_s[1][rh * G + g] = lp[g];
+                }
             named_sync(1, kSoftmax);
             const uint64_t so = a.units_off[s], ns = a.units_off[s + 1] - so;
             const uint64_t f = so / Lw, nr = (so + ns - 1) / Lw - f + 1;
-            float* out = a.out + (s * a.Hq + (uint64_t)g * G) * kD + my;
-            if (nr == 1) {  // the whole sequence: its normalised result
+            if (nr == 1) {  // the whole sequence: its normalised result, thread = dim
+                float* out = a.out + s * a.Hq * kD + my;
 #pragma unroll
-                for (int h = 0; h < G; ++h) out[h * kD] = acc[h] / l[h];
+                for (int i = 0; i < kAcc; ++i)
+                    if ((uint32_t)i < a.Hq) out[(uint64_t)i * kD] = acc[i] / ml_s[1][i];
             } else {
-                const uint64_t row0 = ((s + v) * a.Hkv + g) * G;
+                const uint64_t row0 = (s + v) * a.Hq;  // record rows of all query heads
 #pragma unroll
-                for (int h = 0; h < G; ++h) a.part_acc[(row0 + h) * kD + my] = acc[h];
-                if (t == 0) {
-#pragma unroll
-                    for (int h = 0; h < G; ++h)
-                        reinterpret_cast<float2*>(a.part_ml)[row0 + h] = make_float2(m[h], l[h]);
-                }
+                for (int i = 0; i < kAcc; ++i)
+                    if ((uint32_t)i < a.Hq) a.part_acc[(row0 + i) * kD + my] = acc[i];
+                if (t < a.Hq)
+                    reinterpret_cast<float2*>(a.part_ml)[row0 + t] = make_float2(ml_s[0][t], ml_s[1][t]);
                 __threadfence();  // the record is visible before the count moves
                 named_sync(1, kSoftmax);
                 if (t == 0) {
-                    const unsigned done = atomicAdd(a.seg_done + s * a.Hkv + g, 1u);
+                    const unsigned done = atomicAdd(a.seg_done + s * a.Hkv, 1u);
                     merge_done = done + 1 == nr;
                 }
                 named_sync(1, kSoftmax);
-                if (merge_done && t < 32) {  // the last segment: merge them all (one warp)
+                if (merge_done) {  // the last segment: merge every head's records, a warp each
                     __threadfence();
-                    merge_segments<G, kD / 32>(a, ((s + f) * a.Hkv + g) * G, nr,
-                                               a.out + (s * a.Hq + (uint64_t)g * G) * kD + lane * (kD / 32),
-                                               lane);
-                    if (lane == 0) a.seg_done[s * a.Hkv + g] = 0u;
+                    for (uint32_t hh = t >> 5; hh < HKV; hh += 4)
+                        merge_segments<G, kD / 32>(a, ((s + f) * a.Hkv + hh) * G, nr,
+                                                   a.out + (s * a.Hq + (uint64_t)hh * G) * kD +
+                                                       lane * (kD / 32),
+                                                   lane);
+                    if (t == 0) a.seg_done[s * a.Hkv] = 0u;
                 }
-                named_sync(1, kSoftmax);  // merge_done is rewritten by the next segment
             }
-            ++seg;
+            named_sync(1, kSoftmax);  // ml_s and merge_done are rewritten by the next segment
         }
     }
-    // every role is done; the TMEM goes back (the MMA warp waited for its operations)
+    // every role is done; the TMEM goes back (the issuers waited for their operations)
     fence_before();
     __syncthreads();
     fence_after();
@@ -607,7 +748,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                      : "memory");
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point, looked up once.
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -643,15 +783,15 @@ bool pool_map(CUtensorMap* m, const void* pool, const AttnArgs& a, bool bf16)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The queries [num_seqs * Hq rows, 128] as a 2-d tensor: boxes of 64 dims x G rows (the
-// query heads of one K/V head), 128-byte swizzled.
+// The queries [num_seqs * Hq rows, 128] as a 2-d tensor: boxes of 64 dims x Hq rows (the
+// query heads of one sequence), 128-byte swizzled.
 bool query_map(CUtensorMap* m, const AttnArgs& a, bool bf16)
 {
     EncodeFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {kD, a.num_seqs * a.Hq};
     const cuuint64_t strides[1] = {kD * 2};
-    const cuuint32_t box[2] = {64, a.G};
+    const cuuint32_t box[2] = {64, a.Hq};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
               const_cast<void*>(a.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -659,35 +799,31 @@ bool query_map(CUtensorMap* m, const AttnArgs& a, bool bf16)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename IndexT, bool BF16, int G>
-int launch_g(const AttnArgs& a, cudaStream_t st)
+
+template <int G>
+int launch_g(const AttnArgs& a, const TcShape& sh, cudaStream_t st)
 {
     CUtensorMap mk, mv, mq;
-    if (!pool_map(&mk, a.k_pool, a, BF16) || !pool_map(&mv, a.v_pool, a, BF16) ||
-        !query_map(&mq, a, BF16))
+    const bool bf16 = sh.bf16 != 0;
+    if (!pool_map(&mk, a.k_pool, a, bf16) || !pool_map(&mv, a.v_pool, a, bf16) ||
+        !query_map(&mq, a, bf16))
         return HP_ERR_CUDA;
     int dev = 0;
     const int sms = current_sms(&dev);
-    if (sms == 0 || !allow_dynamic_smem<attn_tc_kernel<IndexT, BF16, G>>(dev, (int)kSmemTc))
-        return HP_ERR_CUDA;
+    if (sms == 0 || !allow_dynamic_smem<attn_tc_kernel<G>>(dev, (int)kSmemTc)) return HP_ERR_CUDA;
     AttnArgs b = a;
     b.workers = (uint64_t)sms;
-    return launch_dependent(attn_tc_kernel<IndexT, BF16, G>, (unsigned)sms, kThreadsTc,
-                            (size_t)kSmemTc, st, b, mk, mv, mq) == cudaSuccess
+    return launch_dependent(attn_tc_kernel<G>, (unsigned)sms, kThreadsTc, (size_t)kSmemTc, st, b,
+                            sh, mk, mv, mq) == cudaSuccess
                ? HP_OK
                : HP_ERR_CUDA;
 }
 
-template <typename IndexT, bool BF16>
-int launch_b(const AttnArgs& a, cudaStream_t st)
+uint32_t log2_exact(uint32_t x)
 {
-    switch (a.G) {
-    case 1: return launch_g<IndexT, BF16, 1>(a, st);
-    case 2: return launch_g<IndexT, BF16, 2>(a, st);
-    case 4: return launch_g<IndexT, BF16, 4>(a, st);
-    case 8: return launch_g<IndexT, BF16, 8>(a, st);
-    default: return HP_ERR_ARG;
-    }
+    uint32_t l = 0;
+    while ((1u << l) < x) ++l;
+    return l;
 }
 
 }  // namespace
@@ -696,24 +832,40 @@ int launch_b(const AttnArgs& a, cudaStream_t st)
 #define HP_ATTN_TC 1
 #endif
 
-bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory)
+bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory,
+                       uint64_t num_kv_heads, uint64_t num_q_heads)
 {
-    return HP_ATTN_TC && !host_memory && head_dim == kD &&
-           (page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 ||
-            page_size == 128) &&
+    const uint64_t hkv = num_kv_heads;
+    if (!HP_ATTN_TC || host_memory || head_dim != kD) return false;
+    if (hkv != 1 && hkv != 2 && hkv != 4 && hkv != 8) return false;
+    if (num_q_heads > (uint64_t)kNS || num_q_heads % hkv != 0) return false;
+    const uint64_t g = num_q_heads / hkv;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return false;
+    // a step's pages tile its TS = 128 / H_kv tokens exactly
+    const uint64_t ts = kRows / hkv;
+    return page_size >= 8 && page_size <= ts && (page_size & (page_size - 1)) == 0 &&
            num_pages * page_size < (1ull << 31);
 }
 
-
-uint64_t attention_tc_step_tokens() { return kTok; }
+uint64_t attention_tc_step_tokens(uint64_t num_kv_heads) { return kRows / num_kv_heads; }
 
 int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (index_u64)
-        return a.elem_bf16 ? launch_b<unsigned long long, true>(a, st)
-                           : launch_b<unsigned long long, false>(a, st);
-    return a.elem_bf16 ? launch_b<unsigned int, true>(a, st) : launch_b<unsigned int, false>(a, st);
+    TcShape sh;
+    sh.hkv = a.Hkv;
+    sh.ts = kRows / a.Hkv;
+    sh.lts = log2_exact(sh.ts);
+    sh.pps = sh.ts / (uint32_t)a.page_size;
+    sh.idx64 = index_u64 != 0;
+    sh.bf16 = a.elem_bf16 != 0;
+    switch (a.G) {
+    case 1: return launch_g<1>(a, sh, st);
+    case 2: return launch_g<2>(a, sh, st);
+    case 4: return launch_g<4>(a, sh, st);
+    case 8: return launch_g<8>(a, sh, st);
+    default: return HP_ERR_ARG;
+    }
 }
 
 }  // namespace hp

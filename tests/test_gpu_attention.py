@@ -22,8 +22,8 @@ KF = 0  # the kernel the current test asks for (HP_ATTN_TENSOR_CORES or HP_ATTN_
 @pytest.fixture(autouse=True, params=["tensor_cores", "cuda_cores"])
 def attn_kernel(request, hp):
     """Every test here runs once on each kernel: the tensor-core kernel (where the shape
-    allows it: head_dim 128, pages of 8-128 slots; the others fall back to the CUDA cores)
-    and the CUDA-core kernel."""
+    allows it: head_dim 128, 1, 2, 4 or 8 K/V heads, at most 32 query heads, pages of 8 to
+    128 / H_kv slots; the others fall back to the CUDA cores) and the CUDA-core kernel."""
     global KF
     KF = hp.ATTN_TENSOR_CORES if request.param == "tensor_cores" else hp.ATTN_CUDA_CORES
     yield request.param
@@ -69,8 +69,10 @@ def _check(got, want, vmax):
     ("bf16", 4, 2, 256, 5, None), ("f16", 3, 8, 128, 3, None), ("bf16", 12, 1, 128, 32, None),
     ("bf16", 2, 8, 256, 16, None), ("f16", 2, 8, 64, 16, None), ("f16", 1, 4, 64, 1, None),
     ("bf16", 8, 4, 128, 16, 1.5),  # peaked softmax: a few tokens carry the weight
-    # the tensor-core kernel's other page sizes (steps of 16, 4, 2 and 1 pages)
-    ("bf16", 2, 8, 128, 8, None), ("f16", 4, 2, 128, 64, None), ("bf16", 1, 1, 128, 128, None),
+    # the tensor-core kernel's other shapes: its steps are 128 / H_kv tokens of every K/V
+    # head, so these have 8, 1, 1, 2 and 1 pages per step and 1, 2, 4 or 8 heads
+    ("bf16", 2, 8, 128, 8, None), ("f16", 2, 2, 128, 64, None), ("bf16", 1, 1, 128, 128, None),
+    ("bf16", 4, 8, 128, 8, None), ("f16", 4, 2, 128, 32, None), ("bf16", 1, 8, 128, 16, None),
 ])
 def test_attention_matches_oracle(hp, oracle, dtype, Hkv, G, D, P, scale):
     # lengths up to ~1300 tokens: small pages move the 32-page window many times
