@@ -752,6 +752,9 @@ def lane_only(dev, hp, inputs, peak, reps):
     ms_t = median_ms(lambda: torch.index_select(rows, 0, idx, out=dst), stream, reps)
     res["torch_index_select_same_runs"] = rate_entry(2 * dst.numel() * 2 + idx.numel() * 8,
                                                      ms_t, peak)
+    # one contiguous copy of the snapshot's bytes: the ceiling of a launch this size
+    cg = d2d_copy_gbps(lw.lanes * lw.n * lw.width * 2, dev, stream)
+    res["d2d_copy_same_bytes"] = {"gbps": round(cg, 1), "frac": round(cg / peak, 4)}
     return res
 
 
