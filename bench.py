@@ -1005,17 +1005,14 @@ def config_entry(dev, hp, inputs, w, peak, med_ms, oracle_mod, cold=None, e2e=Fa
         e["frac_unique"] = round(ub / (ms * 1e-3) / 1e9 / peak, 4)
         if traffic is not None:
             e["traffic_over_unique"] = round(traffic / ub, 4)
-        # the same rows through a generic gather (torch index_select over the pool's rows)
-        # and the output's bytes written alone (fill_): what this traffic pattern reaches
-        # without this kernel, for reading frac_unique
+        # the same rows through a generic gather (torch index_select over the pool's rows),
+        # for reading frac_unique
         rows = st.pool.view(w.num_pages * w.page_size, -1)
         it = torch.from_numpy(physical_rows(w)).to(dev)
         dst = torch.empty((it.numel(), rows.shape[1]), dtype=rows.dtype, device=dev)
         ms_i = med_ms(lambda: torch.index_select(rows, 0, it, out=dst), n=10)
         e["torch_index_select_same_rows"] = {
             "ms": round(ms_i, 4), "frac_unique": round(ub / (ms_i * 1e-3) / 1e9 / peak, 4)}
-        ms_f = med_ms(lambda: dst.fill_(0), n=10)
-        e["write_only_output_bytes"] = rate_entry(dst.numel() * dst.element_size(), ms_f, peak)
         del dst, it
         if cold is not None:
             ms_c = med_ms(lambda: st.copy(stream), n=10, between=cold)
