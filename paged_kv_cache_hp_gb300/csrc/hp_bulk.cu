@@ -14,15 +14,20 @@
 //   8 KiB x 24 stages (units of 64 KiB and more): one producer thread issues both the
 //               loads and the stores, keeping up to 23 loads in flight and reusing a
 //               stage once all but the newest store have read shared memory;
-//   32 KiB x 6 stages (units of 16-64 KiB): a loader thread (warp 0) and a storer
+//   16 KiB x 12 stages (units of 16-64 KiB): a loader thread (warp 0) and a storer
 //               thread (warp 1).  The loader waits for a free stage, records the chunk's
 //               destination and size with it and issues the load; the storer waits for
 //               each stage in turn to be loaded, issues its store, and hands a stage back
-//               through its "free" mbarrier once all but the newest kStoresInFlight
-//               stores have read shared memory.  After the last chunk the loader hands
-//               the storer a zero-byte chunk to end on.
+//               through its "free" mbarrier once all but the newest kStoresInFlight = 8
+//               stores have read shared memory, so up to 8 stores and 4 loads are in
+//               flight.  After the last chunk the loader hands the storer a zero-byte
+//               chunk to end on.
 // (Split roles lose on 8 KiB chunks -- the storer's per-chunk wait caps the stores in
-// flight -- and a single thread loses on 32 KiB chunks.)  Every wait is bounded (about
+// flight -- and a single thread loses on 16-32 KiB chunks.  On the 16-64 KiB units, 16 KiB
+// x 12 with 8 stores in flight beat 32 KiB x 6 with 3 (0.97 -> 0.995 of the copy
+// bandwidth on 2 KiB rows, and a little better with shared prefix pages); 32 KiB x 6 with
+// 4 stores reached 1.01 on the first and lost 3% on the second; 7, 9 or 10 stores of
+// 16 KiB, or 5 of 32 KiB, were slower on one or both.)  Every wait is bounded (about
 // 2 s of %globaltimer); a wait that runs out stores HP_ERR_TIMEOUT in *d_status, stops
 // issuing and lets the loads in flight land (again bounded) before the CTA's shared
 // memory goes.
@@ -53,12 +58,12 @@ struct Desc {
 };
 
 // The ring holds kStages stages of kStage bytes (192 KiB either way): 8 KiB stages
-// suit copy units of 64 KiB and more, 32 KiB stages units of 16-64 KiB (measured).
+// suit copy units of 64 KiB and more, 16 KiB stages units of 16-64 KiB (measured).
 // STALL: the HP_TEST_STALL variant (a separate instantiation, so the copy path carries
 // no test check in its per-chunk loop).
 template <uint32_t kStage> __host__ __device__ constexpr int threads_for()
 {
-    return kStage >= 32768 ? 160 : 128;
+    return kStage >= 16384 ? 160 : 128;
 }
 
 template <int MODE, typename IndexT, uint32_t kStage, int kStages, bool STALL = false>
@@ -71,13 +76,13 @@ __global__ void __launch_bounds__(threads_for<kStage>(), 1) bulk_kernel(const Co
     __shared__ unsigned long long chunk_dst[kStages];
     __shared__ uint32_t chunk_bytes[kStages];
 
-    // split roles (loader and storer threads) for 32 KiB stages, one producer for 8 KiB
-    constexpr bool kSplit = kStage >= 32768;
+    // split roles (loader and storer threads) for 16 KiB stages, one producer for 8 KiB
+    constexpr bool kSplit = kStage >= 16384;
     constexpr int kFirstResolver = kSplit ? 64 : 32;
     static_assert(threads_for<kStage>() - kFirstResolver == kResolvers, "96 resolvers");
     // split roles: stores left reading shared memory before their stages are handed back;
     // fewer than kStages, so the loader always has a stage it can wait for without a cycle
-    constexpr int kStoresInFlight = 3;
+    constexpr int kStoresInFlight = 8;
     static_assert(kStoresInFlight < kStages, "a free stage must not wait on a later load");
     uint64_t total;
     if (MODE == kGather || MODE == kAppend) {
@@ -344,10 +349,10 @@ int launch_ring(const CopyArgs& a, int big_stages, cudaStream_t st)
 {
     if constexpr (MODE == kGather) {
         if (a.test_stall)
-            return big_stages ? launch_t<MODE, IndexT, 32768, 6, true>(a, st)
+            return big_stages ? launch_t<MODE, IndexT, 16384, 12, true>(a, st)
                               : launch_t<MODE, IndexT, 8192, 24, true>(a, st);
     }
-    return big_stages ? launch_t<MODE, IndexT, 32768, 6>(a, st)
+    return big_stages ? launch_t<MODE, IndexT, 16384, 12>(a, st)
                       : launch_t<MODE, IndexT, 8192, 24>(a, st);
 }
 

@@ -402,7 +402,7 @@ int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* 
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Engine by copy-unit size (measured on GB300): the TMA ring with 8 KiB stages for
-    // units of 64 KiB and more, with 32 KiB stages for 16-64 KiB, registers below.
+    // units of 64 KiB and more, with 16 KiB stages for 16-64 KiB, registers below.
 #ifndef HP_BULK_MIN_UNIT
 #define HP_BULK_MIN_UNIT 16384
 #endif

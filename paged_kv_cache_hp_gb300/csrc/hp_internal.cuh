@@ -190,7 +190,7 @@ int launch_copy(CopyMode mode, int index_u64, const CopyArgs& a, int vec, void* 
 int launch_append_rows(int index_u64, const CopyArgs& a, int vec, void* stream);
 
 // The TMA bulk engine (hp_bulk.cu): pure copies whose rows and bases are 16-byte aligned.
-// big_stages selects 32 KiB ring stages (else 8 KiB).
+// big_stages selects 16 KiB ring stages with split roles (else 8 KiB, one producer).
 int launch_bulk(CopyMode mode, int index_u64, const CopyArgs& a, int big_stages, void* stream);
 
 // ------------------------------------------------------- per-device launch facts

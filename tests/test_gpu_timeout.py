@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("heads", [32, 8])
 def test_stalled_bulk_gather_times_out_and_the_context_survives(hp, oracle, heads):
     """32 heads: rows of 8 KiB, 128 KiB copy units (the one-thread producer with 8 KiB
-    stages); 8 heads: rows of 2 KiB, 32 KiB units (loader and storer threads with 32 KiB
+    stages); 8 heads: rows of 2 KiB, 32 KiB units (loader and storer threads with 16 KiB
     stages).  Both batches are too large for the one-launch path."""
     import torch
     w = inputs.decode_gather(seed=12, num_pages=1200, num_heads=heads, head_dim=128,
