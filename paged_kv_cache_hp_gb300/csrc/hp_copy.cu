@@ -193,7 +193,11 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
     constexpr int kU = kScheme == kQDim ? kDqUnrollDim : kDqUnroll;
     const uint2* s = reinterpret_cast<const uint2*>(src);
     uint4* d = reinterpret_cast<uint4*>(dst);
+    // per slot: when a row's groups divide the CTA width, the row of group v0 + k * kThreads
+    // is the row of v0 plus k * (kThreads / groups per row), one division per pass
+    const uint32_t rstep = kScheme == kQSlot && kThreads % a.q_gpr == 0 ? kThreads / a.q_gpr : 0;
     for (uint32_t v0 = threadIdx.x; v0 < n8; v0 += kThreads * kU) {
+        const uint32_t r0 = rstep ? div_invariant(v0, a.div_m, a.div_l) : 0;
         uint2 q[kU];
 #pragma unroll
         for (int k = 0; k < kU; ++k) {
@@ -204,11 +208,12 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
         for (int k = 0; k < kU; ++k) {
             const uint32_t v = v0 + k * kThreads;
             if (v >= n8) continue;
-            float sc[8], zc[8], f[8];
+            float sc[8], zc[8];
             if (kScheme == kQSlot || kScheme == kQTensor) {
                 float s1 = s_t, z1 = z_t;
                 if (kScheme == kQSlot) {
-                    const uint64_t i = slot0 + div_invariant(v, a.div_m, a.div_l);
+                    const uint64_t i =
+                        slot0 + (rstep ? r0 + k * rstep : div_invariant(v, a.div_m, a.div_l));
                     s1 = __ldg(scales + i);
                     if (kZp) z1 = code_to_f32(__ldg(zps + i), sgn);
                 }
@@ -244,12 +249,11 @@ __device__ __forceinline__ void dequant_run8(const CopyArgs& a, const char* __re
                     if (kZp) codes_to_f32(__ldg(reinterpret_cast<const uint2*>(zps + d0)), sgn, zc);
                 }
             }
-            codes_to_f32(q[k], sgn, f);
-            if (kZp) {
+            if (!kZp) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] -= zc[e];  // exact: |q - zp| <= 255
+                for (int e = 0; e < 8; ++e) zc[e] = 0.0f;
             }
-            st_stream(d + v, round8(f, sc));
+            st_stream(d + v, dequant8(q[k], sgn, zc, sc));
         }
     }
 }
@@ -353,7 +357,12 @@ int launch_t(const CopyArgs& a, cudaStream_t st)
     const int per_sm =
         sms ? resident_ctas<copy_kernel<MODE, IndexT, VEC, WARP_UNITS, Q>>(dev, kThreads, 0) : 0;
     if (sms == 0 || per_sm == 0) return HP_ERR_CUDA;
-    uint64_t grid = (uint64_t)sms * (uint64_t)per_sm;
+    // dequantising gathers: at most 3 CTAs per SM except per head_dim, whose scales and zero
+    // points are read per group (measured on GB300: per slot 0.891 -> 0.945 of the copy
+    // bandwidth with 3 instead of 4, per head 0.896 -> 0.935, per slot affine 0.886 -> 0.929,
+    // per tensor unchanged; per head_dim 0.901 with 4, 0.827 with 3)
+    const bool cap3 = MODE == kDequant && (Q >> 1) != kQDim;
+    uint64_t grid = (uint64_t)sms * (uint64_t)(cap3 ? std::min(per_sm, 3) : per_sm);
     if (host_counted(MODE)) grid = std::min<uint64_t>(grid, a.lane_units);
     if (grid == 0) return HP_OK;
     if (host_counted(MODE)) {
