@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __shared__ float corr_s[2][kNS];  // per step parity: each query head's rescale factor
     __shared__ float red_s[4][8];     // per-warp maxima or sums when a head's rows span warps
     __shared__ float ml_s[2][kNS];    // a segment's maxima and weight sums per query head
+    __shared__ float inv_s[kNS];      // and the reciprocals of those sums
     __shared__ unsigned merge_done;
     __shared__ int fail_s[2];         // softmax waits that ran out, by step parity
 
@@ -702,6 +703,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 for (int g = 0; g < G; ++g) {
                     ml_s[0][rh * G + g] = m_run[g];
                     ml_s[1][rh * G + g] = lp[g];
+                    inv_s[rh * G + g] = 1.0f / lp[g];  // one division per query head
                 }
             named_sync(1, kSoftmax);
             const uint64_t so = a.units_off[s], ns = a.units_off[s + 1] - so;
@@ -710,7 +712,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 float* out = a.out + s * a.Hq * kD + my;
 #pragma unroll
                 for (int i = 0; i < kAcc; ++i)
-                    if ((uint32_t)i < a.Hq) out[(uint64_t)i * kD] = acc[i] / ml_s[1][i];
+                    if ((uint32_t)i < a.Hq) out[(uint64_t)i * kD] = acc[i] * inv_s[i];
             } else {
                 const uint64_t row0 = (s + v) * a.Hq;  // record rows of all query heads
 #pragma unroll
