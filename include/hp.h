@@ -159,8 +159,10 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * up the first load of each of its CTAs but never issues it, so the wait for it runs out
  * (after about 2 s), the call stores HP_ERR_TIMEOUT in *d_status and returns without
  * copying the rest.  Only a gather that takes the TMA engine (16-byte rows and bases,
- * copy units of 16 KiB or more, a batch too large for the one-launch path) sees it;
- * never set it outside tests. */
+ * copy units of 16 KiB or more, a batch too large for the one-launch path) sees it, and
+ * decode attention on the tensor cores, whose K loaders arm their first step's loads
+ * without issuing them (every role's waits then run out, the call stores HP_ERR_TIMEOUT
+ * and the output is undefined); never set it outside tests. */
 #define HP_TEST_STALL 0x100u
 
 /*

@@ -789,6 +789,7 @@ HP_API int hp_attention_decode_planned(const hp_paged_desc* k_desc, const void* 
     a.seg_done = p.seg_done;
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
+    a.test_stall = (d->flags & HP_TEST_STALL) != 0;
     a.d_status = d_status;
     if (attn_on_tensor_cores(d, p.G)) return hp::launch_attention_tc(d->index_type == HP_IDX_U64, a, stream);
     return hp::launch_attention(d->index_type == HP_IDX_U64, a, stream);

@@ -30,6 +30,8 @@ struct AttnArgs {
                               // again when the launch ends
     float* out;               // [num_seqs, Hq, D] fp32
     int elem_bf16;            // element type: bf16 (1) or f16 (0)
+    int test_stall;           // HP_TEST_STALL: the tensor-core kernel never issues its
+                              // first K load
     int* d_status;
 };
 int launch_attention(int index_u64, const AttnArgs& a, void* stream);

@@ -291,6 +291,7 @@ struct TcShape {
     uint32_t pps;   // pages per step: ts / page_size
     uint32_t idx64; // index type: uint64 (1) or uint32 (0)
     uint32_t bf16;  // element type: bf16 (1) or f16 (0)
+    uint32_t stall; // HP_TEST_STALL: the K loader arms its first step but never issues it
 };
 
 template <int G>
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 if (lane == 0) mbar_expect_tx(smem_u32(&full[st]), nlive * P * 256);
                 __syncwarp();
-                if (live) {
+                if (live && !(is_k && sh.stall && j == 0)) {
                     const uint32_t dst = base + st * kTile + (lh * TS + li * P) * 128;
                     const int row = (int)(phys * P);
                     tma_3d(dst, map, 0, (int)lh, row, smem_u32(&full[st]));
@@ -861,6 +862,7 @@ int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream)
     sh.pps = sh.ts / (uint32_t)a.page_size;
     sh.idx64 = index_u64 != 0;
     sh.bf16 = a.elem_bf16 != 0;
+    sh.stall = a.test_stall != 0;
     switch (a.G) {
     case 1: return launch_g<1>(a, sh, st);
     case 2: return launch_g<2>(a, sh, st);
