@@ -73,6 +73,7 @@ def _check(got, want, vmax):
     # head, so these have 8, 1, 1, 2 and 1 pages per step and 1, 2, 4 or 8 heads
     ("bf16", 2, 8, 128, 8, None), ("f16", 2, 2, 128, 64, None), ("bf16", 1, 1, 128, 128, None),
     ("bf16", 4, 8, 128, 8, None), ("f16", 4, 2, 128, 32, None), ("bf16", 1, 8, 128, 16, None),
+    ("bf16", 8, 2, 128, 8, None),  # 8 K/V heads on pages of 8 slots: two pages per step
 ])
 def test_attention_matches_oracle(hp, oracle, dtype, Hkv, G, D, P, scale):
     # lengths up to ~1300 tokens: small pages move the 32-page window many times
@@ -175,9 +176,10 @@ def test_attention_one_long_sequence_split_over_many_warps(hp, oracle):
     _check(got, want, _vmax_read(od, vpool.cpu().numpy(), "bf16"))
 
 
-def test_attention_mostly_empty_batch(hp, oracle):
+@pytest.mark.parametrize("D", [64, 128])
+def test_attention_mostly_empty_batch(hp, oracle, D):
     """600 sequences, all but three empty (the first and the last nine among them): empty
-    ones give zeros, the others match."""
+    ones give zeros, the others match (head_dim 128 reaches the tensor-core kernel)."""
     import torch
     rng = np.random.default_rng(8)
     lens = np.zeros(600, np.uint32)
@@ -185,7 +187,7 @@ def test_attention_mostly_empty_batch(hp, oracle):
     pages = -(-lens.astype(np.int64) // 16)
     sp = np.concatenate([[0], np.cumsum(pages)]).astype(np.uint32)
     table = rng.permutation(400)[:int(sp[-1])].astype(np.uint32)
-    w = inputs.Workload("sparse", 400, 16, 4, 64, "f16", np.uint32, table, sp, lens, 6, "normal")
+    w = inputs.Workload("sparse", 400, 16, 4, D, "f16", np.uint32, table, sp, lens, 6, "normal")
     b, vpool, qt, got, scale = _run(hp, oracle, w, 8, seed=5)
     od = b.oracle_desc()
     want = od.attention_decode(vpool.cpu().numpy(), qt.view(torch.int16).numpy().view(np.uint16),
