@@ -125,10 +125,12 @@ __device__ __forceinline__ uint2 ld_stream8(const uint2* p)
 
 // 8-byte loads in flight per thread, by measurement on GB300 (a 2.5 GB pool, fraction of
 // the copy bandwidth): per slot 0.85 / 0.90 / 0.81 at 16 / 12 / 24; per head 0.83 at 8,
-// 0.86 at 12; per head_dim 0.84 at 8, 0.79 at 6 and 12.  Fewer loads leave too little in
-// flight; more cost registers and resident CTAs.
+// 0.86 at 12; per head_dim 0.84 at 8, 0.79 at 6 and 12.  With the packed conversion at 3
+// CTAs per SM (the 13 GB pool): per slot 0.949 / 0.945 / 0.897 at 10 / 12 / 16, per slot
+// affine 0.936 / 0.929 / 0.902, per tensor 0.918 / 0.923 / 0.903.  Fewer loads leave too
+// little in flight; more cost registers and resident CTAs.
 #ifndef HP_DQ_UNROLL
-#define HP_DQ_UNROLL 12
+#define HP_DQ_UNROLL 10
 #endif
 #ifndef HP_DQ_UNROLL_DIM
 #define HP_DQ_UNROLL_DIM 8
