@@ -93,6 +93,41 @@ def test_attention_matches_oracle(hp, oracle, dtype, Hkv, G, D, P, scale):
             assert (got[s] == 0).all()
 
 
+def _tc_shapes():
+    """Every shape the tensor-core kernel takes: 1, 2, 4 or 8 K/V heads, G in {1, 2, 4, 8}
+    with at most 32 query heads, pages of a power of two from 8 to 128 / H_kv slots."""
+    out = []
+    for hkv in (1, 2, 4, 8):
+        for g in (1, 2, 4, 8):
+            if hkv * g > 32:
+                continue
+            p = 8
+            while p <= 128 // hkv:
+                out.append((hkv, g, p))
+                p *= 2
+    return out
+
+
+@pytest.mark.parametrize("Hkv,G,P", _tc_shapes())
+def test_attention_every_tensor_core_shape(hp, oracle, Hkv, G, P):
+    """Each supported (K/V heads, query heads per K/V head, page size) on a small ragged
+    batch (lengths 0 to about 600, so partial last steps and empty sequences), dtype
+    alternating, on whichever kernel the fixture asks for: the tensor-core kernel takes
+    every one of these shapes."""
+    import torch
+    dtype = "bf16" if (Hkv + G + P) % 2 == 0 else "f16"
+    w = inputs.decode_gather(seed=Hkv * 100 + G * 10 + P, num_pages=1200, page_size=P,
+                             num_heads=Hkv, head_dim=128, num_seqs=4, len_lo=0, len_hi=600,
+                             dtype=dtype)
+    Hq = Hkv * G
+    b, vpool, qt, got, scale = _run(hp, oracle, w, Hq, seed=P + G)
+    kh = b.host_pool()
+    vh = vpool.cpu().numpy()
+    od = b.oracle_desc(pool_host=kh)
+    want = od.attention_decode(vh, qt.view(torch_int16()).numpy().view(np.uint16), Hq, scale)
+    _check(got, want, _vmax_read(od, vh, dtype))
+
+
 def torch_int16():
     import torch
     return torch.int16
