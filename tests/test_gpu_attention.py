@@ -111,14 +111,15 @@ def _tc_shapes():
 @pytest.mark.parametrize("Hkv,G,P", _tc_shapes())
 def test_attention_every_tensor_core_shape(hp, oracle, Hkv, G, P):
     """Each supported (K/V heads, query heads per K/V head, page size) on a small ragged
-    batch (lengths 0 to about 600, so partial last steps and empty sequences), dtype
-    alternating, on whichever kernel the fixture asks for: the tensor-core kernel takes
-    every one of these shapes."""
+    batch (lengths 0 to about 600, so partial last steps and empty sequences), element
+    type and index width alternating, on whichever kernel the fixture asks for: the
+    tensor-core kernel takes every one of these shapes."""
     import torch
     dtype = "bf16" if (Hkv + G + P) % 2 == 0 else "f16"
+    index_dtype = np.uint64 if (Hkv * G + P // 8) % 2 == 1 else np.uint32
     w = inputs.decode_gather(seed=Hkv * 100 + G * 10 + P, num_pages=1200, page_size=P,
                              num_heads=Hkv, head_dim=128, num_seqs=4, len_lo=0, len_hi=600,
-                             dtype=dtype)
+                             dtype=dtype, index_dtype=index_dtype)
     Hq = Hkv * G
     b, vpool, qt, got, scale = _run(hp, oracle, w, Hq, seed=P + G)
     kh = b.host_pool()
