@@ -647,25 +647,43 @@ u64 attn_step_tokens(u64 G, u64 D)
 }
 uint32_t attn_ranges_per_cta(u64 Hkv) { return Hkv < 8 ? (uint32_t)(8 / Hkv) : 1u; }
 
-// The tensor-core kernel serves head_dim 128 on device-memory pools with power-of-two K/V
-// head counts up to 8, at most 32 query heads and pages of 8 .. 128 / H_kv slots (its steps
-// are 128 (head, token) rows); by default only batches with at least HP_ATTN_TC_MIN_STEPS
-// such steps per SM.  The plan and the planned call decide alike, from the descriptor and
-// the query heads alone.
+// Head_dim 64 reaches the tensor-core kernel as pairs of K/V heads: two adjacent 64-dim
+// heads are one 128-dim row of the pool, and each query, zero-padded to 128 dims in its own
+// head's half, scores only its head's keys.  So an even K/V head count, and G <= 2: the
+// pairs have 2G query heads each, and with 8 the kernel's softmax warps set its pace
+// (measured on GB300, 32 sequences: 8 K/V heads of G = 4 0.707 in pairs against 0.704 on
+// the CUDA cores; 16 of G = 2 0.961 against 0.770).
+bool attn_pairs(const hp_paged_desc* d, u64 G)
+{
+    return d->head_dim == 64 && d->num_heads % 2 == 0 && G <= 2;
+}
+// The K/V heads as the tensor-core kernel sees them.
+u64 attn_tc_heads(const hp_paged_desc* d, u64 G) { return attn_pairs(d, G) ? d->num_heads / 2 : d->num_heads; }
+
+// The tensor-core kernel serves head_dim 128 (and 64 in pairs) on device-memory pools with
+// power-of-two K/V head counts up to 8, at most 32 query heads and pages of 8 .. 128 / H_kv
+// slots (its steps are 128 (head, token) rows); by default only batches with at least
+// HP_ATTN_TC_MIN_STEPS such steps per SM.  The plan and the planned call decide alike, from
+// the descriptor and the query heads alone.
 bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
 {
-    if (!hp::attention_tc_fits(d->head_dim, d->page_size, d->num_pages,
-                               (d->flags & HP_HOST_MEMORY) != 0, d->num_heads, G * d->num_heads) ||
+    const u64 hkv = attn_tc_heads(d, G);
+    const u64 dim = attn_pairs(d, G) ? 128 : d->head_dim;
+    if (!hp::attention_tc_fits(dim, d->page_size, d->num_pages, (d->flags & HP_HOST_MEMORY) != 0,
+                               hkv, G * d->num_heads) ||
         (d->flags & HP_ATTN_CUDA_CORES) || (u128)d->num_seqs * G * d->num_heads >= (1ull << 31))
         return false;  // (the query rows are addressed by a 32-bit tensor coordinate)
     if (d->flags & HP_ATTN_TENSOR_CORES) return true;
     int dev = 0;
     const int sms = hp::current_sms(&dev);
     if (sms == 0) return false;
-    const u128 steps =
-        (u128)d->table_len * d->page_size / hp::attention_tc_step_tokens(d->num_heads);
+    const u128 steps = (u128)d->table_len * d->page_size / hp::attention_tc_step_tokens(hkv);
     return steps >= (u128)HP_ATTN_TC_MIN_STEPS * (u128)sms;
 }
+
+// Floats of one segment record's value sums: head_dim, or 128 for head_dim 64 (a record of
+// the tensor-core kernel then holds a pair of heads).
+u64 attn_record_dim(const hp_paged_desc* d) { return d->head_dim == 64 ? 128 : d->head_dim; }
 
 // Segment records a batch can leave: worker v (of at most HP_ATTN_MAX_CTAS * R) writes
 // record (s + v) * H_kv + g for each sequence s and head g it meets.
@@ -679,10 +697,12 @@ int attention_ws(const hp_paged_desc* d, uint32_t hq, u64* bytes)
     u64 plan = 0;
     int rc = ws_bytes(d, &plan);
     if (rc) return rc;
-    const u128 part = (u128)attn_records(d) * (hq / d->num_heads) * (d->head_dim + 2) * 4;
+    const u128 part = (u128)attn_records(d) * (hq / d->num_heads) * (attn_record_dim(d) + 2) * 4;
     const u128 counts = (u128)d->num_seqs * d->num_heads * 4;
-    if ((part + plan + counts) >> 64) return HP_ERR_OVERFLOW;
-    *bytes = plan + (u64)part + (u64)counts;
+    // head_dim 64: the queries padded to 128 dims for the tensor-core kernel, 256-aligned
+    const u128 qpad = d->head_dim == 64 ? (u128)d->num_seqs * hq * 256 + 256 : 0;
+    if ((part + plan + counts + qpad) >> 64) return HP_ERR_OVERFLOW;
+    *bytes = plan + (u64)part + (u64)counts + (u64)qpad;
     return HP_OK;
 }
 
@@ -704,6 +724,7 @@ struct AttnPrep {
     u64 G;
     char* part;          // the records, after the plan's workspace
     unsigned* seg_done;  // one count per (sequence, K/V head), after the records
+    void* qpad;          // head_dim 64: the padded queries, after the counts (256-aligned)
 };
 
 int attention_prepare(const hp_paged_desc* k_desc, uint32_t num_q_heads, const void* workspace,
@@ -728,7 +749,10 @@ int attention_prepare(const hp_paged_desc* k_desc, uint32_t num_q_heads, const v
     u64 plan_bytes = 0;
     ws_bytes(d, &plan_bytes);
     p->part = static_cast<char*>(const_cast<void*>(workspace)) + plan_bytes;
-    p->seg_done = reinterpret_cast<unsigned*>(p->part + attn_records(d) * p->G * (d->head_dim + 2) * 4);
+    p->seg_done =
+        reinterpret_cast<unsigned*>(p->part + attn_records(d) * p->G * (attn_record_dim(d) + 2) * 4);
+    const uintptr_t end = reinterpret_cast<uintptr_t>(p->seg_done + d->num_seqs * d->num_heads);
+    p->qpad = reinterpret_cast<void*>((end + 255) & ~uintptr_t(255));
     return HP_OK;
 }
 
@@ -745,8 +769,9 @@ HP_API int hp_attention_plan(const hp_paged_desc* k_desc, uint32_t num_q_heads, 
                                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return HP_ERR_CUDA;
     hp::PlanArgs pa = plan_args(d, workspace, d_status);
-    pa.step_tokens = attn_on_tensor_cores(d, p.G) ? hp::attention_tc_step_tokens(d->num_heads)
-                                                  : attn_step_tokens(p.G, d->head_dim);
+    pa.step_tokens = attn_on_tensor_cores(d, p.G)
+                         ? hp::attention_tc_step_tokens(attn_tc_heads(d, p.G))
+                         : attn_step_tokens(p.G, d->head_dim);
     return hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
 }
 
@@ -785,13 +810,25 @@ HP_API int hp_attention_decode_planned(const hp_paged_desc* k_desc, const void* 
     a.hdr = ws.hdr;
     a.units_off = ws.units_off;
     a.part_acc = reinterpret_cast<float*>(p.part);
-    a.part_ml = a.part_acc + attn_records(d) * p.G * d->head_dim;
+    a.part_ml = a.part_acc + attn_records(d) * p.G * attn_record_dim(d);
     a.seg_done = p.seg_done;
     a.out = out;
     a.elem_bf16 = d->dtype == HP_BF16;
     a.test_stall = (d->flags & HP_TEST_STALL) != 0;
     a.d_status = d_status;
-    if (attn_on_tensor_cores(d, p.G)) return hp::launch_attention_tc(d->index_type == HP_IDX_U64, a, stream);
+    if (attn_on_tensor_cores(d, p.G)) {
+        if (attn_pairs(d, p.G)) {
+            // pairs of 64-dim heads as 128-dim heads: padded queries, half the heads, twice G
+            rc = hp::launch_attention_qpad(q, p.qpad, d->num_seqs, num_q_heads, (uint32_t)p.G, stream);
+            if (rc) return rc;
+            a.q = p.qpad;
+            a.Hkv = (uint32_t)(d->num_heads / 2);
+            a.G = (uint32_t)(2 * p.G);
+            a.D = 128;
+            a.pair = 1;
+        }
+        return hp::launch_attention_tc(d->index_type == HP_IDX_U64, a, stream);
+    }
     return hp::launch_attention(d->index_type == HP_IDX_U64, a, stream);
 }
 

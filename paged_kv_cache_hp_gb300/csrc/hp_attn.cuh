@@ -32,6 +32,9 @@ struct AttnArgs {
     int elem_bf16;            // element type: bf16 (1) or f16 (0)
     int test_stall;           // HP_TEST_STALL: the tensor-core kernel never issues its
                               // first K load
+    int pair;                 // tensor cores, head_dim 64 taken as pairs of K/V heads: Hkv,
+                              // G and D describe the pairs (D = 128), q the padded queries,
+                              // out keeps 64 dims per query head
     int* d_status;
 };
 int launch_attention(int index_u64, const AttnArgs& a, void* stream);
@@ -40,10 +43,16 @@ int launch_attention(int index_u64, const AttnArgs& a, void* stream);
 // memory, H_kv in {1, 2, 4, 8} K/V heads, G in {1, 2, 4, 8} query heads per K/V head with
 // at most 32 query heads, pages of 8 .. 128 / H_kv slots (a power of two); a step is
 // attention_tc_step_tokens(H_kv) = 128 / H_kv tokens of a sequence and all its K/V heads.
+// Head_dim 64 runs as pairs of K/V heads (AttnArgs::pair): the queries are first written,
+// zero-padded to 128 dims in their head's half, by launch_attention_qpad.
 bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory,
                        uint64_t num_kv_heads, uint64_t num_q_heads);
 uint64_t attention_tc_step_tokens(uint64_t num_kv_heads);
 int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream);
+// q [num_seqs, Hq, 64] (16-bit) -> qpad [num_seqs, Hq, 128]: query head qh (K/V head
+// qh / G) in dims 64 * ((qh / G) % 2) .. + 64, zeros in the other half.
+int launch_attention_qpad(const void* q, void* qpad, uint64_t num_seqs, uint32_t Hq, uint32_t G,
+                          void* stream);
 
 
 }  // namespace hp

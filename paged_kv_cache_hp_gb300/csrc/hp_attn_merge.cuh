@@ -41,8 +41,12 @@ __device__ __forceinline__ void load_dims(const float* p, float (&x)[E])
 // at row row0 + j * H_kv * G + hh -- into the G normalised results at out + hh * D (the
 // lane's E dims).  The maxima and weight sums first: lane l takes head l % G of records
 // l / G, l / G + 32 / G, ... with a running (max, sum), and the lanes of a head merge
-// theirs pairwise; then the weighted accumulators, CH records at a time.
-template <int G, int E>
+// theirs pairwise; then the weighted accumulators, CH records at a time.  PAIR: the
+// record's D = 128 dims are two 64-dim K/V heads side by side (head_dim 64 taken two heads
+// at a time), query head hh belongs to the first for hh < G / 2 and to the second after
+// it, and only its own head's 64 dims are written, to out + hh * 64 (out then carries no
+// lane offset).
+template <int G, int E, bool PAIR = false>
 __device__ __forceinline__ void merge_segments(const AttnArgs& a, uint64_t row0, uint64_t nr,
                                             float* out, unsigned lane)
 {
@@ -97,6 +101,11 @@ __device__ __forceinline__ void merge_segments(const AttnArgs& a, uint64_t row0,
     for (int hh = 0; hh < G; ++hh) {
         const float inv = 1.0f / __shfl_sync(0xffffffffu, L, hh);
         float* o = out + hh * D;
+        if (PAIR) {
+            const unsigned d0 = lane * E, half = (unsigned)(2 * hh / G);
+            if ((d0 >> 6) != half) continue;
+            o = out + hh * 64 + (d0 & 63);
+        }
 #pragma unroll
         for (int e = 0; e < E; e += 2)
             *reinterpret_cast<float2*>(o + e) = make_float2(acc[hh][e] * inv, acc[hh][e + 1] * inv);

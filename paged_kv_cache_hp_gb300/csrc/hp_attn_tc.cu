@@ -292,6 +292,7 @@ struct TcShape {
     uint32_t idx64; // index type: uint64 (1) or uint32 (0)
     uint32_t bf16;  // element type: bf16 (1) or f16 (0)
     uint32_t stall; // HP_TEST_STALL: the K loader arms its first step but never issues it
+    uint32_t pair;  // head_dim 64 as pairs of K/V heads: 64 output dims per query head
 };
 
 template <int G>
@@ -317,11 +318,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     pdl_wait();  // the plan before this launch is complete
     if (a.hdr->verdict != kVerdictOk) return;
     const unsigned warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t outD = sh.pair ? 64 : kD;  // output dims per query head
     // a sequence without tokens has no step: the grid writes its zeros
     for (uint64_t s = (uint64_t)blockIdx.x * 8 + warp; s < a.num_seqs; s += (uint64_t)gridDim.x * 8)
         if (a.units_off[s] == a.units_off[s + 1]) {
-            float4* o = reinterpret_cast<float4*>(a.out + s * a.Hq * a.D);
-            for (uint64_t i = lane; i < a.Hq * a.D / 4; i += 32) o[i] = make_float4(0, 0, 0, 0);
+            float4* o = reinterpret_cast<float4*>(a.out + s * a.Hq * outD);
+            for (uint64_t i = lane; i < a.Hq * outD / 4; i += 32) o[i] = make_float4(0, 0, 0, 0);
         }
     const uint64_t S_steps = a.hdr->total_units;  // steps of all sequences (all heads each)
     const uint64_t Lw = (S_steps + a.workers - 1) / a.workers;
@@ -710,10 +712,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint64_t so = a.units_off[s], ns = a.units_off[s + 1] - so;
             const uint64_t f = so / Lw, nr = (so + ns - 1) / Lw - f + 1;
             if (nr == 1) {  // the whole sequence: its normalised result, thread = dim
-                float* out = a.out + s * a.Hq * kD + my;
+                if (sh.pair) {  // query head i keeps the 64 dims of its own K/V head
+                    float* out = a.out + s * a.Hq * 64 + (my & 63);
 #pragma unroll
-                for (int i = 0; i < kAcc; ++i)
-                    if ((uint32_t)i < a.Hq) out[(uint64_t)i * kD] = acc[i] * inv_s[i];
+                    for (int i = 0; i < kAcc; ++i)
+                        if ((uint32_t)i < a.Hq && (my >> 6) == (uint32_t)((2 * (i % G)) / G))
+                            out[(uint64_t)i * 64] = acc[i] * inv_s[i];
+                } else {
+                    float* out = a.out + s * a.Hq * kD + my;
+#pragma unroll
+                    for (int i = 0; i < kAcc; ++i)
+                        if ((uint32_t)i < a.Hq) out[(uint64_t)i * kD] = acc[i] * inv_s[i];
+                }
             } else {
                 const uint64_t row0 = (s + v) * a.Hq;  // record rows of all query heads
 #pragma unroll
@@ -730,11 +740,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 named_sync(1, kSoftmax);
                 if (merge_done) {  // the last segment: merge every head's records, a warp each
                     __threadfence();
-                    for (uint32_t hh = t >> 5; hh < HKV; hh += 4)
-                        merge_segments<G, kD / 32>(a, ((s + f) * a.Hkv + hh) * G, nr,
-                                                   a.out + (s * a.Hq + (uint64_t)hh * G) * kD +
-                                                       lane * (kD / 32),
-                                                   lane);
+                    for (uint32_t hh = t >> 5; hh < HKV; hh += 4) {
+                        const uint64_t r0 = ((s + f) * a.Hkv + hh) * G;
+                        if (sh.pair)
+                            merge_segments<G, kD / 32, true>(
+                                a, r0, nr, a.out + (s * a.Hq + (uint64_t)hh * G) * 64, lane);
+                        else
+                            merge_segments<G, kD / 32>(a, r0, nr,
+                                                       a.out + (s * a.Hq + (uint64_t)hh * G) * kD +
+                                                           lane * (kD / 32),
+                                                       lane);
+                    }
                     if (t == 0) a.seg_done[s * a.Hkv] = 0u;
                 }
             }
@@ -852,6 +868,37 @@ bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages
 
 uint64_t attention_tc_step_tokens(uint64_t num_kv_heads) { return kRows / num_kv_heads; }
 
+namespace {
+
+// One 16-byte vector (8 elements) of the padded queries per thread, grid-stride.
+__global__ void qpad_kernel(const uint4* __restrict__ q, uint4* __restrict__ qpad, uint64_t nvec,
+                            uint32_t Hq, uint32_t G)
+{
+    for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t row = v >> 4;          // (sequence, query head): 16 vectors of 128 dims
+        const uint32_t part = (uint32_t)(v & 15), qh = (uint32_t)(row % Hq);
+        const uint32_t half = (qh / G) & 1u;  // the K/V head's place in its pair
+        qpad[v] = (part >> 3) == half ? q[row * 8 + (part & 7)] : make_uint4(0, 0, 0, 0);
+    }
+}
+
+}  // namespace
+
+int launch_attention_qpad(const void* q, void* qpad, uint64_t num_seqs, uint32_t Hq, uint32_t G,
+                          void* stream)
+{
+    const uint64_t nvec = num_seqs * Hq * 16;
+    if (nvec == 0) return HP_OK;
+    int dev = 0;
+    const int sms = current_sms(&dev);
+    if (sms == 0) return HP_ERR_CUDA;
+    const uint64_t grid = std::min<uint64_t>((nvec + 255) / 256, (uint64_t)sms * 8);
+    qpad_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(q), static_cast<uint4*>(qpad), nvec, Hq, G);
+    return cudaGetLastError() == cudaSuccess ? HP_OK : HP_ERR_CUDA;
+}
+
 int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -863,6 +910,7 @@ int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream)
     sh.idx64 = index_u64 != 0;
     sh.bf16 = a.elem_bf16 != 0;
     sh.stall = a.test_stall != 0;
+    sh.pair = a.pair != 0;
     switch (a.G) {
     case 1: return launch_g<1>(a, sh, st);
     case 2: return launch_g<2>(a, sh, st);

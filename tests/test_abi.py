@@ -164,8 +164,10 @@ def test_lane_host_checks(hpc):
 ])
 def test_attention_workspace_bound(hpc, num_seqs, num_heads, G, D):
     """hp_attention_decode_workspace_bytes = the plan's workspace + fp32 records (max, sum,
-    acc[D]) of every query head for (num_seqs + 512 * R) * num_heads segments, R = 8 /
-    num_heads below 8 K/V heads, else 1, and a 4-byte count per (sequence, K/V head)."""
+    acc[D], 128 accumulators for D = 64) of every query head for (num_seqs + 512 * R) *
+    num_heads segments, R = 8 / num_heads below 8 K/V heads, else 1, a 4-byte count per
+    (sequence, K/V head), and for D = 64 the padded queries (256 bytes per query head) with
+    256 bytes of alignment room."""
     W, f = fake_desc(hpc, num_seqs=num_seqs, table_len=3, num_heads=num_heads, head_dim=D,
                      num_pages=4)
     plan = ctypes.c_uint64(0)
@@ -173,5 +175,7 @@ def test_attention_workspace_bound(hpc, num_seqs, num_heads, G, D):
     R = 8 // num_heads if num_heads < 8 else 1
     rc, n = hpc.hp_attention_decode_workspace_bytes(W, G * num_heads)
     assert rc == 0
-    assert n == (plan.value + (num_seqs + 512 * R) * num_heads * G * (D + 2) * 4
-                 + 4 * num_seqs * num_heads)
+    rd = 128 if D == 64 else D
+    qpad = num_seqs * num_heads * G * 256 + 256 if D == 64 else 0
+    assert n == (plan.value + (num_seqs + 512 * R) * num_heads * G * (rd + 2) * 4
+                 + 4 * num_seqs * num_heads + qpad)

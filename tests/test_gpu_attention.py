@@ -108,6 +108,41 @@ def _tc_shapes():
     return out
 
 
+def _tc_pair_shapes():
+    """Head_dim 64 shapes the tensor-core kernel takes in pairs of K/V heads: 2, 4, 8 or 16
+    K/V heads, G in {1, 2} with at most 32 query heads, pages from 8 to 256 / H_kv (and G = 4,
+    which stays on the CUDA cores)."""
+    out = []
+    for hkv in (2, 4, 8, 16):
+        for g in (1, 2, 4):
+            if hkv * g > 32:
+                continue
+            p = 8
+            while p <= 256 // hkv:
+                out.append((hkv, g, p))
+                p *= 2
+    return out
+
+
+@pytest.mark.parametrize("Hkv,G,P", _tc_pair_shapes())
+def test_attention_every_head_dim_64_pair_shape(hp, oracle, Hkv, G, P):
+    """Head_dim 64 on each shape the tensor-core kernel takes as pairs of K/V heads (and on
+    the CUDA-core kernel), small ragged batches, element type and index width alternating."""
+    import torch
+    dtype = "bf16" if (Hkv + G + P) % 2 == 0 else "f16"
+    index_dtype = np.uint64 if (Hkv * G + P // 8) % 2 == 1 else np.uint32
+    w = inputs.decode_gather(seed=Hkv * 100 + G * 10 + P + 7, num_pages=1200, page_size=P,
+                             num_heads=Hkv, head_dim=64, num_seqs=4, len_lo=0, len_hi=600,
+                             dtype=dtype, index_dtype=index_dtype)
+    Hq = Hkv * G
+    b, vpool, qt, got, scale = _run(hp, oracle, w, Hq, seed=P + G + 1)
+    kh = b.host_pool()
+    vh = vpool.cpu().numpy()
+    od = b.oracle_desc(pool_host=kh)
+    want = od.attention_decode(vh, qt.view(torch_int16()).numpy().view(np.uint16), Hq, scale)
+    _check(got, want, _vmax_read(od, vh, dtype))
+
+
 @pytest.mark.parametrize("Hkv,G,P", _tc_shapes())
 def test_attention_every_tensor_core_shape(hp, oracle, Hkv, G, P):
     """Each supported (K/V heads, query heads per K/V head, page size) on a small ragged
