@@ -146,9 +146,10 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * the tensor-core kernel when the shape allows it (head_dim 128; 1, 2, 4 or 8 K/V heads;
  * G = num_q_heads / num_heads in {1, 2, 4, 8} with at most 32 query heads; pages of a
  * power of two from 8 to 128 / num_heads slots; device memory -- or head_dim 64 in pairs
- * of K/V heads, see hp_attention_decode) and the batch has at least HP_ATTN_TC_MIN_STEPS
- * steps of 128 (head, token) rows per SM (table_len * page_size * num_heads / 128 / SMs,
- * with head_dim 64 the pairs counted as heads), the CUDA-core kernel otherwise (measured on GB300: the
+ * of K/V heads, see hp_attention_decode) and either G = 8 at head_dim 128 or the batch has
+ * at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token) rows per SM (table_len *
+ * page_size * num_heads / 128 / SMs, with head_dim 64 the pairs counted as heads), the
+ * CUDA-core kernel otherwise (measured on GB300: the
  * tensor-core kernel is as fast or faster from about 150 steps per SM up, the CUDA-core one
  * on batches of few, short sequences).  HP_ATTN_TENSOR_CORES asks for the tensor-core
  * kernel wherever the shape allows it, HP_ATTN_CUDA_CORES for the CUDA-core kernel always.
@@ -445,7 +446,7 @@ int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t nu
  * sums may run on the tensor cores (products of the 16-bit inputs accumulated in fp32; the
  * weights as two 16-bit parts, so the result stays within about 2^-16 of max|V| of the
  * fp32 one); so may head_dim 64 with 2, 4, 8 or 16 K/V heads and num_q_heads / num_heads
- * <= 2, taken as pairs of K/V heads (two adjacent 64-dim heads as one 128-dim row, each
+ * <= 4, taken as pairs of K/V heads (two adjacent 64-dim heads as one 128-dim row, each
  * query zero-padded to 128 dims in its own head's half, pages of 8 to 256 / num_heads
  * slots); otherwise on the CUDA cores in fp32 --
  * see HP_ATTN_TENSOR_CORES for the choice.  K and V pools in page-locked host memory need

@@ -649,22 +649,24 @@ uint32_t attn_ranges_per_cta(u64 Hkv) { return Hkv < 8 ? (uint32_t)(8 / Hkv) : 1
 
 // Head_dim 64 reaches the tensor-core kernel as pairs of K/V heads: two adjacent 64-dim
 // heads are one 128-dim row of the pool, and each query, zero-padded to 128 dims in its own
-// head's half, scores only its head's keys.  So an even K/V head count, and G <= 2: the
-// pairs have 2G query heads each, and with 8 the kernel's softmax warps set its pace
-// (measured on GB300, 32 sequences: 8 K/V heads of G = 4 0.707 in pairs against 0.704 on
-// the CUDA cores; 16 of G = 2 0.961 against 0.770).
+// head's half, scores only its head's keys.  So an even K/V head count, and G <= 4 (the
+// pairs have 2G query heads each).  Measured on GB300, 32 sequences of 1K-32K tokens: 8 K/V
+// heads of G = 4 0.896 of the copy bandwidth in pairs against 0.704 on the CUDA cores, 16
+// of G = 2 0.961 against 0.770.
 bool attn_pairs(const hp_paged_desc* d, u64 G)
 {
-    return d->head_dim == 64 && d->num_heads % 2 == 0 && G <= 2;
+    return d->head_dim == 64 && d->num_heads % 2 == 0 && G <= 4;
 }
 // The K/V heads as the tensor-core kernel sees them.
 u64 attn_tc_heads(const hp_paged_desc* d, u64 G) { return attn_pairs(d, G) ? d->num_heads / 2 : d->num_heads; }
 
 // The tensor-core kernel serves head_dim 128 (and 64 in pairs) on device-memory pools with
 // power-of-two K/V head counts up to 8, at most 32 query heads and pages of 8 .. 128 / H_kv
-// slots (its steps are 128 (head, token) rows); by default only batches with at least
-// HP_ATTN_TC_MIN_STEPS such steps per SM.  The plan and the planned call decide alike, from
-// the descriptor and the query heads alone.
+// slots (its steps are 128 (head, token) rows); by default head_dim 128 with G = 8 always
+// (the CUDA-core kernel reaches 0.32-0.48 of the copy bandwidth there, the tensor-core one
+// 0.53-0.87, and small batches are faster too), every other shape only on batches with at
+// least HP_ATTN_TC_MIN_STEPS such steps per SM.  The plan and the planned call decide
+// alike, from the descriptor and the query heads alone.
 bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
 {
     const u64 hkv = attn_tc_heads(d, G);
@@ -673,7 +675,7 @@ bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
                                hkv, G * d->num_heads) ||
         (d->flags & HP_ATTN_CUDA_CORES) || (u128)d->num_seqs * G * d->num_heads >= (1ull << 31))
         return false;  // (the query rows are addressed by a 32-bit tensor coordinate)
-    if (d->flags & HP_ATTN_TENSOR_CORES) return true;
+    if ((d->flags & HP_ATTN_TENSOR_CORES) || (G == 8 && !attn_pairs(d, G))) return true;
     int dev = 0;
     const int sms = hp::current_sms(&dev);
     if (sms == 0) return false;

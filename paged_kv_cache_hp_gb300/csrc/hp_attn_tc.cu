@@ -75,6 +75,7 @@ constexpr int kThreadsTc = 8 * 32;
 constexpr int kSoftmax = 128;       // warps 2-5
 constexpr uint32_t kTmemCols = 512; // S x 2 (64 columns), O x 2 (up to 2 x 8 x 16)
 constexpr uint32_t kOCol = 2 * kNS; // first O column
+constexpr float kTau = 8.0f;        // log2 units a score may exceed its head's reference by
 
 // shared memory: K ring, V ring, then P (2 steps x hi/lo), then Q (2 segments)
 constexpr uint32_t kOffP = kKV * 2 * kTile;
@@ -637,24 +638,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 fence_before();
                 mbar_arrive(smem_u32(&s_free[j % 2]));
                 const bool valid = k * TS + rt < len;
+                // Lazy rescaling: each query head's weights are exp2(x - m_ref) against a
+                // reference m_ref that moves only when some score exceeds it by more than
+                // kTau (weights stay below 2^kTau, well inside the fp32 sums and the two
+                // 16-bit parts) -- on a head's first step, and rarely after.  The step
+                // barrier is the vote; only when it passes are the heads' maxima reduced and
+                // the factors that rescale the sums and (at the next fold) the accumulators
+                // formed.
+                bool need = false;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     x[g] = valid ? x[g] * qscale : -INFINITY;
-                    mx[g] = x[g];
+                    need |= x[g] > m_run[g] + kTau;  // (m_run -inf: any valid score)
                 }
-                head_reduce(mx, true);  // the step's maximum of each query head of rh
-                bool up = false;
+                // the step barrier: whether any reference must move, and whether any wait
+                // of this window ran out
+                need = named_or(3, kSoftmax, need);
+                ok_w = true;
+                if (*(volatile int*)&fail_s[j % 2]) {
+                    stop = true;
+                    break;
+                }
+                if (need) {  // the same in every softmax thread
+#pragma unroll
+                    for (int g = 0; g < G; ++g) mx[g] = x[g];
+                    head_reduce(mx, true);  // the step's maximum of each query head of rh
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float mn = fmaxf(m_run[g], mx[g]);
+                        const float c = exp2_approx(m_run[g] - mn);  // 0 while nothing is summed
+                        lp[g] *= c;
+                        if (rt == 0) corr_s[j % 2][rh * G + g] = c;
+                        m_run[g] = mn;
+                    }
+                }
                 unsigned char* pb = smem + kOffP + (uint32_t)(j % 2) * 2 * kPBuf;
                 const uint32_t pcol = my & 63, patom = (my >> 6) * 2048;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float mn = fmaxf(m_run[g], mx[g]);
-                    up |= mn > m_run[g];
-                    const float c = exp2_approx(m_run[g] - mn);  // 0 while nothing is summed
-                    const float p = exp2_approx(x[g] - mn);      // 0 past the sequence
-                    lp[g] = lp[g] * c + p;
-                    if (rt == 0) corr_s[j % 2][rh * G + g] = c;
-                    m_run[g] = mn;
+                    const float p = exp2_approx(x[g] - m_run[g]);  // 0 past the sequence
+                    lp[g] += p;
                     unsigned short hi, lo;
                     if (bf16) {
                         const __nv_bfloat16 bh = __float2bfloat16_rn(p);
@@ -672,7 +695,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 // rows of V past the sequence become zeros (their weights are zero, and a
                 // stale or undefined value must not reach the product)
                 if ((k + 1) * TS > len) {  // the same in every softmax thread
-                    wait_one(smem_u32(&v_full[j % kKV]), (uint32_t)((j / kKV) & 1), j);
+                    wait_one(smem_u32(&v_full[j % kKV]), (uint32_t)((j / kKV) & 1), j + 1);
                     if (!valid) {
                         unsigned char* vrow = smem + (kKV + (uint32_t)(j % kKV)) * kTile + my * 128;
 #pragma unroll
@@ -684,17 +707,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(smem_u32(&p_full[j % 2]));
-                // the step barrier: whether any maximum rose (and the step's factors, now
-                // visible to all), and whether any wait of this window ran out
-                up = named_or(3, kSoftmax, up);
-                ok_w = true;
-                if (*(volatile int*)&fail_s[j % 2]) {
-                    stop = true;
-                    break;
-                }
-                // the previous step's O, now that this step's weights are handed over
+                // the previous step's O, now that this step's weights are handed over (the
+                // factors of step j - 1 were written before this step's barrier)
                 if (k > k0) fold(j - 1, up_prev, j + 1);
-                up_prev = up;
+                up_prev = need;
             }
             if (stop) break;
             fold(j - 1, up_prev, j);

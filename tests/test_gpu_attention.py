@@ -110,8 +110,7 @@ def _tc_shapes():
 
 def _tc_pair_shapes():
     """Head_dim 64 shapes the tensor-core kernel takes in pairs of K/V heads: 2, 4, 8 or 16
-    K/V heads, G in {1, 2} with at most 32 query heads, pages from 8 to 256 / H_kv (and G = 4,
-    which stays on the CUDA cores)."""
+    K/V heads, G in {1, 2, 4} with at most 32 query heads, pages from 8 to 256 / H_kv."""
     out = []
     for hkv in (2, 4, 8, 16):
         for g in (1, 2, 4):
