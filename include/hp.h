@@ -143,13 +143,14 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * hp_copy_pages, hp_lane_gather and hp_lane_append. */
 #define HP_HOST_MEMORY 0x4u
 /* Decode attention's kernel (no counterpart in the pages).  By default the library picks:
- * the tensor-core kernel when the shape allows it (head_dim 128; 1, 2, 4 or 8 K/V heads;
- * G = num_q_heads / num_heads in {1, 2, 4, 8} with at most 32 query heads; pages of a
- * power of two from 8 to 128 / num_heads slots; device memory -- or head_dim 64 in pairs
- * of K/V heads, see hp_attention_decode) and either G = 8 at head_dim 128 or the batch has
- * at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token) rows per SM (table_len *
- * page_size * num_heads / 128 / SMs, with head_dim 64 the pairs counted as heads), the
- * CUDA-core kernel otherwise (measured on GB300: the
+ * the tensor-core kernel when the shape allows it (head_dim 128, or 64 in pairs of K/V
+ * heads, see hp_attention_decode; a power-of-two number of K/V heads; G = num_q_heads /
+ * num_heads in {1, 2, 4, 8}; pages of a power of two from 8 to 128 / h slots, h the K/V
+ * heads of one launch: at most 8, with at most 32 query heads, more K/V heads running as
+ * groups of h, one launch each; device memory) and either G = 8 at head_dim 128 or, in at
+ * most two launches, the batch has at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token)
+ * rows per SM (table_len * page_size * num_heads / 128 / SMs, with head_dim 64 the pairs
+ * counted as heads), the CUDA-core kernel otherwise (measured on GB300: the
  * tensor-core kernel is as fast or faster from about 150 steps per SM up, the CUDA-core one
  * on batches of few, short sequences).  HP_ATTN_TENSOR_CORES asks for the tensor-core
  * kernel wherever the shape allows it, HP_ATTN_CUDA_CORES for the CUDA-core kernel always.
@@ -441,14 +442,15 @@ int hp_attention_decode_workspace_bytes(const hp_paged_desc* k_desc, uint32_t nu
  * has the pool's element type (HP_F16 or HP_BF16); out (device, fp32, same shape) gets 0
  * for a sequence with no tokens.  Arithmetic is fp32.  Supported: head_dim 64, 128 or
  * 256, num_q_heads / num_heads in {1, 2, 4, 8}, page_size <= 2^26 (HP_ERR_ARG otherwise).
- * With head_dim 128, 1, 2, 4 or 8 K/V heads, at most 32 query heads, pages of 8 to
- * 128 / num_heads slots and both pools in device memory the scores and the weighted value
+ * With head_dim 128, a power-of-two number of K/V heads (more than 8, or more than 32
+ * query heads, in groups of K/V heads, one launch each), pages of 8 to 128 / h slots (h the
+ * K/V heads of one launch) and both pools in device memory the scores and the weighted value
  * sums may run on the tensor cores (products of the 16-bit inputs accumulated in fp32; the
  * weights as two 16-bit parts, so the result stays within about 2^-16 of max|V| of the
- * fp32 one); so may head_dim 64 with 2, 4, 8 or 16 K/V heads and num_q_heads / num_heads
- * <= 4, taken as pairs of K/V heads (two adjacent 64-dim heads as one 128-dim row, each
- * query zero-padded to 128 dims in its own head's half, pages of 8 to 256 / num_heads
- * slots); otherwise on the CUDA cores in fp32 --
+ * fp32 one); so may head_dim 64 with an even, power-of-two number of K/V heads and
+ * num_q_heads / num_heads <= 4, taken as pairs of K/V heads (two adjacent 64-dim heads as
+ * one 128-dim row, each query zero-padded to 128 dims in its own head's half; h then counts
+ * pairs); otherwise on the CUDA cores in fp32 --
  * see HP_ATTN_TENSOR_CORES for the choice.  K and V pools in page-locked host memory need
  * HP_HOST_MEMORY in k_desc's flags (they are then read in place over the host link by the
  * CUDA-core kernel).

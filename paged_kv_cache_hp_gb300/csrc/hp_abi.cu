@@ -657,29 +657,43 @@ bool attn_pairs(const hp_paged_desc* d, u64 G)
 {
     return d->head_dim == 64 && d->num_heads % 2 == 0 && G <= 4;
 }
-// The K/V heads as the tensor-core kernel sees them.
+// The K/V heads as the tensor-core kernel sees them, their query heads per head, and the
+// heads of one launch: at most 8, with at most 32 query heads (larger counts run as groups
+// of K/V heads, one launch each).
 u64 attn_tc_heads(const hp_paged_desc* d, u64 G) { return attn_pairs(d, G) ? d->num_heads / 2 : d->num_heads; }
+u64 attn_tc_g(const hp_paged_desc* d, u64 G) { return attn_pairs(d, G) ? 2 * G : G; }
+u64 attn_tc_group(const hp_paged_desc* d, u64 G)
+{
+    u64 hg = attn_tc_heads(d, G);
+    while (hg > 1 && (hg > 8 || hg * attn_tc_g(d, G) > 32)) hg /= 2;
+    return hg;
+}
 
 // The tensor-core kernel serves head_dim 128 (and 64 in pairs) on device-memory pools with
-// power-of-two K/V head counts up to 8, at most 32 query heads and pages of 8 .. 128 / H_kv
-// slots (its steps are 128 (head, token) rows); by default head_dim 128 with G = 8 always
-// (the CUDA-core kernel reaches 0.32-0.48 of the copy bandwidth there, the tensor-core one
-// 0.53-0.87, and small batches are faster too), every other shape only on batches with at
-// least HP_ATTN_TC_MIN_STEPS such steps per SM.  The plan and the planned call decide
-// alike, from the descriptor and the query heads alone.
+// power-of-two K/V head counts, in launches of at most 8 K/V heads and 32 query heads, pages
+// of 8 .. 128 / H_kv slots (H_kv of one launch; its steps are 128 (head, token) rows); by
+// default head_dim 128 with G = 8 always (the CUDA-core kernel reaches 0.32-0.50 of the copy
+// bandwidth there, the tensor-core one 0.53-0.90, and small batches are faster too), every
+// other shape in at most two launches and only on batches with at least
+// HP_ATTN_TC_MIN_STEPS such steps per SM.  The plan and the planned call decide alike, from
+// the descriptor and the query heads alone.
 bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
 {
-    const u64 hkv = attn_tc_heads(d, G);
+    const u64 hkv = attn_tc_heads(d, G), hg = attn_tc_group(d, G);
     const u64 dim = attn_pairs(d, G) ? 128 : d->head_dim;
-    if (!hp::attention_tc_fits(dim, d->page_size, d->num_pages, (d->flags & HP_HOST_MEMORY) != 0,
-                               hkv, G * d->num_heads) ||
-        (d->flags & HP_ATTN_CUDA_CORES) || (u128)d->num_seqs * G * d->num_heads >= (1ull << 31))
-        return false;  // (the query rows are addressed by a 32-bit tensor coordinate)
+    if (hkv % hg || !hp::attention_tc_fits(dim, d->page_size, d->num_pages,
+                                           (d->flags & HP_HOST_MEMORY) != 0, hg,
+                                           hg * attn_tc_g(d, G)) ||
+        (d->flags & HP_ATTN_CUDA_CORES) || d->num_seqs >= (1ull << 31))
+        return false;  // (a sequence is a 32-bit tensor coordinate of the queries)
     if ((d->flags & HP_ATTN_TENSOR_CORES) || (G == 8 && !attn_pairs(d, G))) return true;
+    // more than two launches cost more than they save unless G = 8 (measured: 32 K/V heads
+    // of G = 2 in 4 groups 0.855 of the copy bandwidth against 0.895 on the CUDA cores)
+    if (hkv / hg > 2) return false;
     int dev = 0;
     const int sms = hp::current_sms(&dev);
     if (sms == 0) return false;
-    const u128 steps = (u128)d->table_len * d->page_size / hp::attention_tc_step_tokens(hkv);
+    const u128 steps = (u128)d->table_len * d->page_size * hkv / 128;
     return steps >= (u128)HP_ATTN_TC_MIN_STEPS * (u128)sms;
 }
 
@@ -772,7 +786,7 @@ HP_API int hp_attention_plan(const hp_paged_desc* k_desc, uint32_t num_q_heads, 
         return HP_ERR_CUDA;
     hp::PlanArgs pa = plan_args(d, workspace, d_status);
     pa.step_tokens = attn_on_tensor_cores(d, p.G)
-                         ? hp::attention_tc_step_tokens(attn_tc_heads(d, p.G))
+                         ? hp::attention_tc_step_tokens(attn_tc_group(d, p.G))
                          : attn_step_tokens(p.G, d->head_dim);
     return hp::launch_plan(hp::kPlanAttention, d->index_type == HP_IDX_U64, pa, stream);
 }
@@ -829,7 +843,25 @@ HP_API int hp_attention_decode_planned(const hp_paged_desc* k_desc, const void* 
             a.D = 128;
             a.pair = 1;
         }
-        return hp::launch_attention_tc(d->index_type == HP_IDX_U64, a, stream);
+        // groups of K/V heads with at most 32 query heads, one launch each: the pool rows
+        // and the query and output rows keep their full strides, the pointers move to the
+        // group's first head (256 bytes of K or V per head; 128-dim queries; outD floats)
+        const uint32_t hg = (uint32_t)attn_tc_group(d, p.G), groups = a.Hkv / hg;
+        const uint64_t outD = a.pair ? 64 : 128;
+        hp::AttnArgs ag = a;
+        ag.Hkv_row = a.Hkv;
+        ag.Hq_row = a.Hq;
+        ag.Hkv = hg;
+        ag.Hq = hg * a.G;
+        for (uint32_t grp = 0; grp < groups; ++grp) {
+            ag.k_pool = static_cast<const char*>(a.k_pool) + (u64)grp * hg * 256;
+            ag.v_pool = static_cast<const char*>(a.v_pool) + (u64)grp * hg * 256;
+            ag.q = static_cast<const char*>(a.q) + (u64)grp * ag.Hq * 256;
+            ag.out = a.out + (u64)grp * ag.Hq * outD;
+            rc = hp::launch_attention_tc(d->index_type == HP_IDX_U64, ag, stream);
+            if (rc) return rc;
+        }
+        return HP_OK;
     }
     return hp::launch_attention(d->index_type == HP_IDX_U64, a, stream);
 }

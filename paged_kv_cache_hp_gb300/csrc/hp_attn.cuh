@@ -35,6 +35,11 @@ struct AttnArgs {
     int pair;                 // tensor cores, head_dim 64 taken as pairs of K/V heads: Hkv,
                               // G and D describe the pairs (D = 128), q the padded queries,
                               // out keeps 64 dims per query head
+    uint32_t Hkv_row;         // tensor cores, one group of K/V heads per launch: the heads of
+                              // a pool row (k_pool, v_pool point at the group's first head);
+                              // 0 = Hkv
+    uint32_t Hq_row;          // and the query heads of a sequence in q and out (both point at
+                              // the group's first query head); 0 = Hq
     int* d_status;
 };
 int launch_attention(int index_u64, const AttnArgs& a, void* stream);
@@ -44,7 +49,8 @@ int launch_attention(int index_u64, const AttnArgs& a, void* stream);
 // at most 32 query heads, pages of 8 .. 128 / H_kv slots (a power of two); a step is
 // attention_tc_step_tokens(H_kv) = 128 / H_kv tokens of a sequence and all its K/V heads.
 // Head_dim 64 runs as pairs of K/V heads (AttnArgs::pair): the queries are first written,
-// zero-padded to 128 dims in their head's half, by launch_attention_qpad.
+// zero-padded to 128 dims in their head's half, by launch_attention_qpad.  More than 32 query
+// heads run as groups of K/V heads, one launch each (AttnArgs::Hkv_row, Hq_row).
 bool attention_tc_fits(uint64_t head_dim, uint64_t page_size, uint64_t num_pages, bool host_memory,
                        uint64_t num_kv_heads, uint64_t num_q_heads);
 uint64_t attention_tc_step_tokens(uint64_t num_kv_heads);

@@ -211,16 +211,6 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
         : "memory");
 }
 
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                       uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
 // Byte offset of element (row r, column c) of a 128-byte-swizzled K-major operand whose
 // 8-row groups are 1024 bytes apart, c < 64 (one 128-byte row).
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c)
@@ -294,6 +284,7 @@ struct TcShape {
     uint32_t bf16;  // element type: bf16 (1) or f16 (0)
     uint32_t stall; // HP_TEST_STALL: the K loader arms its first step but never issues it
     uint32_t pair;  // head_dim 64 as pairs of K/V heads: 64 output dims per query head
+    uint32_t hq_row;  // query heads per sequence in out (this launch's group: a.Hq of them)
 };
 
 template <int G>
@@ -323,7 +314,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // a sequence without tokens has no step: the grid writes its zeros
     for (uint64_t s = (uint64_t)blockIdx.x * 8 + warp; s < a.num_seqs; s += (uint64_t)gridDim.x * 8)
         if (a.units_off[s] == a.units_off[s + 1]) {
-            float4* o = reinterpret_cast<float4*>(a.out + s * a.Hq * outD);
+            float4* o = reinterpret_cast<float4*>(a.out + s * sh.hq_row * outD);
             for (uint64_t i = lane; i < a.Hq * outD / 4; i += 32) o[i] = make_float4(0, 0, 0, 0);
         }
     const uint64_t S_steps = a.hdr->total_units;  // steps of all sequences (all heads each)
@@ -403,10 +394,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     ok = seg < 2 || mbar_wait(smem_u32(&q_free[seg % 2]), (uint32_t)((seg / 2 - 1) & 1));
                     if (ok) {
                         const uint32_t qb = sm0 + kOffQ + (uint32_t)(seg % 2) * kQBuf;
-                        const int row = (int)(s * a.Hq);
                         mbar_expect_tx(smem_u32(&q_full[seg % 2]), 2 * a.Hq * 128);
-                        tma_2d(qb, &tmq, 0, row, smem_u32(&q_full[seg % 2]));
-                        tma_2d(qb + kNS * 128, &tmq, 64, row, smem_u32(&q_full[seg % 2]));
+                        tma_3d(qb, &tmq, 0, 0, (int)s, smem_u32(&q_full[seg % 2]));
+                        tma_3d(qb + kNS * 128, &tmq, 64, 0, (int)s, smem_u32(&q_full[seg % 2]));
                     }
                 }
                 if (failed(__shfl_sync(0xffffffffu, ok, 0) != 0)) break;
@@ -729,13 +719,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint64_t f = so / Lw, nr = (so + ns - 1) / Lw - f + 1;
             if (nr == 1) {  // the whole sequence: its normalised result, thread = dim
                 if (sh.pair) {  // query head i keeps the 64 dims of its own K/V head
-                    float* out = a.out + s * a.Hq * 64 + (my & 63);
+                    float* out = a.out + s * sh.hq_row * 64 + (my & 63);
 #pragma unroll
                     for (int i = 0; i < kAcc; ++i)
                         if ((uint32_t)i < a.Hq && (my >> 6) == (uint32_t)((2 * (i % G)) / G))
                             out[(uint64_t)i * 64] = acc[i] * inv_s[i];
                 } else {
-                    float* out = a.out + s * a.Hq * kD + my;
+                    float* out = a.out + s * sh.hq_row * kD + my;
 #pragma unroll
                     for (int i = 0; i < kAcc; ++i)
                         if ((uint32_t)i < a.Hq) out[(uint64_t)i * kD] = acc[i] * inv_s[i];
@@ -760,12 +750,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         const uint64_t r0 = ((s + f) * a.Hkv + hh) * G;
                         if (sh.pair)
                             merge_segments<G, kD / 32, true>(
-                                a, r0, nr, a.out + (s * a.Hq + (uint64_t)hh * G) * 64, lane);
+                                a, r0, nr, a.out + (s * sh.hq_row + (uint64_t)hh * G) * 64, lane);
                         else
-                            merge_segments<G, kD / 32>(a, r0, nr,
-                                                       a.out + (s * a.Hq + (uint64_t)hh * G) * kD +
-                                                           lane * (kD / 32),
-                                                       lane);
+                            merge_segments<G, kD / 32>(
+                                a, r0, nr,
+                                a.out + (s * sh.hq_row + (uint64_t)hh * G) * kD + lane * (kD / 32),
+                                lane);
                     }
                     if (t == 0) a.seg_done[s * a.Hkv] = 0u;
                 }
@@ -802,14 +792,15 @@ EncodeFn encode_fn()
     return fn;
 }
 
-// A pool [num_pages * P tokens, H_kv, 128] as a 3-d tensor: boxes of 64 dims x 1 head x P
-// tokens, 128-byte swizzled.
+// A pool [num_pages * P tokens, H_kv, 128] as a 3-d tensor (this launch's H_kv heads of the
+// Hkv_row in each token's row): boxes of 64 dims x 1 head x P tokens, 128-byte swizzled.
 bool pool_map(CUtensorMap* m, const void* pool, const AttnArgs& a, bool bf16)
 {
     EncodeFn fn = encode_fn();
     if (!fn) return false;
+    const uint64_t row = a.Hkv_row ? a.Hkv_row : a.Hkv;
     const cuuint64_t dims[3] = {kD, a.Hkv, a.num_pages * a.page_size};
-    const cuuint64_t strides[2] = {kD * 2, (cuuint64_t)a.Hkv * kD * 2};
+    const cuuint64_t strides[2] = {kD * 2, (cuuint64_t)row * kD * 2};
     const cuuint32_t box[3] = {64, 1, (cuuint32_t)a.page_size};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -818,17 +809,18 @@ bool pool_map(CUtensorMap* m, const void* pool, const AttnArgs& a, bool bf16)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The queries [num_seqs * Hq rows, 128] as a 2-d tensor: boxes of 64 dims x Hq rows (the
-// query heads of one sequence), 128-byte swizzled.
+// The queries [num_seqs, Hq, 128] as a 3-d tensor (this launch's Hq query heads of the
+// Hq_row of each sequence): boxes of 64 dims x Hq heads x 1 sequence, 128-byte swizzled.
 bool query_map(CUtensorMap* m, const AttnArgs& a, bool bf16)
 {
     EncodeFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {kD, a.num_seqs * a.Hq};
-    const cuuint64_t strides[1] = {kD * 2};
-    const cuuint32_t box[2] = {64, a.Hq};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const uint64_t row = a.Hq_row ? a.Hq_row : a.Hq;
+    const cuuint64_t dims[3] = {kD, a.Hq, a.num_seqs};
+    const cuuint64_t strides[2] = {kD * 2, (cuuint64_t)row * kD * 2};
+    const cuuint32_t box[3] = {64, a.Hq, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
               const_cast<void*>(a.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -927,6 +919,7 @@ int launch_attention_tc(int index_u64, const AttnArgs& a, void* stream)
     sh.bf16 = a.elem_bf16 != 0;
     sh.stall = a.test_stall != 0;
     sh.pair = a.pair != 0;
+    sh.hq_row = a.Hq_row ? a.Hq_row : a.Hq;
     switch (a.G) {
     case 1: return launch_g<1>(a, sh, st);
     case 2: return launch_g<2>(a, sh, st);

@@ -142,6 +142,29 @@ def test_attention_every_head_dim_64_pair_shape(hp, oracle, Hkv, G, P):
     _check(got, want, _vmax_read(od, vh, dtype))
 
 
+@pytest.mark.parametrize("Hkv,G,D,P", [
+    (8, 8, 128, 16), (16, 4, 128, 8), (16, 8, 128, 16), (32, 2, 128, 16),
+    (16, 4, 64, 16), (32, 2, 64, 8), (8, 8, 64, 16),
+])
+def test_attention_more_than_32_query_heads(hp, oracle, Hkv, G, D, P):
+    """More than 32 query heads: the tensor-core kernel runs once per group of K/V heads with
+    at most 32 query heads (2 or 4 groups here; head_dim 64 in pairs first), each launch on
+    its heads' slice of the pool rows, the queries and the output (head_dim 64 at G = 8 stays
+    on the CUDA cores).  Small ragged batches against the oracle."""
+    import torch
+    dtype = "bf16" if (Hkv + G) % 2 == 0 else "f16"
+    w = inputs.decode_gather(seed=Hkv * 10 + G + D + P, num_pages=2000, page_size=P,
+                             num_heads=Hkv, head_dim=D, num_seqs=5, len_lo=0, len_hi=700,
+                             dtype=dtype, index_dtype=np.uint64 if G == 2 else np.uint32)
+    Hq = Hkv * G
+    b, vpool, qt, got, scale = _run(hp, oracle, w, Hq, seed=Hq + P)
+    kh = b.host_pool()
+    vh = vpool.cpu().numpy()
+    od = b.oracle_desc(pool_host=kh)
+    want = od.attention_decode(vh, qt.view(torch_int16()).numpy().view(np.uint16), Hq, scale)
+    _check(got, want, _vmax_read(od, vh, dtype))
+
+
 @pytest.mark.parametrize("Hkv,G,P", _tc_shapes())
 def test_attention_every_tensor_core_shape(hp, oracle, Hkv, G, P):
     """Each supported (K/V heads, query heads per K/V head, page size) on a small ragged
