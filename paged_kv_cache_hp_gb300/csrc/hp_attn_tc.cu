@@ -1,5 +1,5 @@
 // hp_attn_tc.cu -- decode attention through the block table on the tensor cores (tcgen05),
-// for head_dim 128.
+// for head_dim 128 (and head_dim 64 taken two K/V heads at a time, see below).
 //
 // The same computation as hp_attention.cu ("Visualize PagedAttention block layout", How the
 // attention kernel uses the block table; K(s,t,g) and V(s,t,g) read through the Element
@@ -32,17 +32,27 @@
 //               and N <= 64 keeps the tensor pipe only about 45 cycles (measured on GB300),
 //               less than a loop that rebuilds descriptors takes to issue it;
 //   warps 2-5   softmax and accumulation, one thread per TMEM lane: a step's scores (lane =
-//               row = (head, token)), masked past the sequence, the running maximum of each
-//               query head (a shuffle reduction over the head's rows), the weights written as
-//               16-bit pairs hi + lo = p (so P.V keeps about 16 significant bits where one
-//               16-bit P would keep 8), then the previous step's O (lane = dim) folded into
-//               fp32 registers, rescaled only on the steps where some query's maximum rose.
+//               row = (head, token)), masked past the sequence, weighed against each query
+//               head's reference maximum -- which moves (a shuffle reduction over the head's
+//               rows, a factor for the sums and the accumulators) only when some score exceeds
+//               it by more than 2^kTau: lazy rescaling --, the weights written as 16-bit pairs
+//               hi + lo = p (so P.V keeps about 16 significant bits where one 16-bit P would
+//               keep 8), then the previous step's O (lane = dim) folded into fp32 registers,
+//               rescaled only after the steps whose references moved.
 // Rows of V past the sequence (an unfilled last page, or pages a step does not have) are
 // zeroed in shared memory before their weights (zero) are handed over, so no stale or
 // undefined value reaches the product.  Every wait is bounded (about 2 s); a wait that runs
 // out reports HP_ERR_TIMEOUT, every role leaves its loop (the softmax threads decide it
 // together at their one barrier per step, so none is left at a barrier), and the loads and
 // matrix operations already issued are waited for (bounded) before the TMEM is freed.
+//
+// One launch takes up to 8 K/V heads and 32 query heads of 128 dims.  The host runs more as
+// groups of K/V heads, one launch each on the same plan: the tensor maps then cover the
+// group's slice of each pool row and of each sequence's queries (full-row strides), and the
+// output pointer and its sequence stride (TcShape::hq_row) do the same.  Head_dim 64 runs as
+// pairs of K/V heads (TcShape::pair): two adjacent 64-dim heads are one 128-dim row, each
+// query is zero-padded to 128 dims in its own head's half (qpad_kernel), so its score is its
+// 64-dim one, and each query head keeps only its head's 64 dims of the value sums.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
