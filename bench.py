@@ -702,13 +702,21 @@ def rate_entry(bytes_, ms, peak, **kw):
     return dict(ms=round(ms, 4), gbps=round(gbps, 1), frac=round(gbps / peak, 4), **kw)
 
 
-def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False, kernel="auto"):
+def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False, kernel="auto",
+                   heads=(8, 4, 128)):
     """Decode attention alone on the decode-append batch at `scale` ("full": 256 sequences
     of 1K-32K tokens; "mid": 32 of them, about 2.5 GB on the device, the profiler's case;
     "short": 2048 sequences of 16-1024 tokens); host_kv: K and V in page-locked host
-    memory (HP_HOST_MEMORY); kernel: "auto" (the library's choice), "tensor" or "cuda"."""
+    memory (HP_HOST_MEMORY); kernel: "auto" (the library's choice), "tensor" or "cuda";
+    heads: (K/V heads, query heads per K/V head, head_dim) -- the same token counts and
+    page tables with another head layout."""
     import torch
     w = inputs.config("decode_append", scale)
+    hkv, g, hd = heads
+    if (hkv, hd) != (w.num_heads, w.head_dim):
+        lo, hi = (16, 1024) if scale == "short" else (1024, 32768)
+        w = inputs.decode_append(num_pages=w.num_pages, num_seqs=w.num_seqs, len_lo=lo,
+                                 len_hi=hi, num_heads=hkv, head_dim=hd, name=w.name)
     pool = inputs.device_pool(w, dev)
     hk = None
     if host_kv:
@@ -725,7 +733,8 @@ def attention_only(scale, dev, hp, inputs, peak, reps, host_kv=False, kernel="au
     stream = torch.cuda.current_stream()
     res = attention_measurement(dev, hp, inputs, w, d_k, peak,
                                 lambda b, ms, **kw: rate_entry(b, ms, peak, **kw),
-                                lambda fn, n: median_ms(fn, stream, n), reps=reps, host_kv=hk)
+                                lambda fn, n: median_ms(fn, stream, n), Hq=hkv * g, reps=reps,
+                                host_kv=hk)
     res.update(op="decode_attention", workload=w.name, num_seqs=w.num_seqs,
                total_tokens=w.total_tokens, num_heads=w.num_heads, head_dim=w.head_dim,
                kv_memory="page-locked host" if host_kv else "device", kernel=kernel)
@@ -1255,6 +1264,9 @@ def main():
                     help="with --attention: K and V pools in page-locked host memory")
     ap.add_argument("--attention-kernel", default="auto", choices=["auto", "tensor", "cuda"],
                     help="with --attention: the library's choice of kernel, or force one")
+    ap.add_argument("--attention-heads", default="8,4,128",
+                    help="with --attention: K/V heads, query heads per K/V head and head_dim "
+                         "(the same sequences with another head layout)")
     ap.add_argument("--transpose", action="store_true",
                     help="time only the two cache layout conversions (kernel-internal "
                          "[10000, 32, 16, 16, 8] <-> interchange [10000, 16, 32, 128], fp16) "
@@ -1317,9 +1329,10 @@ def main():
         from paged_kv_cache_hp_gb300 import build, hp, inputs
         build.build()
         hp.lib()
+        heads = tuple(int(x) for x in args.attention_heads.split(","))
         print(json.dumps(attention_only(args.attention, "cuda", hp, inputs, peak_hbm()[0],
                                         args.steps, host_kv=args.host_kv,
-                                        kernel=args.attention_kernel)))
+                                        kernel=args.attention_kernel, heads=heads)))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -149,8 +149,8 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * heads of one launch: at most 8, with at most 32 query heads, more K/V heads running as
  * groups of h, one launch each; device memory) and either G = 8 at head_dim 128 or, in at
  * most two launches, the batch has at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token)
- * rows per SM (table_len * page_size * num_heads / 128 / SMs, with head_dim 64 the pairs
- * counted as heads), the CUDA-core kernel otherwise (measured on GB300: the
+ * rows per SM (table_len * page_size * num_heads / 128 / SMs; with head_dim 64 the pairs
+ * counted as heads and a quarter of that many steps), the CUDA-core kernel otherwise (measured on GB300: the
  * tensor-core kernel is as fast or faster from about 150 steps per SM up, the CUDA-core one
  * on batches of few, short sequences).  HP_ATTN_TENSOR_CORES asks for the tensor-core
  * kernel wherever the shape allows it, HP_ATTN_CUDA_CORES for the CUDA-core kernel always.

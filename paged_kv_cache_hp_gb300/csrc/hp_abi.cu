@@ -693,8 +693,13 @@ bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
     int dev = 0;
     const int sms = hp::current_sms(&dev);
     if (sms == 0) return false;
+    // head_dim 64 (pairs) from a quarter of the steps: its CUDA-core kernel is the weaker
+    // (32 sequences, 8 K/V heads of G = 4, 103 steps per SM: 0.858 of the copy bandwidth on
+    // the tensor cores against 0.687; 64 sequences of 256-2048 tokens, 18 per SM: 62 us
+    // against 59)
     const u128 steps = (u128)d->table_len * d->page_size * hkv / 128;
-    return steps >= (u128)HP_ATTN_TC_MIN_STEPS * (u128)sms;
+    const u128 min_steps = attn_pairs(d, G) ? HP_ATTN_TC_MIN_STEPS / 4 : HP_ATTN_TC_MIN_STEPS;
+    return steps >= min_steps * (u128)sms;
 }
 
 // Floats of one segment record's value sums: head_dim, or 128 for head_dim 64 (a record of
