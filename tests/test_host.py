@@ -154,3 +154,19 @@ def test_whole_output_comparison_catches_one_wrong_byte(oracle):
         with pytest.raises(AssertionError, match="first at row %d" % bad_row):
             compare_whole_gather(oracle, w, pool, w.lens, lambda a, b: wrong[a:b],
                                  group_tokens=300)
+
+
+@pytest.mark.parametrize("name", ["prefix_sharing", "decode_gather"])
+def test_bench_physical_rows_brute_force(name):
+    """The pool row of every output token that the bench's generic-gather comparison reads
+    (bench.physical_rows) equals the Element Lookup taken token by token: page
+    block_table[seq_ptr[s] + t / P], slot t % P, for the small version of each batch."""
+    import bench
+    w = inputs.config(name, "small")
+    got = bench.physical_rows(w)
+    want = []
+    for s in range(w.num_seqs):
+        for t in range(int(w.lens[s])):
+            page = int(w.table[int(w.seq_ptr[s]) + t // w.page_size])
+            want.append(page * w.page_size + t % w.page_size)
+    assert got.tolist() == want
