@@ -142,19 +142,20 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * device memory only.  In the descriptor's `flags`, and in the `flags` argument of
  * hp_copy_pages, hp_lane_gather and hp_lane_append. */
 #define HP_HOST_MEMORY 0x4u
-/* Decode attention's kernel (no counterpart in the pages).  By default the library picks:
- * the tensor-core kernel when the shape allows it (head_dim 128, or 64 in pairs of K/V
- * heads, see hp_attention_decode; a power-of-two number of K/V heads; G = num_q_heads /
+/* Decode attention's kernel (no counterpart in the pages).  By default the library picks
+ * the tensor-core kernel when the shape allows it -- head_dim 128, or 64 in pairs of K/V
+ * heads (see hp_attention_decode); a power-of-two number of K/V heads; G = num_q_heads /
  * num_heads in {1, 2, 4, 8}; pages of a power of two from 8 to 128 / h slots, h the K/V
- * heads of one launch: at most 8, with at most 32 query heads, more K/V heads running as
- * groups of h, one launch each; device memory) and either G = 8 at head_dim 128 or, in at
- * most two launches, the batch has at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token)
- * rows per SM (table_len * page_size * num_heads / 128 / SMs; with head_dim 64 the pairs
- * counted as heads and a quarter of that many steps), the CUDA-core kernel otherwise (measured on GB300: the
- * tensor-core kernel is as fast or faster from about 150 steps per SM up, the CUDA-core one
- * on batches of few, short sequences).  HP_ATTN_TENSOR_CORES asks for the tensor-core
- * kernel wherever the shape allows it, HP_ATTN_CUDA_CORES for the CUDA-core kernel always.
- * The plan and the planned calls that follow it must carry the same flags. */
+ * heads of one launch (at most 8, with at most 32 query heads; more K/V heads run as groups
+ * of h, one launch each); device memory -- and either G = 8 at head_dim 128, or the batch
+ * has at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token) rows per SM (table_len *
+ * page_size * num_heads / 128 / SMs; for head_dim 64 the pairs count as heads and a
+ * quarter of that many steps suffices) and takes at most two launches.  Otherwise the
+ * CUDA-core kernel.  (Measured on GB300: the tensor-core kernel is the faster on batches
+ * of that size and at G = 8, the CUDA-core one on batches of few, short sequences.)
+ * HP_ATTN_TENSOR_CORES asks for the tensor-core kernel wherever the shape allows it,
+ * HP_ATTN_CUDA_CORES for the CUDA-core kernel always.  The plan and the planned calls that
+ * follow it must carry the same flags. */
 #define HP_ATTN_TENSOR_CORES 0x8u
 #define HP_ATTN_CUDA_CORES 0x10u
 #define HP_ATTN_TC_MIN_STEPS 128
