@@ -148,17 +148,19 @@ typedef enum hp_index_type { /* [HF] block_table_index_type; also the type of se
  * num_heads in {1, 2, 4, 8}; pages of a power of two from 8 to 128 / h slots, h the K/V
  * heads of one launch (at most 8, with at most 32 query heads; more K/V heads run as groups
  * of h, one launch each); device memory -- and either G = 8 at head_dim 128, or the batch
- * has at least HP_ATTN_TC_MIN_STEPS steps of 128 (head, token) rows per SM (table_len *
- * page_size * num_heads / 128 / SMs; for head_dim 64 the pairs count as heads and a
- * quarter of that many steps suffices) and takes at most two launches.  Otherwise the
- * CUDA-core kernel.  (Measured on GB300: the tensor-core kernel is the faster on batches
+ * takes at most two launches and has at least HP_ATTN_TC_MIN_STEPS steps of 128 (head,
+ * token) rows per SM (table_len * page_size * num_heads / 128 / SMs, pairs counting as
+ * heads for head_dim 64), a quarter of that when its sequences average
+ * HP_ATTN_TC_LONG_TOKENS slots of capacity (table_len * page_size / num_seqs) or more.
+ * Otherwise the CUDA-core kernel.  (Measured on GB300: the tensor-core kernel is the faster on batches
  * of that size and at G = 8, the CUDA-core one on batches of few, short sequences.)
  * HP_ATTN_TENSOR_CORES asks for the tensor-core kernel wherever the shape allows it,
  * HP_ATTN_CUDA_CORES for the CUDA-core kernel always.  The plan and the planned calls that
  * follow it must carry the same flags. */
 #define HP_ATTN_TENSOR_CORES 0x8u
 #define HP_ATTN_CUDA_CORES 0x10u
-#define HP_ATTN_TC_MIN_STEPS 128
+#define HP_ATTN_TC_MIN_STEPS 32
+#define HP_ATTN_TC_LONG_TOKENS 2048
 /* Test hook for the bounded waits (no counterpart in the pages): the TMA copy engine sets
  * up the first load of each of its CTAs but never issues it, so the wait for it runs out
  * (after about 2 s), the call stores HP_ERR_TIMEOUT in *d_status and returns without

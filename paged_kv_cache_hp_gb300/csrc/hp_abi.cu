@@ -675,7 +675,7 @@ u64 attn_tc_group(const hp_paged_desc* d, u64 G)
 // default head_dim 128 with G = 8 always (the CUDA-core kernel reaches 0.32-0.50 of the copy
 // bandwidth there, the tensor-core one 0.53-0.90, and small batches are faster too), every
 // other shape in at most two launches and only on batches with at least
-// HP_ATTN_TC_MIN_STEPS such steps per SM.  The plan and the planned call decide alike, from
+// HP_ATTN_TC_MIN_STEPS such steps per SM (a quarter as many for long sequences).  The plan and the planned call decide alike, from
 // the descriptor and the query heads alone.
 bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
 {
@@ -693,12 +693,16 @@ bool attn_on_tensor_cores(const hp_paged_desc* d, u64 G)
     int dev = 0;
     const int sms = hp::current_sms(&dev);
     if (sms == 0) return false;
-    // head_dim 64 (pairs) from a quarter of the steps: its CUDA-core kernel is the weaker
-    // (32 sequences, 8 K/V heads of G = 4, 103 steps per SM: 0.858 of the copy bandwidth on
-    // the tensor cores against 0.687; 64 sequences of 256-2048 tokens, 18 per SM: 62 us
-    // against 59)
+    // HP_ATTN_TC_MIN_STEPS steps per SM, or a quarter of that when the sequences average
+    // HP_ATTN_TC_LONG_TOKENS of capacity or more (measured on GB300, 32 sequences of 1K-32K
+    // tokens: 4 K/V heads of G = 4, 103 steps per SM, 0.896 of the copy bandwidth on the
+    // tensor cores against 0.808; 1 K/V head of G = 4, 26 per SM, 0.592 against 0.438;
+    // head_dim 64 in pairs, 8 K/V heads of G = 4, 103 per SM, 0.858 against 0.687; but 256
+    // sequences of 64-512 tokens, 31 per SM, 80 us against 76 on the CUDA cores)
     const u128 steps = (u128)d->table_len * d->page_size * hkv / 128;
-    const u128 min_steps = attn_pairs(d, G) ? HP_ATTN_TC_MIN_STEPS / 4 : HP_ATTN_TC_MIN_STEPS;
+    const u128 cap = d->num_seqs ? (u128)d->table_len * d->page_size / d->num_seqs : 0;
+    const u128 min_steps =
+        cap >= HP_ATTN_TC_LONG_TOKENS ? HP_ATTN_TC_MIN_STEPS / 4 : HP_ATTN_TC_MIN_STEPS;
     return steps >= min_steps * (u128)sms;
 }
 
